@@ -1,0 +1,439 @@
+"""Pins that tie the CPU oracle to facts outside itself.
+
+Each ``check_*`` function takes an oracle library handle (the real one, or a
+deliberately broken copy built by ``test_oracle_mutants.py``) and raises
+AssertionError when the oracle disagrees with:
+  * the other of the two forms the memra mla.rs source proves equal
+    (naive per-head decompression vs the absorbed form, fns mla_attend_naive
+    and mla_attend_absorbed, and its unit tests);
+  * brute force in f64 on tiny inputs, and torch's scaled-dot-product
+    attention (a library routine that the T=1 decode reduces to);
+  * closed forms (empty request, one key, identical keys, zero scale, a
+    hand-worked two-key example stored under tests/golden/);
+  * structural invariants (split + LSE combine equals the unsplit result;
+    paged equals contiguous; unused rows never read);
+  * the rope facts of the mla.rs rope section (interleaved rope followed by
+    the load-time permutation equals the permutation followed by NEOX rope,
+    and roped dot products agree), and the scale of the NoPE geometry.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ------------------------------------------------------------------ helpers
+def uniform_case(rng, H, Dn, P, Dv, R, t_q, t_kv):
+    """Inputs in the style of the mla.rs unit tests: uniform [-1, 1) values,
+    weights scaled by 1/sqrt(kv_rank)."""
+    ws = 1.0 / math.sqrt(R)
+    u = lambda *s: rng.uniform(-1.0, 1.0, size=s).astype(np.float32)
+    return (u(t_q, H, Dn), u(t_q, H, P), u(t_kv, R), u(t_kv, P),
+            (u(H, Dn, R) * ws).astype(np.float32), (u(H, Dv, R) * ws).astype(np.float32))
+
+
+def maxdiff(a, b):
+    return float(np.max(np.abs(np.asarray(a, np.float64) - np.asarray(b, np.float64))))
+
+
+def rel_ok(ref, got, tol):
+    scale = max(float(np.max(np.abs(ref))), 1.0)
+    return maxdiff(ref, got) <= tol * scale
+
+
+def page(rows_f32, seq_lens, rng, bs=16, spare=3, poison=1e30):
+    """Scatter per-request contiguous rows into a shuffled paged pool.
+
+    rows_f32: list of [S_b, W] arrays. Returns (cache, block_table)."""
+    nblk = [-(-r.shape[0] // bs) for r in rows_f32]
+    W = rows_f32[0].shape[1] if rows_f32 else 1
+    pool = sum(nblk) + spare
+    perm = rng.permutation(pool).astype(np.int32)
+    cache = np.full((pool, bs, W), poison, np.float32)
+    bt = np.full((len(rows_f32), max(1, max(nblk) if nblk else 1)), -1, np.int32)
+    k = 0
+    for b, r in enumerate(rows_f32):
+        for i in range(nblk[b]):
+            blk = perm[k]
+            k += 1
+            bt[b, i] = blk
+            chunk = r[i * bs:(i + 1) * bs]
+            cache[blk, :chunk.shape[0]] = chunk
+    return cache, bt
+
+
+# ------------------------------------------------------------------ pins
+def check_naive_equals_absorbed(lib):
+    """mla.rs unit tests: both forms agree on several shapes, decode (t_q=1)
+    and causal prefill, to 1e-5 relative."""
+    rng = np.random.default_rng(7)
+    shapes = [(4, 24, 8, 32, 64), (2, 16, 16, 16, 32), (3, 12, 4, 20, 48),
+              (4, 32, 0, 32, 64), (3, 16, 0, 24, 48)]
+    for (H, Dn, P, Dv, R) in shapes:
+        for (t_q, t_kv) in [(1, 17), (5, 9), (3, 3)]:
+            args = uniform_case(rng, H, Dn, P, Dv, R, t_q, t_kv)
+            scale = 1.0 / math.sqrt(Dn + P)
+            a = oracle.attend_naive(*args, scale, lib=lib)
+            b = oracle.attend_absorbed(*args, scale, lib=lib)
+            assert np.all(np.isfinite(a)) and float(np.max(np.abs(a))) > 1e-6
+            assert rel_ok(a, b, 1e-5), (H, Dn, P, Dv, R, t_q, t_kv, maxdiff(a, b))
+
+
+def check_naive_equals_absorbed_full_dims(lib):
+    """mla.rs unit tests at full GLM-5.2 and GLM-5.3-Flash (NoPE) dims, 1e-4."""
+    rng = np.random.default_rng(20260801)
+    for (H, Dn, P, Dv, R, t_q, t_kv) in [(64, 192, 64, 256, 512, 1, 8),
+                                          (64, 256, 0, 256, 512, 1, 8),
+                                          (64, 256, 0, 256, 512, 4, 4)]:
+        args = uniform_case(rng, H, Dn, P, Dv, R, t_q, t_kv)
+        scale = 1.0 / math.sqrt(Dn + P)
+        a = oracle.attend_naive(*args, scale, lib=lib)
+        b = oracle.attend_absorbed(*args, scale, lib=lib)
+        assert rel_ok(a, b, 1e-4), (H, Dn, P, maxdiff(a, b))
+
+
+def _chain(lib, q_nope, q_pe, w_uk, w_uv, cache, bt, seq_lens, t_q, R, scale):
+    B = seq_lens.shape[0]
+    H = q_nope.shape[1]
+    q_abs = oracle.absorb_q(q_nope, q_pe, w_uk, lib=lib)
+    o, lse = oracle.decode_paged(q_abs.reshape(B, t_q, H, -1), cache, bt, seq_lens, t_q,
+                                 R, scale, lib=lib)
+    out = oracle.decompress(o.reshape(B * t_q, H, R), w_uv, lib=lib)
+    return q_abs, o, lse, out
+
+
+def check_paged_chain_equals_naive(lib):
+    """absorb -> paged decode (shuffled blocks, poisoned spare rows) ->
+    decompress equals the naive form on each request's contiguous cache."""
+    rng = np.random.default_rng(11)
+    for (H, Dn, P, Dv, R, t_q, lens) in [(4, 16, 8, 16, 32, 1, [37, 64, 5]),
+                                         (3, 12, 4, 20, 48, 3, [19, 3, 33]),
+                                         (2, 16, 0, 24, 32, 2, [17, 40])]:
+        W = R + P
+        B = len(lens)
+        scale = 1.0 / math.sqrt(Dn + P)
+        per_req = [uniform_case(rng, H, Dn, P, Dv, R, t_q, s) for s in lens]
+        w_uk, w_uv = per_req[0][4], per_req[0][5]
+        rows = [np.concatenate([c[2], c[3]], axis=1) for c in per_req]
+        cache, bt = page(rows, np.array(lens), rng)
+        q_nope = np.concatenate([c[0] for c in per_req])
+        q_pe = np.concatenate([c[1] for c in per_req])
+        sl = np.array(lens, np.int32)
+        _, _, _, out = _chain(lib, q_nope, q_pe, w_uk, w_uv, cache, bt, sl, t_q, R, scale)
+        out = out.reshape(B, t_q, H, Dv)
+        for b, c in enumerate(per_req):
+            ref = oracle.attend_naive(c[0], c[1], c[2], c[3], w_uk, w_uv, scale, lib=lib)
+            assert rel_ok(ref, out[b], 2e-5), (H, Dn, P, b, maxdiff(ref, out[b]))
+
+
+def _bruteforce(q_abs_row, rows, R, scale):
+    s = (rows.astype(np.float64) @ q_abs_row.astype(np.float64)) * scale
+    m = s.max()
+    e = np.exp(s - m)
+    o = (e[:, None] * rows[:, :R].astype(np.float64)).sum(0) / e.sum()
+    return o, m + math.log(e.sum())
+
+
+def check_bruteforce_f64(lib):
+    """Direct f64 softmax over every visible row agrees with the single-pass
+    f32 decode, including causal rows and a request whose keys start in the
+    middle of a block table."""
+    rng = np.random.default_rng(3)
+    H, R, P, t_q = 3, 32, 8, 3
+    W = R + P
+    lens = [1, 16, 17, 50]
+    rows = [rng.standard_normal((s, W)).astype(np.float32) for s in lens]
+    cache, bt = page(rows, lens, rng)
+    q = rng.standard_normal((len(lens), t_q, H, W)).astype(np.float32)
+    sl = np.array(lens, np.int32)
+    scale = 0.3
+    lens_ok = [s for s in lens if s >= t_q]
+    o, lse, st = oracle.decode_paged(q, cache, bt, sl, t_q, R, scale, lib=lib,
+                                     allow_errors=True)
+    for b, s in enumerate(lens):
+        for t in range(t_q):
+            for h in range(H):
+                if s < t_q:  # a request shorter than t_q is invalid: empty result
+                    assert np.all(o[b, t, h] == 0) and lse[b, t, h] == -np.inf
+                    continue
+                vis = s - t_q + t + 1
+                ro, rl = _bruteforce(q[b, t, h], rows[b][:vis], R, scale)
+                assert maxdiff(ro, o[b, t, h]) <= 2e-6 * max(1.0, np.abs(ro).max())
+                assert abs(rl - lse[b, t, h]) <= 2e-6 * max(1.0, abs(rl))
+    assert st == -4  # the length-1 request is shorter than t_q
+    assert lens_ok
+
+
+def check_sdpa_reduction(lib):
+    """For t_q = 1 the decode is ordinary attention with K = the whole row and
+    V = its leading kv_rank columns: torch's SDPA (f64) on the gathered rows
+    gives the same output, and logsumexp of the scaled scores the same LSE."""
+    import torch
+    rng = np.random.default_rng(5)
+    H, R, P = 4, 32, 8
+    W = R + P
+    lens = [9, 40]
+    rows = [rng.standard_normal((s, W)).astype(np.float32) for s in lens]
+    cache, bt = page(rows, lens, rng)
+    q = rng.standard_normal((len(lens), 1, H, W)).astype(np.float32)
+    scale = 1.0 / math.sqrt(24)
+    o, lse = oracle.decode_paged(q, cache, bt, np.array(lens, np.int32), 1, R, scale, lib=lib)
+    for b, s in enumerate(lens):
+        qt = torch.from_numpy(q[b, 0].astype(np.float64))[None, :, None, :]   # [1,H,1,W]
+        kt = torch.from_numpy(rows[b].astype(np.float64))[None, None].expand(1, H, s, W)
+        vt = kt[..., :R]
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=scale)
+        ref = ref[0, :, 0, :].numpy()
+        ref_lse = torch.logsumexp((qt @ kt.transpose(-1, -2))[0, :, 0, :] * scale, -1).numpy()
+        assert maxdiff(ref, o[b, 0]) <= 3e-6, maxdiff(ref, o[b, 0])
+        assert maxdiff(ref_lse, lse[b, 0]) <= 3e-6
+
+
+def check_closed_forms(lib):
+    """Empty request, one key, identical keys, zero scale, and the hand-worked
+    two-key example in tests/golden/closed_form_decode.json."""
+    rng = np.random.default_rng(9)
+    R, P, H = 16, 4, 2
+    W = R + P
+    row = rng.standard_normal(W).astype(np.float32)
+    one = [row[None, :]]
+    same = [np.repeat(row[None, :], 23, 0)]
+    mixed = [rng.standard_normal((29, W)).astype(np.float32)]
+    q = rng.standard_normal((1, 1, H, W)).astype(np.float32)
+
+    # empty request: zero row, -inf LSE
+    cache, bt = page([np.zeros((0, W), np.float32)], [0], rng)
+    o, lse = oracle.decode_paged(q, cache, np.full((1, 1), -1, np.int32),
+                                 np.array([0], np.int32), 1, R, 0.5, lib=lib)
+    assert np.all(o == 0) and np.all(lse == -np.inf)
+
+    # one key: o = row[:R], lse = scale * q.row
+    cache, bt = page(one, [1], rng)
+    o, lse = oracle.decode_paged(q, cache, bt, np.array([1], np.int32), 1, R, 0.5, lib=lib)
+    for h in range(H):
+        assert maxdiff(o[0, 0, h], row[:R]) <= 1e-6
+        s = 0.5 * float(np.dot(q[0, 0, h].astype(np.float64), row.astype(np.float64)))
+        assert abs(lse[0, 0, h] - s) <= 1e-5 * max(1, abs(s))
+
+    # identical keys: o = row[:R], lse = s + ln S
+    cache, bt = page(same, [23], rng)
+    o, lse = oracle.decode_paged(q, cache, bt, np.array([23], np.int32), 1, R, 0.5, lib=lib)
+    for h in range(H):
+        assert maxdiff(o[0, 0, h], row[:R]) <= 2e-6 * max(1, np.abs(row).max())
+        s = 0.5 * float(np.dot(q[0, 0, h].astype(np.float64), row.astype(np.float64)))
+        assert abs(lse[0, 0, h] - (s + math.log(23))) <= 2e-5 * max(1, abs(s))
+
+    # zero scale: uniform weights, o = mean of rows, lse = ln S
+    cache, bt = page(mixed, [29], rng)
+    o, lse = oracle.decode_paged(q, cache, bt, np.array([29], np.int32), 1, R, 0.0, lib=lib)
+    mean = mixed[0][:, :R].astype(np.float64).mean(0)
+    for h in range(H):
+        assert maxdiff(o[0, 0, h], mean) <= 2e-6
+        assert abs(lse[0, 0, h] - math.log(29)) <= 1e-6
+
+    # hand-worked example
+    with open(os.path.join(GOLDEN, "closed_form_decode.json")) as f:
+        g = json.load(f)
+    for case in g["cases"]:
+        rows = np.array(case["rows"], np.float32)
+        Rc = case["kv_rank"]
+        qq = np.array(case["q"], np.float32).reshape(1, 1, 1, -1)
+        cache, bt = page([rows], [rows.shape[0]], rng, bs=case["block_size"])
+        o, lse = oracle.decode_paged(qq, cache, bt, np.array([rows.shape[0]], np.int32), 1,
+                                     Rc, case["scale"], lib=lib)
+        assert maxdiff(o[0, 0, 0], case["o"]) <= 1e-6, (case["name"], o[0, 0, 0])
+        assert abs(lse[0, 0, 0] - case["lse"]) <= 1e-6, (case["name"], lse[0, 0, 0])
+
+
+def check_split_combine(lib):
+    """Any split of the visible keys, merged by LSE, equals the unsplit
+    decode; an empty split carries no weight; all-empty gives 0 and -inf."""
+    rng = np.random.default_rng(21)
+    R, P = 32, 8
+    W = R + P
+    S = 70
+    rows = [rng.standard_normal((S, W)).astype(np.float32)]
+    cache, bt = page(rows, [S], rng)
+    q = rng.standard_normal(W).astype(np.float32)
+    full_o, full_l = oracle.decode_range(q, cache, bt[0], S, 1, 0, R, 0.4, 0, S, lib=lib)
+    for cuts in ([0, 35, 70], [0, 1, 2, 70], [0, 16, 16, 48, 70], [0, 69, 70]):
+        parts = [oracle.decode_range(q, cache, bt[0], S, 1, 0, R, 0.4, a, b, lib=lib)
+                 for a, b in zip(cuts[:-1], cuts[1:])]
+        o, l = oracle.combine(np.stack([p[0] for p in parts]),
+                              np.array([p[1] for p in parts], np.float32), lib=lib)
+        assert maxdiff(o, full_o) <= 2e-6 * max(1, np.abs(full_o).max()), cuts
+        assert abs(l - full_l) <= 2e-6 * max(1, abs(full_l)), cuts
+    o, l = oracle.combine(np.zeros((2, R), np.float32),
+                          np.array([-np.inf, -np.inf], np.float32), lib=lib)
+    assert np.all(o == 0) and l == -np.inf
+
+
+def check_paged_equals_contiguous(lib):
+    """The same rows under two different block layouts give bit-identical
+    results (same summation order), and unused rows are never read (poison
+    1e30 or NaN leaves every bit unchanged)."""
+    rng = np.random.default_rng(33)
+    R, P, H, t_q = 32, 8, 3, 2
+    W = R + P
+    lens = [33, 16, 2]
+    rows = [rng.standard_normal((s, W)).astype(np.float32) for s in lens]
+    q = rng.standard_normal((3, t_q, H, W)).astype(np.float32)
+    sl = np.array(lens, np.int32)
+    c1, bt1 = page(rows, lens, np.random.default_rng(1), poison=1e30)
+    c2, bt2 = page(rows, lens, np.random.default_rng(2), poison=np.nan, spare=9)
+    # identity layout: request b's blocks are consecutive
+    nb = [-(-s // 16) for s in lens]
+    c3 = np.full((sum(nb), 16, W), np.nan, np.float32)
+    bt3 = np.full((3, max(nb)), -1, np.int32)
+    k = 0
+    for b, r in enumerate(rows):
+        for i in range(nb[b]):
+            ch = r[i * 16:(i + 1) * 16]
+            c3[k, :ch.shape[0]] = ch
+            bt3[b, i] = k
+            k += 1
+    outs = [oracle.decode_paged(q, c, bt, sl, t_q, R, 0.25, lib=lib)
+            for c, bt in ((c1, bt1), (c2, bt2), (c3, bt3))]
+    for o, l in outs[1:]:
+        assert np.array_equal(o.view(np.uint32), outs[0][0].view(np.uint32))
+        assert np.array_equal(l.view(np.uint32), outs[0][1].view(np.uint32))
+
+
+def check_decode_rows_consistent(lib):
+    """Sampled-row decode returns exactly the rows of the full decode, for
+    f32 inputs and for bf16 patterns (whose f32 values are the upper half)."""
+    rng = np.random.default_rng(44)
+    R, P, H, t_q = 32, 8, 4, 2
+    W = R + P
+    lens = [20, 7]
+    rows = [rng.standard_normal((s, W)).astype(np.float32) for s in lens]
+    cache, bt = page(rows, lens, rng)
+    q = rng.standard_normal((2, t_q, H, W)).astype(np.float32)
+    sl = np.array(lens, np.int32)
+    o, l = oracle.decode_paged(q, cache, bt, sl, t_q, R, 0.2, lib=lib)
+    ids = np.array([0, 5, 9, 15], np.int64)
+    so, sl_ = oracle.decode_rows(q, cache, bt, sl, t_q, R, 0.2, ids, lib=lib)
+    assert np.array_equal(so, o.reshape(-1, R)[ids])
+    assert np.array_equal(sl_, l.reshape(-1)[ids])
+    # bf16 patterns: truncating to the upper half gives exact bf16 values
+    qb = (q.view(np.uint32) >> 16).astype(np.uint16)
+    cb = (cache.view(np.uint32) >> 16).astype(np.uint16)
+    qf = (qb.astype(np.uint32) << 16).view(np.float32)
+    cf = (cb.astype(np.uint32) << 16).view(np.float32)
+    ob, lb = oracle.decode_paged(qb, cb, bt, sl, t_q, R, 0.2, lib=lib)
+    of, lf = oracle.decode_paged(qf, cf, bt, sl, t_q, R, 0.2, lib=lib)
+    assert np.array_equal(ob, of) and np.array_equal(lb, lf)
+
+
+def check_invalid_requests(lib):
+    """Out-of-range block ids, a seq_len beyond the block-table row and a
+    non-empty request shorter than t_q are reported and give empty rows."""
+    rng = np.random.default_rng(55)
+    R, P = 16, 0
+    rows = [rng.standard_normal((20, R)).astype(np.float32)]
+    cache, bt = page(rows, [20], rng)
+    q = rng.standard_normal((1, 1, 1, R)).astype(np.float32)
+    bad = bt.copy()
+    bad[0, 1] = cache.shape[0]  # one past the pool
+    o, l, st = oracle.decode_paged(q, cache, bad, np.array([20], np.int32), 1, R, 1.0,
+                                   lib=lib, allow_errors=True)
+    assert st == -2 and np.all(o == 0) and l[0, 0, 0] == -np.inf
+    o, l, st = oracle.decode_paged(q, cache, bt, np.array([33], np.int32), 1, R, 1.0,
+                                   lib=lib, allow_errors=True)
+    assert st == -3 and np.all(o == 0)
+    q2 = rng.standard_normal((1, 4, 1, R)).astype(np.float32)
+    o, l, st = oracle.decode_paged(q2, cache, bt, np.array([3], np.int32), 4, R, 1.0,
+                                   lib=lib, allow_errors=True)
+    assert st == -4 and np.all(o == 0)
+
+
+def check_absorb_decompress_unit_weights(lib):
+    """With unit-vector weights the absorb copies q_nope into rank space and
+    the decompress picks single latent coordinates; the rope tail of q_abs is
+    q_pe itself."""
+    rng = np.random.default_rng(66)
+    H, Dn, R, P, Dv, rows = 3, 8, 12, 4, 5, 2
+    perm = [rng.permutation(R)[:Dn] for _ in range(H)]
+    w_uk = np.zeros((H, Dn, R), np.float32)
+    for h in range(H):
+        w_uk[h, np.arange(Dn), perm[h]] = 1.0
+    q_nope = rng.standard_normal((rows, H, Dn)).astype(np.float32)
+    q_pe = rng.standard_normal((rows, H, P)).astype(np.float32)
+    qa = oracle.absorb_q(q_nope, q_pe, w_uk, lib=lib)
+    for h in range(H):
+        expect = np.zeros((rows, R), np.float32)
+        expect[:, perm[h]] = q_nope[:, h]
+        assert np.array_equal(qa[:, h, :R], expect)
+        assert np.array_equal(qa[:, h, R:], q_pe[:, h])
+    sel = [rng.integers(0, R, size=Dv) for _ in range(H)]
+    w_uv = np.zeros((H, Dv, R), np.float32)
+    for h in range(H):
+        w_uv[h, np.arange(Dv), sel[h]] = 2.0
+    o_lat = rng.standard_normal((rows, H, R)).astype(np.float32)
+    out = oracle.decompress(o_lat, w_uv, lib=lib)
+    for h in range(H):
+        assert np.array_equal(out[:, h], 2.0 * o_lat[:, h][:, sel[h]])
+
+
+def check_rope_permutation(lib):
+    """mla.rs rope section: permute(interleaved(x)) == neox(permute(x))
+    elementwise to 1e-6 and roped dot products agree to 1e-4 relative, at
+    n=64, base 8e6, positions 0, 1, 17, 4096, 1e6; the permutation for n=8 is
+    [0, 4, 1, 5, 2, 6, 3, 7] and is a bijection for every even n."""
+    assert list(oracle.norm_to_neox_perm(8, lib=lib)) == [0, 4, 1, 5, 2, 6, 3, 7]
+    for n in (2, 4, 16, 64):
+        assert sorted(oracle.norm_to_neox_perm(n, lib=lib)) == list(range(n))
+    n, base = 64, 8_000_000.0
+    perm = oracle.norm_to_neox_perm(n, lib=lib)
+    rng = np.random.default_rng(99)
+    for pos in (0.0, 1.0, 17.0, 4096.0, 1_000_000.0):
+        x0 = rng.uniform(-1, 1, n).astype(np.float32)
+        y0 = rng.uniform(-1, 1, n).astype(np.float32)
+        xa = oracle.rope_interleaved(x0, pos, base, lib=lib)
+        xa_p = np.empty_like(xa)
+        xa_p[perm] = xa
+        xb_in = np.empty_like(x0)
+        xb_in[perm] = x0
+        xb = oracle.rope_neox(xb_in, pos, base, lib=lib)
+        assert maxdiff(xa_p, xb) <= 1e-6, pos
+        ya = oracle.rope_interleaved(y0, pos, base, lib=lib)
+        yb_in = np.empty_like(y0)
+        yb_in[perm] = y0
+        yb = oracle.rope_neox(yb_in, pos, base, lib=lib)
+        dn = float(np.dot(xa.astype(np.float64), ya))
+        dx = float(np.dot(xb.astype(np.float64), yb))
+        assert abs(dn - dx) <= 1e-4 * max(abs(dn), 1.0), pos
+
+
+def check_rope_against_rotation(lib):
+    """Each rope pairing is a rotation of its pairs by theta_j = pos *
+    base^(-2j/n): compared with an f64 rotation at small positions, and the
+    identity at position 0."""
+    from mla_latent_cache_absorbed_gb300 import workloads as wlmod
+    rng = np.random.default_rng(12)
+    n, base = 16, 10000.0
+    x = rng.standard_normal(n).astype(np.float32)
+    assert np.array_equal(oracle.rope_neox(x, 0.0, base, lib=lib), x)
+    assert np.array_equal(oracle.rope_interleaved(x, 0.0, base, lib=lib), x)
+    for pos in (1.0, 3.0, 40.0):
+        a = oracle.rope_neox(x, pos, base, lib=lib)
+        b = wlmod.apply_rope_neox(x, np.array(pos), base)
+        assert maxdiff(a, b) <= 2e-5, pos
+        a = oracle.rope_interleaved(x, pos, base, lib=lib)
+        b = wlmod.apply_rope_interleaved(x, np.array(pos), base)
+        assert maxdiff(a, b) <= 2e-5, pos
+
+
+QUICK_CHECKS = [check_naive_equals_absorbed, check_paged_chain_equals_naive,
+                check_bruteforce_f64, check_sdpa_reduction, check_closed_forms,
+                check_split_combine, check_paged_equals_contiguous,
+                check_decode_rows_consistent, check_invalid_requests,
+                check_absorb_decompress_unit_weights, check_rope_permutation,
+                check_rope_against_rotation]

@@ -1,0 +1,80 @@
+"""Planted mistakes in the oracle must trip at least one pin.
+
+Each case copies oracle/mla_oracle.c, applies one small textual change of the
+kind a careless restatement could make (a dropped term, a wrong sign, a wrong
+index or operand), builds the copy into a temporary library and runs every
+quick pin against it. The real oracle passes all pins (test_oracle_pins.py);
+each mutant must fail at least one. Every mutant keeps its reads in bounds.
+"""
+import os
+
+import pytest
+
+import oracle
+import pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "mla_oracle.c")
+
+# (id, original text, replacement, occurrence index)
+MUTANTS = [
+    ("absorb_drops_q_pe", "dst[kv_rank + j] = qp[j];", "dst[kv_rank + j] = 0.0f;", 0),
+    ("absorb_head0_weights", "const float* wuk = w_uk + (int64_t)h * d_nope * kv_rank;",
+     "const float* wuk = w_uk;", 0),
+    ("absorb_head0_query", "const float* qn = q_nope + ((int64_t)r * n_head + h) * d_nope;",
+     "const float* qn = q_nope + ((int64_t)r * n_head) * d_nope;", 0),
+    ("decode_drops_rope_term", "for (int d = 0; d < W; ++d)\n            qk +=",
+     "for (int d = 0; d < kv_rank; ++d)\n            qk +=", 0),
+    ("decode_no_scale", "qk *= scale;", "qk *= 1.0f;", 0),
+    ("decode_rescale_sign", "expf(m - m_new)", "expf(m_new - m)", 0),
+    ("decode_acc_not_rescaled", "acc[d] = acc[d] * rescale + p *", "acc[d] = acc[d] + p *", 0),
+    ("decode_l_not_rescaled", "l = l * rescale + p;", "l = l + p;", 0),
+    ("decode_v_reversed", "p * load_elem(kv_cache, kv_dtype, entry + d);",
+     "p * load_elem(kv_cache, kv_dtype, entry + W - 1 - d);", 0),
+    ("decode_horizon_off_by_one", "horizon = seq_len - t_q + t + 1;",
+     "horizon = seq_len - t_q + t;", 0),
+    ("decode_row_in_block_reversed", "(j % block_size)) * W;",
+     "(block_size - 1 - j % block_size)) * W;", 0),
+    ("decode_lse_no_log", "*lse_out = l > 0.0f ? m + logf(l) : -INFINITY;",
+     "*lse_out = l > 0.0f ? m + l : -INFINITY;", 0),
+    ("decode_wrong_table_row", "block_table + (int64_t)b * max_blocks", "block_table", 0),
+    ("bf16_wrong_shift", "[i] << 16;", "[i] << 15;", 0),
+    ("combine_weight_sign", "expf(lse_parts[s] - M)", "expf(M - lse_parts[s])", 0),
+    ("combine_lse_no_log", "*lse_out = M + logf(wsum);", "*lse_out = M;", 0),
+    ("decompress_reversed", "acc += wrow[l] * o[l];", "acc += wrow[l] * o[kv_rank - 1 - l];", 0),
+    ("naive_drops_rope_term", "for (int p = 0; p < dr; ++p) s += qp[p] * k_pe[(int64_t)t * dr + p];",
+     "for (int p = 0; p < dr; ++p) s += 0.0f;", 0),
+    ("absorbed_form_drops_rope_term",
+     "for (int p = 0; p < dr; ++p) s += qp[p] * k_pe[(int64_t)t * dr + p];",
+     "for (int p = 0; p < dr; ++p) s += 0.0f;", 1),
+    ("naive_v_uses_w_uk", "acc += wuv[(int64_t)j * r + l] * c[l];",
+     "acc += wuk[(int64_t)(j % dn) * r + l] * c[l];", 0),
+    ("rope_neox_sign", "x[j + half] = a * s + b * c;", "x[j + half] = a * s - b * c;", 0),
+    ("rope_interleaved_pair", "x[2 * j + 1] = a * s + b * c;", "x[2 * j + 1] = b * c;", 0),
+    ("perm_wrong", "perm[2 * j + 1] = j + half;", "perm[2 * j + 1] = n_dims - 1 - j;", 0),
+]
+
+
+def _mutate(text, old, new, occurrence):
+    idx = -1
+    for _ in range(occurrence + 1):
+        idx = text.find(old, idx + 1)
+        assert idx >= 0, f"mutation anchor not found: {old!r}"
+    return text[:idx] + new + text[idx + len(old):]
+
+
+@pytest.mark.parametrize("mid,old,new,occ", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, mid, old, new, occ):
+    with open(SRC) as f:
+        text = f.read()
+    mutated = _mutate(text, old, new, occ)
+    assert mutated != text
+    src = tmp_path / f"{mid}.c"
+    src.write_text(mutated)
+    lib = oracle.load(oracle.build(str(src), str(tmp_path / f"lib{mid}.so")))
+    failed = []
+    for check in pins.QUICK_CHECKS:
+        try:
+            check(lib)
+        except (AssertionError, oracle.OracleError):
+            failed.append(check.__name__)
+    assert failed, f"mutant {mid} passed every pin"
