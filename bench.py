@@ -1,0 +1,459 @@
+#!/usr/bin/env python3
+"""Benchmark of the absorbed MLA decode hot path on GB300.
+
+One step = one pass of the whole path (absorb -> paged decode with split
+combine -> decompress) over one batch of the workload, as one decoding layer
+would run it. Default workload: GLM-5.2 dims decode (H=64, d_nope 192, d_rope
+64, d_v 256, kv_rank 512, bf16, batch 8, seq_lens U[1,4096] with one empty
+request, 16-row blocks). The KV cache stays resident in HBM (it is the
+server's state); each layer of a model has its own cache, so the benchmark
+cycles through NL distinct layers (own cache and weights, shared block table)
+whose total exceeds 4x the L2 size: every step reads its operands from HBM.
+
+Prints ONE JSON line (rank 0). --impl reference runs the CPU oracle instead,
+on a bounded sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode tokens/s/GPU & µs/layer; % of max(HBM, bf16-tensor) roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ---------------------------------------------------------------- workload facts
+def algorithmic(wl):
+    """Algorithmic bytes and flops of one step (per unit definitions).
+
+    decode bytes = cache rows read once per request (sum S_b * W * e)
+                 + q_abs (B*T*H*W*e) + o_lat (B*T*H*R*e) + lse (B*T*H*4)
+    decode flops = 2 * H * sum over query rows of visible keys * (W + R)
+    absorb bytes = w_uk + q_nope + q_pe + q_abs;  flops 2*B*T*H*Dn*R
+    decompress   = w_uv + o_lat + out;             flops 2*B*T*H*R*Dv
+    """
+    g = wl.geom
+    e = 2 if g.dtype == "bf16" else 4
+    H, R, W, T, Dn, Dv, P = g.n_head, g.kv_rank, g.width, g.t_q, g.d_nope, g.d_v, g.d_rope
+    S = wl.seq_lens.astype(np.int64)
+    rows = wl.rows
+    cache = int(S.sum()) * W * e
+    dec_bytes = cache + rows * H * W * e + rows * H * R * e + rows * H * 4
+    vis = 0
+    for s in S:
+        if s > 0:
+            vis += sum(int(s) - T + t + 1 for t in range(T))
+    dec_flops = 2 * H * vis * (W + R)
+    abs_bytes = H * Dn * R * e + rows * H * (Dn + P) * e + rows * H * W * e
+    abs_flops = 2 * rows * H * Dn * R
+    dcp_bytes = H * Dv * R * e + rows * H * R * e + rows * H * Dv * e
+    dcp_flops = 2 * rows * H * R * Dv
+    return {"decode": (dec_bytes, dec_flops), "absorb": (abs_bytes, abs_flops),
+            "decompress": (dcp_bytes, dcp_flops), "cache_bytes": cache}
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        self.proc.wait(timeout=5)
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for name, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- oracle (CPU) leg
+def oracle_sample(wl, budget_s: float, threads: int):
+    """Time the CPU oracle's full path on a bounded sample of query rows.
+
+    The absorb and decompress run on every row; the decode on a growing set
+    of query rows (spread over all requests and heads) until the budget is
+    used. Returns (tokens/s estimate for the whole step, description, threads).
+    """
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    from mla_latent_cache_absorbed_gb300 import workloads as W
+    g = wl.geom
+    H, R, T = g.n_head, g.kv_rank, g.t_q
+    lib = oracle.load()
+    t0 = time.perf_counter()
+    q_abs = oracle.absorb_q(wl.q_nope, wl.q_pe, wl.w_uk, lib=lib)
+    t_abs = time.perf_counter() - t0
+    q_abs = W.round_bf16(q_abs) if g.dtype == "bf16" else q_abs
+    q4 = q_abs.reshape(wl.batch, T, H, -1)
+    total_rows = wl.rows * H
+    rng = np.random.default_rng(0)
+    order = rng.permutation(total_rows)
+    chunk = max(1, min(64, total_rows // max(1, threads)))
+    done = 0
+    t0 = time.perf_counter()
+
+    def work(ids):
+        oracle.decode_rows(q4, wl.kv_cache, wl.block_table, wl.seq_lens, T, R, wl.scale,
+                           ids, lib=lib, allow_errors=True)
+
+    with ThreadPoolExecutor(threads) as ex:
+        while done < total_rows and time.perf_counter() - t0 < budget_s:
+            batch = [order[done + i * chunk: done + (i + 1) * chunk] for i in range(threads)]
+            batch = [b for b in batch if b.size]
+            list(ex.map(work, batch))
+            done += sum(b.size for b in batch)
+    t_dec = time.perf_counter() - t0
+    frac = done / total_rows
+    o_in = np.zeros((wl.rows, H, R), np.float32)
+    t0 = time.perf_counter()
+    oracle.decompress(o_in, wl.w_uv, lib=lib)
+    t_dcp = time.perf_counter() - t0
+    t_step = t_abs + t_dec / frac + t_dcp
+    desc = (f"absorb and decompress on all {wl.rows} query rows x {H} heads; decode on "
+            f"{done} of {total_rows} (query row, head) pairs ({100 * frac:.2f}%), "
+            f"extrapolated to the whole step")
+    return wl.rows / t_step, desc, threads, t_step
+
+
+def run_reference(args, wl):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    threads = os.cpu_count() or 1
+    vals = []
+    desc = ""
+    budget = max(2.0, min(20.0, 60.0 / max(1, args.steps + args.warmup)))
+    for i in range(args.warmup + args.steps):
+        v, desc, threads, t_step = oracle_sample(wl, budget, threads)
+        if i >= args.warmup:
+            vals.append(t_step)
+    t = statistics.mean(vals)
+    value = wl.rows / t
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_dict(wl, world=1),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def config_dict(wl, world):
+    g = wl.geom
+    return {"workload": f"{wl.name}: H={g.n_head} d_nope={g.d_nope} d_rope={g.d_rope} "
+                        f"d_v={g.d_v} kv_rank={g.kv_rank} t_q={g.t_q} {g.dtype} "
+                        f"batch={wl.batch} block=16",
+            "batch": wl.batch, "t_q": g.t_q,
+            "seq_lens_sum": int(wl.seq_lens.sum()), "seq_lens_max": int(wl.seq_lens.max()),
+            "l2": "inputs larger than L2: steps cycle through distinct per-layer caches and "
+                  "weights totalling > 4x L2",
+            "parallelism": f"replicas x{world} (requests shard, no collective)"}
+
+
+# ---------------------------------------------------------------- GPU leg
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+    from mla_latent_cache_absorbed_gb300 import _native as N
+    from mla_latent_cache_absorbed_gb300 import device as D
+    from mla_latent_cache_absorbed_gb300 import workloads as W
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    N.load()
+    g = wl.geom
+    peaks, peaks_src = load_peaks()
+
+    # layers: distinct caches / weights / queries, shared block table
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    per_layer = (wl.kv_cache.nbytes + wl.w_uk.nbytes // 2 + wl.w_uv.nbytes // 2)
+    nl = max(2, min(64, math.ceil(4 * l2 / max(1, per_layer))))
+    base = D.upload(wl, device=dev)
+    layers = [base]
+    for i in range(1, nl):
+        c = D.upload(wl, device=dev)  # same values, distinct memory
+        layers.append(c)
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
+
+    def step(k, which="all"):
+        c = layers[k % nl]
+        if which in ("all", "absorb"):
+            D.absorb(c, stream)
+        if which in ("all", "decode"):
+            D.decode(c, stream)
+        if which in ("all", "decompress"):
+            D.decompress(c, stream)
+
+    # eager warm-up (one-time setup of the library happens outside capture)
+    for k in range(max(3, args.warmup)):
+        step(k)
+    torch.cuda.synchronize()
+
+    def capture(n, which="all"):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for k in range(n):
+                step(k, which)
+        return gr
+
+    g_full = capture(nl)
+
+    def replay(graph_full, n_steps, graph_rem_cache):
+        full, rem = divmod(n_steps, nl)
+        for _ in range(full):
+            graph_full.replay()
+        if rem:
+            if rem not in graph_rem_cache:
+                graph_rem_cache[rem] = capture(rem, graph_rem_cache["which"])
+            graph_rem_cache[rem].replay()
+
+    rem_all = {"which": "all"}
+    # timing probe to choose K when not given
+    replay(g_full, nl, rem_all)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    replay(g_full, 4 * nl, rem_all)
+    torch.cuda.synchronize()
+    est = (time.perf_counter() - t0) / (4 * nl)
+    steps = args.steps if args.steps else int(min(200000, max(100, 2.0 / max(est, 1e-7))))
+    warmup = max(3, args.warmup)
+
+    replay(g_full, warmup, rem_all)
+    if steps % nl and (steps % nl) not in rem_all:
+        rem_all[steps % nl] = capture(steps % nl)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    sampler = ClockSampler(local)
+    sampler.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    replay(g_full, steps, rem_all)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms_total = ev0.elapsed_time(ev1)
+    clocks = sampler.stop()
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+        dist.barrier()
+    ms_per_step = ms_total / steps
+    tokens = wl.rows * world * steps
+    value = tokens / (ms_total / 1e3)
+
+    # per-stage kernel times (same layers, same launch configuration)
+    stage_ms = {}
+    for which in ("absorb", "decode", "decompress"):
+        gs = capture(nl, which)
+        rem = {"which": which}
+        n = max(nl, min(steps, 20 * nl))
+        replay(gs, nl, rem)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        replay(gs, n, rem)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        stage_ms[which] = e0.elapsed_time(e1) / n
+    alg = algorithmic(wl)
+    dominant = max(stage_ms, key=stage_ms.get)
+    dom_bytes, dom_flops = alg[dominant]
+    dom_s = stage_ms[dominant] / 1e3
+    hbm_peak = peaks["hbm_gbs"]
+    tc_peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    t_hbm = dom_bytes / (hbm_peak * 1e9)
+    t_tc = dom_flops / (tc_peak * 1e12)
+    if t_tc > t_hbm:
+        roof = {"bound": "tensor", "achieved": dom_flops / dom_s / 1e12, "peak": tc_peak,
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": dom_bytes / dom_s / 1e9, "peak": hbm_peak,
+                "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = dominant
+    roof["peak_source"] = f"{peaks_src} (MEASURED_PEAKS.json)" if peaks_src == "measured" \
+        else "fallback (profiling recipe)"
+    dec_bytes, dec_flops = alg["decode"]
+    dec_s = stage_ms["decode"] / 1e3
+    t_roof = max(dec_bytes / (hbm_peak * 1e9), dec_flops / (tc_peak * 1e12))
+    decode_roofline = {"us_per_layer": stage_ms["decode"] * 1e3,
+                       "roofline_us": t_roof * 1e6, "frac": t_roof / dec_s,
+                       "bytes": dec_bytes, "flops": dec_flops}
+
+    # end to end through the C ABI with host buffers
+    e2e = run_e2e(args, wl, layers, stream, nl, steps)
+
+    # CPU baseline (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, desc, threads, _ = oracle_sample(wl, args.cpu_budget, os.cpu_count() or 1)
+        cpu = {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": desc}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": steps, "warmup": warmup, "ms_per_step": ms_per_step,
+            "us_per_layer": ms_per_step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if g.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": config_dict(wl, world),
+            "roofline": roof, "decode_roofline": decode_roofline,
+            "stages_ms": stage_ms, "e2e": e2e, "cpu_baseline": cpu,
+            "gpu_launches": steps * LAUNCHES_PER_STEP(wl),
+            "clocks": clocks, "layers": nl,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def LAUNCHES_PER_STEP(wl):
+    """Kernels of this library launched per step: absorb (1), decode (split
+    kernel + combine kernel), decompress (1)."""
+    return 4
+
+
+def run_e2e(args, wl, layers, stream, nl, steps):
+    """Same metric through the C ABI with the step's inputs in pinned host
+    memory: per step, copy q_nope, q_pe, block_table and seq_lens in, run the
+    path, copy the output out (the cache is resident server state)."""
+    import torch
+    from mla_latent_cache_absorbed_gb300 import device as D
+    g = wl.geom
+    tdt = torch.bfloat16 if g.dtype == "bf16" else torch.float32
+    hq_nope = torch.from_numpy(wl.q_nope).to(tdt).pin_memory()
+    hq_pe = torch.from_numpy(wl.q_pe).to(tdt).pin_memory()
+    hbt = torch.from_numpy(wl.block_table).pin_memory()
+    hsl = torch.from_numpy(wl.seq_lens).pin_memory()
+    hout = torch.empty(tuple(layers[0].out.shape), dtype=tdt).pin_memory()
+    n = max(10, min(steps, 2000))
+
+    def one(k):
+        c = layers[k % nl]
+        c.q_nope.copy_(hq_nope, non_blocking=True)
+        c.q_pe.copy_(hq_pe, non_blocking=True)
+        c.block_table.copy_(hbt, non_blocking=True)
+        c.seq_lens.copy_(hsl, non_blocking=True)
+        D.full_step(c, stream)
+        hout.copy_(c.out, non_blocking=True)
+
+    for k in range(3):
+        one(k)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(n):
+        one(k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    h2d = hq_nope.nbytes + hq_pe.nbytes + hbt.nbytes + hsl.nbytes
+    d2h = hout.numel() * hout.element_size()
+    return {"value": wl.rows * n / (ms / 1e3), "unit": "tokens/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "steps": n, "ms_per_step": ms / n}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=0, help="timed steps (default: ~2 s worth)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="glm52_decode")
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle decode work in the CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from mla_latent_cache_absorbed_gb300 import workloads as W
+    rank, world, _ = dist_env()
+    wl = W.make_workload(args.config, seed=None if rank == 0 else 1000 + rank)
+    if args.impl == "reference":
+        if args.steps == 0:
+            args.steps = 3
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

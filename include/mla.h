@@ -1,0 +1,183 @@
+/*
+ * mla.h — C ABI of libmla_gb300: absorbed multi-head latent attention (MLA)
+ * decode over a paged latent KV cache, on one NVIDIA GB300 (sm_103a).
+ *
+ * The path (each entry point cites the passage that defines its operation):
+ *   mla_absorb_q        fold the query through W_UK into rank space
+ *   mla_decode_paged    all heads attend MQA-style to the shared cache rows
+ *                       [c_kv | k_pe], split over the keys, merged by LSE
+ *   mla_decompress_out  decompress the latent output once through W_UV
+ *   mla_rope_norm_to_neox_perm / mla_permute_rope_cols / mla_permute_rope_rows
+ *                       the host-side load-time rope permutation
+ *
+ * Conventions shared by every entry point:
+ *   - Device buffers are caller-owned, dense, row-major and 16-byte aligned.
+ *     The library allocates no device memory; decode scratch is passed in
+ *     (sized by mla_decode_workspace_size).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Device work is enqueued asynchronously; no call synchronises.
+ *   - Host-side validation failures return immediately and enqueue nothing;
+ *     mla_last_error() then describes the failure (thread-local).
+ *   - The GPU device current on the calling thread must be the one that owns
+ *     the buffers.
+ *   - Element types: MLA_F32 or MLA_BF16 for q, cache, weights and outputs;
+ *     the LSE is always f32. Accumulation is always f32.
+ *   - Results are deterministic: the same inputs on the same device give the
+ *     same bits (every reduction has a fixed order).
+ */
+#ifndef MLA_GB300_H
+#define MLA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mla_status {
+    MLA_OK = 0,
+    MLA_ERR_INVALID_ARG = 1,   /* bad pointer, size, alignment or geometry */
+    MLA_ERR_UNSUPPORTED = 2,   /* valid but not built (e.g. an unusual width) */
+    MLA_ERR_CUDA = 3,          /* a CUDA runtime call failed (see mla_last_error) */
+    MLA_ERR_DEVICE_BOUNDS = 4, /* reserved for callers mapping dev_err bits */
+    MLA_ERR_TIMEOUT = 5        /* reserved for callers mapping dev_err bits */
+} mla_status;
+
+typedef enum mla_dtype { MLA_F32 = 0, MLA_BF16 = 1 } mla_dtype;
+
+/*
+ * Head geometry ("memra_engine/mla.rs source", struct MlaDims) plus the decode
+ * query count and cache block size.
+ *   n_head      attention heads H
+ *   d_nope      qk no-position head dim (Dn)
+ *   d_rope      decoupled rope dim (P); 0 for the NoPE geometry
+ *   d_v         per-head decompressed V width (Dv)
+ *   kv_rank     latent rank R; a cache row is W = R + P wide
+ *   t_q         queries per request (1 for plain decode); the queries are the
+ *               last t_q positions of the request
+ *   block_size  cache rows per block; must be 16 ("vllm.v1...cpu_mla",
+ *               CPUMLABackend.get_supported_kernel_block_sizes)
+ *   dtype       mla_dtype of q, cache, weights and outputs
+ */
+typedef struct mla_dims {
+    int32_t n_head, d_nope, d_rope, d_v, kv_rank, t_q, block_size;
+    int32_t dtype;
+} mla_dims;
+
+/* Bits OR-ed into the optional device error word by mla_decode_paged. The
+ * affected query rows get a zero output row and LSE = -inf. */
+#define MLA_DEVERR_BAD_BLOCK 1u     /* a block id outside [0, num_blocks) */
+#define MLA_DEVERR_SEQ_TOO_LONG 2u  /* seq_len > max_blocks * block_size */
+#define MLA_DEVERR_SEQ_SHORT 4u     /* 0 < seq_len < t_q, or seq_len < 0 */
+#define MLA_DEVERR_TIMEOUT 8u       /* a bounded wait inside a kernel gave up */
+
+/*
+ * Absorb ("memra_engine/mla.rs source", fn mla_attend_absorbed, absorb step;
+ * "vllm.v1.attention.backends.mla.cpu_mla", CPUMLAImpl.forward_mqa, the
+ * concatenation of the absorbed query with q_pe):
+ *   q_abs[r][h][l]     = sum_p q_nope[r][h][p] * w_uk[h][p][l]   (l < R)
+ *   q_abs[r][h][R + j] = q_pe[r][h][j]                           (j < P)
+ * q_abs  [rows][H][R+P]   out, dims->dtype
+ * q_nope [rows][H][Dn]    in
+ * q_pe   [rows][H][P]     in; may be NULL only when P == 0
+ * w_uk   [H][Dn][R]       in
+ * rows = batch * t_q query rows. rows == 0 is a no-op.
+ */
+mla_status mla_absorb_q(void* q_abs, const void* q_nope, const void* q_pe,
+                        const void* w_uk, int32_t rows, const mla_dims* dims,
+                        void* stream);
+
+/*
+ * Scratch bytes mla_decode_paged needs for this batch shape on the current
+ * device (split-KV partial outputs and LSEs). The contents need no
+ * initialisation and are dead after the call's work completes on the stream.
+ */
+mla_status mla_decode_workspace_size(int32_t batch, int32_t max_blocks,
+                                     const mla_dims* dims, size_t* bytes);
+
+/*
+ * Paged decode ("vllm.cpp src/vt/cpu/cpu_mla_attn.cpp",
+ * MlaDecodeAttentionKernel; causal horizon from "memra_engine/mla.rs source",
+ * struct MlaInputs). For request b, query t < t_q and head h, with
+ * S = seq_lens[b] and horizon = S - t_q + t + 1:
+ *   row_j  = kv_cache[block_table[b][j / 16]][j % 16][0 : R+P]
+ *   s_j    = scale * (q_abs[b][t][h] . row_j)               j < horizon
+ *   out    = sum_j softmax(s)_j * row_j[0 : R]   (V = leading R of the row)
+ *   lse    = ln sum_j exp(s_j)                   (natural log, scaled scores)
+ * S == 0 gives a zero row and lse = -inf. The work is split over the keys and
+ * the partial results merged by their LSE (the split + combine pair named in
+ * the header of cpu_mla_attn.cpp).
+ *
+ * out         [B][t_q][H][R]         out, dims->dtype
+ * lse         [B][t_q][H] f32        out; may be NULL
+ * q_abs       [B][t_q][H][R+P]       in, dims->dtype
+ * kv_cache    [num_blocks][16][R+P]  in, dims->dtype
+ * block_table [B][max_blocks] int32  in; entries past ceil(S/16) are not read
+ * seq_lens    [B] int32              in
+ * scale       softmax scale; normally 1/sqrt(d_nope + d_rope)
+ *             ("memra_engine/mla.rs source", MlaDims::scale)
+ * workspace   >= mla_decode_workspace_size(batch, max_blocks, dims) bytes,
+ *             256-byte aligned, not shared with a concurrent call
+ * dev_err     optional device int32: MLA_DEVERR_* bits are OR-ed in when the
+ *             device data is invalid (the row is then zero / -inf); the
+ *             library never clears it
+ * Supported: R+P in {576, 512} with R == 512 for bf16 (the tensor-core
+ * path); any R <= 1024, R+P <= 1152 for f32.
+ */
+mla_status mla_decode_paged(void* out, float* lse, const void* q_abs,
+                            const void* kv_cache, const int32_t* block_table,
+                            const int32_t* seq_lens, int32_t batch,
+                            int32_t max_blocks, int32_t num_blocks,
+                            const mla_dims* dims, float scale, void* workspace,
+                            size_t workspace_bytes, int32_t* dev_err,
+                            void* stream);
+
+/*
+ * Decompress ("memra_engine/mla.rs source", fn mla_attend_absorbed,
+ * decompress step):
+ *   out[r][h][j] = sum_l w_uv[h][j][l] * o_lat[r][h][l]
+ * out   [rows][H][Dv]  out, dims->dtype
+ * o_lat [rows][H][R]   in, dims->dtype
+ * w_uv  [H][Dv][R]     in
+ */
+mla_status mla_decompress_out(void* out, const void* o_lat, const void* w_uv,
+                              int32_t rows, const mla_dims* dims, void* stream);
+
+/*
+ * Load-time rope permutation ("memra_engine/mla.rs source", fn
+ * norm_to_neox_perm): perm_out[src] = NEOX index of interleaved index src,
+ * pi(2j) = j, pi(2j+1) = j + n_dims/2. Host only. n_dims must be even, >= 0.
+ */
+mla_status mla_rope_norm_to_neox_perm(int32_t n_dims, int32_t* perm_out);
+
+/*
+ * Apply the permutation in place to the column span [col0, col0 + n_dims) of
+ * each of `rows` rows of a host matrix (row stride in elements):
+ * new[col0 + pi(i)] = old[col0 + i]. elem_bytes is 2 (bf16/f16) or 4 (f32).
+ * Used on activations whose rope features are laid out interleaved.
+ */
+mla_status mla_permute_rope_cols(void* x, int32_t elem_bytes, int64_t rows,
+                                 int64_t row_stride, int32_t col0,
+                                 int32_t n_dims);
+
+/*
+ * Apply the permutation in place to the rows [row0, row0 + n_dims) of a host
+ * row-major matrix whose rows are row_len elements long: new row row0 + pi(i)
+ * = old row row0 + i. This is the "rope rows of the projection weights at
+ * load" form of the same permutation.
+ */
+mla_status mla_permute_rope_rows(void* w, int32_t elem_bytes, int64_t row_len,
+                                 int32_t row0, int32_t n_dims);
+
+/* Static description of a status code. */
+const char* mla_status_str(mla_status status);
+
+/* Message of the last failing call on this thread ("" if none). */
+const char* mla_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_GB300_H */

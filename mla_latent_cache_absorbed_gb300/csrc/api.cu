@@ -1,0 +1,244 @@
+// C ABI of libmla_gb300 (declared in include/mla.h): argument validation,
+// status codes, workspace sizing and dispatch to the kernels.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <vector>
+
+#include "internal.h"
+#include "tc_decode.h"
+
+namespace mla {
+
+static thread_local char g_last_error[512] = "";
+
+void set_error(const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+}
+
+mla_status cuda_status(cudaError_t e, const char* what) {
+    set_error("%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+    return MLA_ERR_CUDA;
+}
+
+namespace {
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+mla_status check_dims(const mla_dims* d) {
+    if (!d) {
+        set_error("dims is NULL");
+        return MLA_ERR_INVALID_ARG;
+    }
+    if (d->n_head <= 0 || d->d_nope <= 0 || d->d_rope < 0 || d->d_v <= 0 ||
+        d->kv_rank <= 0 || d->t_q <= 0) {
+        set_error("dims: n_head, d_nope, d_v, kv_rank, t_q must be > 0 and d_rope >= 0 "
+                  "(got %d %d %d %d %d %d)", d->n_head, d->d_nope, d->d_rope, d->d_v,
+                  d->kv_rank, d->t_q);
+        return MLA_ERR_INVALID_ARG;
+    }
+    if (d->block_size != 16) {
+        set_error("dims: block_size must be 16 (got %d)", d->block_size);
+        return MLA_ERR_INVALID_ARG;
+    }
+    if (d->dtype != MLA_F32 && d->dtype != MLA_BF16) {
+        set_error("dims: dtype must be MLA_F32 or MLA_BF16 (got %d)", d->dtype);
+        return MLA_ERR_INVALID_ARG;
+    }
+    if (d->kv_rank > 1024 || d->kv_rank + d->d_rope > 1152 || d->d_nope > 1024 ||
+        d->d_v > 4096) {
+        set_error("dims: kv_rank <= 1024, kv_rank + d_rope <= 1152, d_nope <= 1024 and "
+                  "d_v <= 4096 are supported");
+        return MLA_ERR_UNSUPPORTED;
+    }
+    // every row of every operand must start on a 16-byte boundary
+    const int esz = d->dtype == MLA_F32 ? 4 : 2;
+    const int per16 = 16 / esz;
+    if (d->kv_rank % per16 || d->d_rope % per16 || d->d_nope % per16 || d->d_v % per16) {
+        set_error("dims: kv_rank, d_rope, d_nope and d_v must be multiples of %d for this "
+                  "dtype (16-byte rows)", per16);
+        return MLA_ERR_INVALID_ARG;
+    }
+    return MLA_OK;
+}
+
+#define REQUIRE(cond, ...)               \
+    do {                                 \
+        if (!(cond)) {                   \
+            set_error(__VA_ARGS__);      \
+            return MLA_ERR_INVALID_ARG;  \
+        }                                \
+    } while (0)
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+const char* mla_status_str(mla_status s) {
+    switch (s) {
+        case MLA_OK: return "MLA_OK";
+        case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG: invalid argument";
+        case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED: unsupported geometry";
+        case MLA_ERR_CUDA: return "MLA_ERR_CUDA: CUDA runtime error";
+        case MLA_ERR_DEVICE_BOUNDS: return "MLA_ERR_DEVICE_BOUNDS: invalid device data";
+        case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT: a device wait gave up";
+    }
+    return "unknown mla_status";
+}
+
+const char* mla_last_error(void) { return g_last_error; }
+
+mla_status mla_absorb_q(void* q_abs, const void* q_nope, const void* q_pe, const void* w_uk,
+                        int32_t rows, const mla_dims* dims, void* stream) {
+    g_last_error[0] = 0;
+    if (mla_status st = check_dims(dims)) return st;
+    REQUIRE(rows >= 0, "rows must be >= 0 (got %d)", rows);
+    if (rows == 0) return MLA_OK;
+    REQUIRE(q_abs && q_nope && w_uk, "q_abs, q_nope and w_uk must be non-NULL");
+    REQUIRE(q_pe || dims->d_rope == 0, "q_pe may be NULL only when d_rope == 0");
+    REQUIRE(aligned16(q_abs) && aligned16(q_nope) && aligned16(w_uk) &&
+                (!q_pe || aligned16(q_pe)),
+            "device buffers must be 16-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    if (dims->dtype == MLA_BF16 && tc_gemm_supported(*dims, rows, /*absorb=*/true)) {
+        MLA_CUDA_TRY(launch_absorb_tc(q_abs, q_nope, q_pe, w_uk, rows, *dims, s),
+                     "absorb (tensor cores)");
+        return MLA_OK;
+    }
+    MLA_CUDA_TRY(launch_absorb_simt(q_abs, q_nope, q_pe, w_uk, rows, *dims, s), "absorb");
+    return MLA_OK;
+}
+
+mla_status mla_decompress_out(void* out, const void* o_lat, const void* w_uv, int32_t rows,
+                              const mla_dims* dims, void* stream) {
+    g_last_error[0] = 0;
+    if (mla_status st = check_dims(dims)) return st;
+    REQUIRE(rows >= 0, "rows must be >= 0 (got %d)", rows);
+    if (rows == 0) return MLA_OK;
+    REQUIRE(out && o_lat && w_uv, "out, o_lat and w_uv must be non-NULL");
+    REQUIRE(aligned16(out) && aligned16(o_lat) && aligned16(w_uv),
+            "device buffers must be 16-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    if (dims->dtype == MLA_BF16 && tc_gemm_supported(*dims, rows, /*absorb=*/false)) {
+        MLA_CUDA_TRY(launch_decompress_tc(out, o_lat, w_uv, rows, *dims, s),
+                     "decompress (tensor cores)");
+        return MLA_OK;
+    }
+    MLA_CUDA_TRY(launch_decompress_simt(out, o_lat, w_uv, rows, *dims, s), "decompress");
+    return MLA_OK;
+}
+
+mla_status mla_decode_workspace_size(int32_t batch, int32_t max_blocks, const mla_dims* dims,
+                                     size_t* bytes) {
+    g_last_error[0] = 0;
+    if (mla_status st = check_dims(dims)) return st;
+    REQUIRE(bytes, "bytes must be non-NULL");
+    REQUIRE(batch >= 0 && max_blocks >= 1, "batch >= 0 and max_blocks >= 1 required");
+    if (dims->dtype == MLA_BF16 && tc_decode_supported(*dims)) {
+        size_t b = 0;
+        MLA_CUDA_TRY(tc_decode_workspace(batch, max_blocks, *dims, &b), "decode workspace");
+        *bytes = b;
+        return MLA_OK;
+    }
+    *bytes = simt_decode_plan(batch, max_blocks, *dims).bytes;
+    return MLA_OK;
+}
+
+mla_status mla_decode_paged(void* out, float* lse, const void* q_abs, const void* kv_cache,
+                            const int32_t* block_table, const int32_t* seq_lens,
+                            int32_t batch, int32_t max_blocks, int32_t num_blocks,
+                            const mla_dims* dims, float scale, void* workspace,
+                            size_t workspace_bytes, int32_t* dev_err, void* stream) {
+    g_last_error[0] = 0;
+    if (mla_status st = check_dims(dims)) return st;
+    REQUIRE(batch >= 0 && max_blocks >= 1 && num_blocks >= 1,
+            "batch >= 0, max_blocks >= 1 and num_blocks >= 1 required");
+    if (batch == 0) return MLA_OK;
+    REQUIRE(out && q_abs && kv_cache && block_table && seq_lens && workspace,
+            "out, q_abs, kv_cache, block_table, seq_lens and workspace must be non-NULL");
+    REQUIRE(aligned16(out) && aligned16(q_abs) && aligned16(kv_cache) &&
+                aligned16(block_table) && aligned16(seq_lens) && (!lse || aligned16(lse)),
+            "device buffers must be 16-byte aligned");
+    REQUIRE(((uintptr_t)workspace & 255u) == 0, "workspace must be 256-byte aligned");
+    REQUIRE(scale == scale, "scale is NaN");
+    size_t need = 0;
+    if (mla_status st = mla_decode_workspace_size(batch, max_blocks, dims, &need)) return st;
+    REQUIRE(workspace_bytes >= need, "workspace too small: %zu bytes given, %zu needed",
+            workspace_bytes, need);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (dims->dtype == MLA_BF16 && tc_decode_supported(*dims)) {
+        MLA_CUDA_TRY(launch_decode_tc(out, lse, q_abs, kv_cache, block_table, seq_lens, batch,
+                                      max_blocks, num_blocks, *dims, scale, workspace, dev_err,
+                                      s),
+                     "decode (tensor cores)");
+        return MLA_OK;
+    }
+    MLA_CUDA_TRY(launch_decode_simt(out, lse, q_abs, kv_cache, block_table, seq_lens, batch,
+                                    max_blocks, num_blocks, *dims, scale, workspace, dev_err,
+                                    s),
+                 "decode");
+    return MLA_OK;
+}
+
+mla_status mla_rope_norm_to_neox_perm(int32_t n_dims, int32_t* perm_out) {
+    g_last_error[0] = 0;
+    REQUIRE(n_dims >= 0 && n_dims % 2 == 0, "n_dims must be even and >= 0 (got %d)", n_dims);
+    REQUIRE(perm_out || n_dims == 0, "perm_out must be non-NULL");
+    const int32_t half = n_dims / 2;
+    for (int32_t j = 0; j < half; ++j) {
+        perm_out[2 * j] = j;
+        perm_out[2 * j + 1] = j + half;
+    }
+    return MLA_OK;
+}
+
+mla_status mla_permute_rope_cols(void* x, int32_t elem_bytes, int64_t rows, int64_t row_stride,
+                                 int32_t col0, int32_t n_dims) {
+    g_last_error[0] = 0;
+    REQUIRE(elem_bytes == 2 || elem_bytes == 4, "elem_bytes must be 2 or 4");
+    REQUIRE(rows >= 0 && col0 >= 0 && n_dims >= 0 && n_dims % 2 == 0,
+            "rows >= 0, col0 >= 0 and an even n_dims >= 0 required");
+    REQUIRE(row_stride >= (int64_t)col0 + n_dims, "row_stride must cover col0 + n_dims");
+    if (rows == 0 || n_dims == 0) return MLA_OK;
+    REQUIRE(x, "x must be non-NULL");
+    std::vector<int32_t> perm(n_dims);
+    mla_rope_norm_to_neox_perm(n_dims, perm.data());
+    std::vector<unsigned char> tmp((size_t)n_dims * elem_bytes);
+    unsigned char* base = (unsigned char*)x;
+    for (int64_t r = 0; r < rows; ++r) {
+        unsigned char* span = base + (r * row_stride + col0) * elem_bytes;
+        for (int32_t i = 0; i < n_dims; ++i)
+            memcpy(&tmp[(size_t)perm[i] * elem_bytes], span + (size_t)i * elem_bytes, elem_bytes);
+        memcpy(span, tmp.data(), tmp.size());
+    }
+    return MLA_OK;
+}
+
+mla_status mla_permute_rope_rows(void* w, int32_t elem_bytes, int64_t row_len, int32_t row0,
+                                 int32_t n_dims) {
+    g_last_error[0] = 0;
+    REQUIRE(elem_bytes == 2 || elem_bytes == 4, "elem_bytes must be 2 or 4");
+    REQUIRE(row_len >= 0 && row0 >= 0 && n_dims >= 0 && n_dims % 2 == 0,
+            "row_len >= 0, row0 >= 0 and an even n_dims >= 0 required");
+    if (row_len == 0 || n_dims == 0) return MLA_OK;
+    REQUIRE(w, "w must be non-NULL");
+    std::vector<int32_t> perm(n_dims);
+    mla_rope_norm_to_neox_perm(n_dims, perm.data());
+    const size_t rb = (size_t)row_len * elem_bytes;
+    std::vector<unsigned char> tmp(rb * n_dims);
+    unsigned char* base = (unsigned char*)w + (size_t)row0 * rb;
+    for (int32_t i = 0; i < n_dims; ++i) memcpy(&tmp[(size_t)perm[i] * rb], base + i * rb, rb);
+    memcpy(base, tmp.data(), tmp.size());
+    return MLA_OK;
+}
+
+}  // extern "C"

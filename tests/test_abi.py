@@ -1,0 +1,117 @@
+"""The C-ABI library loads, exports every declared symbol, and its host-side
+logic (validation, workspace sizing, the rope permutation) behaves, with no
+GPU and no kernel launch."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from mla_latent_cache_absorbed_gb300 import _native as N
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_symbols():
+    text = open(os.path.join(ROOT, "include", "mla.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:mla_status|const char\*)\s+(mla_\w+)\s*\(", text,
+                                 re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(N.LIB_PATH):
+        from mla_latent_cache_absorbed_gb300 import build
+        build.build()
+    return N.load()
+
+
+def test_exports_every_header_symbol(lib):
+    syms = header_symbols()
+    assert len(syms) >= 9
+    assert set(syms) == set(N.EXPORTS)
+    for s in syms:
+        assert getattr(lib, s) is not None
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert N.mla_status_str(s).startswith("MLA_")
+
+
+def test_rope_perm_matches_definition(lib):
+    assert list(N.mla_rope_norm_to_neox_perm(8)) == [0, 4, 1, 5, 2, 6, 3, 7]
+    for n in (0, 2, 64):
+        p = N.mla_rope_norm_to_neox_perm(n)
+        assert sorted(p) == list(range(n))
+        assert all(p[2 * j] == j and p[2 * j + 1] == j + n // 2 for j in range(n // 2))
+    with pytest.raises(N.MlaError):
+        N.mla_rope_norm_to_neox_perm(7)
+
+
+def test_rope_perm_agrees_with_oracle(lib):
+    import oracle
+    for n in (2, 8, 64):
+        assert np.array_equal(N.mla_rope_norm_to_neox_perm(n), oracle.norm_to_neox_perm(n))
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.uint16])
+def test_permute_rope_cols(lib, dtype):
+    x = np.arange(3 * 12).reshape(3, 12).astype(dtype)
+    orig = x.copy()
+    N.mla_permute_rope_cols(x, 4, 8)
+    perm = N.mla_rope_norm_to_neox_perm(8)
+    for r in range(3):
+        assert np.array_equal(x[r, :4], orig[r, :4])
+        for i in range(8):
+            assert x[r, 4 + perm[i]] == orig[r, 4 + i]
+
+
+def test_permute_rope_rows_matches_cols_on_transpose(lib):
+    """Permuting the rope rows of a weight W equals permuting the rope
+    columns of the activations x W^T it produces."""
+    rng = np.random.default_rng(0)
+    Wt = rng.standard_normal((10, 6)).astype(np.float32)  # [out_features, in]
+    x = rng.standard_normal((4, 6)).astype(np.float32)
+    y = x @ Wt.T
+    N.mla_permute_rope_cols(y, 2, 8)
+    W2 = Wt.copy()
+    N.mla_permute_rope_rows(W2, 2, 8)
+    assert np.allclose(x @ W2.T, y, atol=1e-6)
+
+
+def test_validation_without_launch(lib):
+    d = N.MlaDims(4, 16, 8, 16, 32, 1, 16, N.MLA_F32)
+    bad = N.MlaDims(4, 16, 8, 16, 32, 1, 32, N.MLA_F32)  # block size 32
+    with pytest.raises(N.MlaError) as e:
+        N.mla_absorb_q(0, 0, 0, 0, 2, bad, 0)
+    assert e.value.status == 1 and "block_size" in N.mla_last_error()
+    with pytest.raises(N.MlaError):
+        N.mla_absorb_q(0, 0, 0, 0, 2, d, 0)  # NULL buffers
+    with pytest.raises(N.MlaError):
+        N.mla_absorb_q(16, 16, 0, 16, 2, d, 0)  # q_pe NULL with d_rope > 0
+    with pytest.raises(N.MlaError):
+        N.mla_absorb_q(17, 16, 16, 16, 2, d, 0)  # misaligned
+    N.mla_absorb_q(0, 0, 0, 0, 0, d, 0)  # zero rows: no-op
+    odd = N.MlaDims(4, 16, 6, 16, 32, 1, 16, N.MLA_BF16)  # 12-byte rope rows
+    with pytest.raises(N.MlaError):
+        N.mla_decompress_out(16, 16, 16, 1, odd, 0)
+
+
+def test_decode_workspace_and_validation(lib):
+    d = N.MlaDims(4, 16, 8, 16, 32, 1, 16, N.MLA_F32)
+    n = N.mla_decode_workspace_size(2, 4, d)
+    assert n > 0
+    assert N.mla_decode_workspace_size(0, 4, d) >= 0
+    with pytest.raises(N.MlaError):
+        N.mla_decode_workspace_size(-1, 4, d)
+    with pytest.raises(N.MlaError) as e:  # workspace too small
+        N.mla_decode_paged(256, 0, 256, 256, 256, 256, 2, 4, 8, d, 0.2, 256, 16, None, 0)
+    assert "workspace" in str(e.value)
+    with pytest.raises(N.MlaError):  # misaligned workspace
+        N.mla_decode_paged(256, 0, 256, 256, 256, 256, 2, 4, 8, d, 0.2, 272, n, None, 0)
+    with pytest.raises(N.MlaError):  # NaN scale
+        N.mla_decode_paged(256, 0, 256, 256, 256, 256, 2, 4, 8, d, float("nan"), 256, n,
+                           None, 0)
+    N.mla_decode_paged(0, 0, 0, 0, 0, 0, 0, 4, 8, d, 0.2, 0, 0, None, 0)  # empty batch
