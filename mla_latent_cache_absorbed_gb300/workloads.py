@@ -277,8 +277,6 @@ def make_workload(name: str, seed: int | None = None, seq_lens=None,
     if bf16:
         q_nope, q_pe = round_bf16(q_nope), round_bf16(q_pe)
         w_uk, w_uv = round_bf16(w_uk), round_bf16(w_uv)
-        if rope == "norm":
-            q_pe_raw = round_bf16(q_pe_raw)
 
     poison_rows(cache, sl, bt, used, poison, bf16)
     return Workload(name=name, geom=g, scale=1.0 / math.sqrt(g.d_nope + g.d_rope),
