@@ -134,6 +134,38 @@ mla_status mla_decode_paged(void* out, float* lse, const void* q_abs,
                             void* stream);
 
 /*
+ * Bytes of the library-owned decode scratch used by mla_decode_paged_static.
+ * Every GPU on which the library's kernels are loaded reserves this much
+ * device memory for the life of the process.
+ */
+#define MLA_STATIC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * mla_decode_paged without a caller workspace. The pages have no counterpart:
+ * this entry point exists for callers that cannot allocate device memory when
+ * they decode (work recorded into CUDA graphs, serving loops whose allocator
+ * forbids cudaMalloc, plugin hosts that hand over only inputs and outputs).
+ * It computes exactly what mla_decode_paged computes, with the same arguments
+ * minus workspace / workspace_bytes; the split scratch lives in a static
+ * device array of MLA_STATIC_SCRATCH_BYTES. It allocates nothing.
+ *   - Returns MLA_ERR_INVALID_ARG (with mla_last_error() saying so) when the
+ *     batch needs more scratch than MLA_STATIC_SCRATCH_BYTES
+ *     (mla_decode_workspace_size tells the need); nothing is enqueued then.
+ *   - The first call on a device looks up the array's device address (and
+ *     loads the library's module there if needed); make that first call
+ *     before any stream capture on that device.
+ *   - All calls on a device share the array, which keeps the last call's
+ *     contents (nothing in it needs clearing between calls). Calls whose GPU
+ *     work overlaps race on it: issue them on one stream or order them.
+ */
+mla_status mla_decode_paged_static(void* out, float* lse, const void* q_abs,
+                                   const void* kv_cache, const int32_t* block_table,
+                                   const int32_t* seq_lens, int32_t batch,
+                                   int32_t max_blocks, int32_t num_blocks,
+                                   const mla_dims* dims, float scale,
+                                   int32_t* dev_err, void* stream);
+
+/*
  * Decompress ("memra_engine/mla.rs source", fn mla_attend_absorbed,
  * decompress step):
  *   out[r][h][j] = sum_l w_uv[h][j][l] * o_lat[r][h][l]

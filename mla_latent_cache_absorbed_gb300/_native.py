@@ -26,8 +26,9 @@ DEVERR_TIMEOUT = 8
 
 # Every exported symbol of include/mla.h.
 EXPORTS = ("mla_absorb_q", "mla_decode_workspace_size", "mla_decode_paged",
-           "mla_decompress_out", "mla_rope_norm_to_neox_perm", "mla_permute_rope_cols",
-           "mla_permute_rope_rows", "mla_status_str", "mla_last_error")
+           "mla_decode_paged_static", "mla_decompress_out", "mla_rope_norm_to_neox_perm",
+           "mla_permute_rope_cols", "mla_permute_rope_rows", "mla_status_str",
+           "mla_last_error")
 
 
 class MlaDims(ctypes.Structure):
@@ -67,6 +68,7 @@ def load(path: str = LIB_PATH):
     lib.mla_decode_workspace_size.argtypes = [I32, I32, D, ctypes.POINTER(ctypes.c_size_t)]
     lib.mla_decode_paged.argtypes = [P, P, P, P, P, P, I32, I32, I32, D, F, P,
                                      ctypes.c_size_t, P, P]
+    lib.mla_decode_paged_static.argtypes = [P, P, P, P, P, P, I32, I32, I32, D, F, P, P]
     lib.mla_decompress_out.argtypes = [P, P, P, I32, D, P]
     lib.mla_rope_norm_to_neox_perm.argtypes = [I32, P]
     lib.mla_permute_rope_cols.argtypes = [P, I32, I64, I64, I32, I32]
@@ -76,7 +78,8 @@ def load(path: str = LIB_PATH):
     lib.mla_last_error.argtypes = []
     lib.mla_last_error.restype = ctypes.c_char_p
     for name in ("mla_absorb_q", "mla_decode_workspace_size", "mla_decode_paged",
-                 "mla_decompress_out", "mla_rope_norm_to_neox_perm", "mla_permute_rope_cols",
+                 "mla_decode_paged_static", "mla_decompress_out",
+                 "mla_rope_norm_to_neox_perm", "mla_permute_rope_cols",
                  "mla_permute_rope_rows"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
@@ -131,6 +134,17 @@ def mla_decode_paged(out, lse, q_abs, kv_cache, block_table, seq_lens, batch: in
                                    num_blocks, ctypes.byref(dims), float(scale),
                                    _ptr(workspace), workspace_bytes, _ptr(dev_err),
                                    _stream(stream)))
+
+
+def mla_decode_paged_static(out, lse, q_abs, kv_cache, block_table, seq_lens, batch: int,
+                            max_blocks: int, num_blocks: int, dims: MlaDims, scale: float,
+                            dev_err=None, stream=None):
+    """mla_decode_paged with the library's static scratch (allocates nothing)."""
+    _check("mla_decode_paged_static",
+           load().mla_decode_paged_static(_ptr(out), _ptr(lse), _ptr(q_abs), _ptr(kv_cache),
+                                          _ptr(block_table), _ptr(seq_lens), batch, max_blocks,
+                                          num_blocks, ctypes.byref(dims), float(scale),
+                                          _ptr(dev_err), _stream(stream)))
 
 
 def mla_decompress_out(out, o_lat, w_uv, rows: int, dims: MlaDims, stream=None):
