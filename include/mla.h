@@ -138,7 +138,7 @@ mla_status mla_decode_paged(void* out, float* lse, const void* q_abs,
  * Every GPU on which the library's kernels are loaded reserves this much
  * device memory for the life of the process.
  */
-#define MLA_STATIC_SCRATCH_BYTES (32u << 20)
+#define MLA_STATIC_SCRATCH_BYTES (64u << 20)
 
 /*
  * mla_decode_paged without a caller workspace. The pages have no counterpart:

@@ -1,18 +1,1096 @@
-// Tensor-core path (not built yet: every geometry goes to the SIMT kernels).
+// Tensor-core paged decode for bf16 (sm_103a): tcgen05 MMAs with TMEM
+// accumulators, TMA-gathered cache blocks, a two-CTA cluster per work unit.
+//
+// What it computes is the paged single-pass decode of "vllm.cpp
+// cpu_mla_attn.cpp" (MlaDecodeAttentionKernel): per query row, softmax over
+// scale * (q_abs . row_j) for the visible keys and the latent output
+// sum_j p_j row_j[0:512] with its LSE; the split + combine pair named in that
+// page's header merges the partial results of a request split across CTAs.
+//
+// Layout of the work. The query rows of one request (t_q * n_head of them)
+// form row groups of 128 (the MMA M dimension); all rows share the same
+// cache rows, so heads are the M dimension and cache tokens the N (scores)
+// or K (P*V) dimension. A unit of work is (request, row group, 64-token
+// tile). A persistent grid of CTA pairs splits the unit sequence evenly.
+// In each pair:
+//   CTA 0 ("S-CTA") holds the 128 query rows in TMEM (A operand) and computes
+//     S = Q K^T for each tile (M=128, N=64, K=576 or 512) into TMEM, runs the
+//     online softmax (one thread per query row, lazy rescaling), and writes
+//     the bf16 probabilities P [128 x 64] into CTA 1's shared memory.
+//   CTA 1 ("O-CTA") holds O [128 x 512] f32 in all 512 TMEM columns and
+//     computes O += P V (M=128, N=2x256, K=64) with V the leading 512 columns
+//     of the same tile, delivered to both CTAs by one multicast TMA load.
+// The O accumulator alone fills a TMEM, so splitting the roles keeps both the
+// QK^T and the P*V contractions at M=128 with no repeated work; the only
+// exchange is P (16 KB per 64-token tile) plus per-row rescale factors.
+//
+// Every wait is bounded; on timeout the kernel records MLA_DEVERR_TIMEOUT,
+// drains its outstanding copies, frees TMEM and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "sm100.cuh"
 #include "tc_decode.h"
 
 namespace mla {
+namespace {
 
-bool tc_decode_supported(const mla_dims&) { return false; }
-cudaError_t tc_decode_workspace(int32_t, int32_t, const mla_dims&, size_t* bytes) {
-    *bytes = 0;
-    return cudaErrorNotSupported;
+using namespace sm100;
+
+constexpr int kTok = 64;                      // cache tokens per tile
+constexpr int kNS = 3;                        // pipeline stages
+constexpr int kChunk = 64 * 128;              // 64 tokens x 64 columns of bf16
+constexpr int kStage = 8 * kChunk;            // latent 512 columns of a tile
+constexpr int kSideOff = kNS * kStage;        // S-CTA: rope chunks; O-CTA: P slots
+constexpr int kPBytes = 128 * 128;            // P [128 rows x 64 tokens] bf16
+constexpr int kCtrlOff = kSideOff + 2 * kPBytes;
+constexpr int kQChunk = 128 * 128;            // 128 query rows x 64 columns of bf16
+constexpr int kVBlock = 8 * 2048;             // O-CTA: one block's V as [8 chunks][16 rows][128 B]
+// the first segment's queries sit in stages 1-2 (latent chunks 0..7) and in
+// the rope chunks of stages 1-2 (chunk 8); tile 0 uses stage 0 meanwhile
+__host__ __device__ constexpr int q_chunk_off(int cc) {
+    return cc < 8 ? kStage + cc * kQChunk : kSideOff + kChunk;
 }
-cudaError_t launch_decode_tc(void*, float*, const void*, const void*, const int32_t*,
-                             const int32_t*, int32_t, int32_t, int32_t, const mla_dims&, float,
-                             void*, int32_t*, cudaStream_t) {
-    return cudaErrorNotSupported;
+static_assert(kSideOff + kChunk + kQChunk <= kSideOff + 3 * kChunk, "q chunk 8 placement");
+constexpr int kThreads = 288;                 // see the role map in the kernel
+constexpr uint64_t kWaitLimit = 2000000000ull;  // ns before a wait gives up
+constexpr float kRescaleThreshold = 8.0f;     // lazy rescale, log2 units
+
+struct Ctrl {
+    uint64_t full[kNS];     // both: this CTA's part of the tile landed (complete_tx)
+    uint64_t empty[kNS];    // both: stage free (own QK / P*V commit)
+    uint64_t sfull[2];      // S: scores ready (QK commit)
+    uint64_t sfree[2];      // S: scores read (128 softmax threads)
+    uint64_t pempty[2];     // S: P slot consumed (O-CTA PV commit)
+    uint64_t qready;        // S: Q stored in TMEM (128 threads)
+    uint64_t qland;         // S: first segment's queries landed in shared memory (TMA)
+    uint64_t qfree;         // S: those queries are in TMEM; stages 1-2 reusable (128)
+    uint64_t statack;       // S: O-CTA has read the segment statistics (1 remote)
+    uint64_t pfull[2];      // O: P + alpha written (1 remote arrival per tile)
+    uint64_t vready[kNS];   // O: tile tail zeroed (fix warp)
+    uint64_t odone;         // O: all issued P*V complete (MMA commit)
+    uint64_t evt;           // O: MMA warp -> row warps event
+    uint64_t evtdone;       // O: row warps -> MMA warp (128)
+    uint64_t statfull;      // O: segment statistics written (1 remote)
+    uint64_t rowbar;        // both: barrier among the 128 row threads
+    uint32_t tmem_base;
+    int32_t abort;
+    int32_t evt_type;       // 1 = rescale slot evt_slot, 2 = segment epilogue
+    int32_t evt_slot;
+    int32_t flags[2][4];    // O: per softmax warp, some row needs a rescale
+    int32_t bad;            // O: the segment met an invalid block id
+    int32_t badw[4];        // S: per row warp, the segment met an invalid block id
+    float alpha[2][128];    // O: per-row rescale factors of the P slot
+    float mstat[128];       // O: segment max (log2 units) per row
+    float lstat[128];       // O: segment sum per row
+};
+constexpr int kSmemBytes = kCtrlOff + (int)sizeof(Ctrl);
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+struct Params {
+    const __nv_bfloat16* q_abs;   // [B][T][H][W]
+    const __nv_bfloat16* kv;      // [num_blocks][16][W]
+    const int32_t* block_table;   // [B][max_blocks]
+    const int32_t* seq_lens;      // [B]
+    __nv_bfloat16* out;           // [B][T][H][512]
+    float* lse;                   // [B][T][H] or null
+    float* ws_o;                  // [2*NP][128][512]
+    float* ws_lse;                // [2*NP][128]
+    int32_t* dev_err;
+    int B, T, H, W, max_blocks, num_blocks;
+    int NP, min_units;
+    float scale_log2;
+};
+
+// ------------------------------------------------------------------ schedule
+__device__ __forceinline__ int ntiles_of(int S, int T, int max_blocks) {
+    if (S <= 0 || S < T || S > max_blocks * 16) return 0;
+    return (S + kTok - 1) / kTok;
 }
+
+// Unit sequence: request b, then row group g, then tile. Every warp of both
+// CTAs computes the same walk.
+struct Walk {
+    int b, g, tile, ntiles, S;
+    long long u, u_end;
+    int G;
+};
+
+// Total units and this pair's range; warp-cooperative, identical result in
+// every lane. Returns false when the pair has no work.
+__device__ bool walk_init(const Params& p, int pair, Walk& w) {
+    const int lane = threadIdx.x & 31;
+    const int Mq = p.T * p.H;
+    const int G = (Mq + 127) / 128;
+    long long U = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+        const int b = b0 + lane;
+        long long v = b < p.B ? (long long)ntiles_of(p.seq_lens[b], p.T, p.max_blocks) * G : 0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        U += v;
+    }
+    int np = p.NP;
+    const long long cap = (U + p.min_units - 1) / p.min_units;
+    if (cap < np) np = (int)(cap > 0 ? cap : 1);
+    w.G = G;
+    if (pair >= np || U == 0) return false;
+    const long long ub = U * pair / np, ue = U * (pair + 1) / np;
+    if (ub >= ue) return false;
+    // locate unit ub
+    long long base = 0;
+    int found_b = -1;
+    long long found_base = 0;
+    for (int b0 = 0; b0 < p.B && found_b < 0; b0 += 32) {
+        const int b = b0 + lane;
+        long long v = b < p.B ? (long long)ntiles_of(p.seq_lens[b], p.T, p.max_blocks) * G : 0;
+        long long incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            long long t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, b < p.B && base + incl > ub);
+        if (hit) {
+            const int l = __ffs(hit) - 1;
+            found_b = b0 + l;
+            found_base = base + __shfl_sync(0xffffffffu, incl - v, l);
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    w.b = found_b;
+    w.S = p.seq_lens[found_b];
+    w.ntiles = ntiles_of(w.S, p.T, p.max_blocks);
+    const long long off = ub - found_base;
+    w.g = (int)(off / w.ntiles);
+    w.tile = (int)(off % w.ntiles);
+    w.u = ub;
+    w.u_end = ue;
+    return true;
+}
+
+// advance to the next unit (caller checks u < u_end first)
+__device__ __forceinline__ void walk_next(const Params& p, Walk& w) {
+    ++w.u;
+    if (w.u >= w.u_end) return;
+    if (++w.tile < w.ntiles) return;
+    w.tile = 0;
+    if (++w.g < w.G) return;
+    w.g = 0;
+    do {
+        ++w.b;
+        w.S = p.seq_lens[w.b];
+        w.ntiles = ntiles_of(w.S, p.T, p.max_blocks);
+    } while (w.ntiles == 0);
+}
+
+__device__ __forceinline__ bool seg_first(const Walk& w, long long ub) {
+    return w.u == ub || w.tile == 0;
+}
+__device__ __forceinline__ bool seg_last(const Walk& w) {
+    return w.u + 1 == w.u_end || w.tile + 1 == w.ntiles;
+}
+
+// ------------------------------------------------------------------ helpers
+struct Waiter {
+    volatile int32_t* abort;
+    int32_t* dev_err;
+    __device__ bool wait(uint32_t bar, uint32_t parity) {
+        if (mbar_try_wait(bar, parity)) return true;
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t i = 1;; ++i) {
+            if (mbar_try_wait(bar, parity)) return true;
+            if ((i & 255) == 0) {
+                if (*abort) return false;
+                if (globaltimer_ns() - t0 > kWaitLimit) break;
+            }
+        }
+        *abort = 1;
+        if (dev_err) atomicOr(dev_err, (int32_t)MLA_DEVERR_TIMEOUT);
+        return false;
+    }
+    // every lane of the warp waits; the result is the same in all lanes, so a
+    // timeout in one lane takes the whole warp out of the loop together
+    __device__ bool wait_warp(uint32_t bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, wait(bar, parity));
+    }
+};
+
+// Bounded barrier among the 128 row threads (warps 2..5) of one CTA; `phase`
+// counts the caller's uses. Returns false on timeout.
+__device__ __forceinline__ bool rows_sync(Waiter& wt, uint32_t bar, uint32_t& phase) {
+    mbar_arrive(bar);
+    return wt.wait_warp(bar, (phase++) & 1);
+}
+
+__device__ __forceinline__ int valid_blocks(const Walk& w) {
+    const int rem = w.S - w.tile * kTok;
+    const int nb = (rem + 15) / 16;
+    return nb < 4 ? nb : 4;
+}
+
+// ------------------------------------------------------------------ kernel
+// Role map (9 warps per CTA):
+//   S-CTA  warps 0-3  K loaders: warp k brings block k of each tile (3-D boxes)
+//          warp 4     S = Q K^T MMA issuer; owns the TMEM allocation
+//          warps 5-8  softmax, one query row per thread
+//   O-CTA  warp 0     V loader: one 4-D box per cache block
+//          warp 1     V landing: zeroes rows past the request, releases the stage
+//          warp 4     O += P V MMA issuer; owns the TMEM allocation
+//          warps 5-8  rescale and epilogue, one query row per thread
+template <int W>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    decode_pair_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap qmap,
+                       const __grid_constant__ CUtensorMap vmap, const Params p) {
+    constexpr int NKC = W / 64;  // 64-column chunks in a cache row (9 or 8)
+    extern __shared__ __align__(1024) unsigned char smem[];
+    Ctrl& c = *reinterpret_cast<Ctrl*>(smem + kCtrlOff);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int pair = blockIdx.x >> 1;
+    Waiter wt{&c.abort, p.dev_err};
+
+    if ((smem_u32(smem) & 1023) != 0) {  // swizzled operands need 1 KB alignment
+        if (tid == 0 && p.dev_err) atomicOr(p.dev_err, (int32_t)MLA_DEVERR_TIMEOUT);
+        return;  // both CTAs take this path together (same layout)
+    }
+    if (tid == 0) {
+        for (int s = 0; s < kNS; ++s) {
+            mbar_init(smem_u32(&c.full[s]), rank == 0 ? 4 : 1);  // S: one per K loader
+            mbar_init(smem_u32(&c.empty[s]), 1);
+            mbar_init(smem_u32(&c.vready[s]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&c.sfull[i]), 1);
+            mbar_init(smem_u32(&c.sfree[i]), 128);
+            mbar_init(smem_u32(&c.pempty[i]), 1);
+            mbar_init(smem_u32(&c.pfull[i]), 1);
+        }
+        mbar_init(smem_u32(&c.qready), 128);
+        mbar_init(smem_u32(&c.qland), 1);
+        mbar_init(smem_u32(&c.qfree), 128);
+        mbar_init(smem_u32(&c.statack), 1);
+        mbar_init(smem_u32(&c.odone), 1);
+        mbar_init(smem_u32(&c.evt), 1);
+        mbar_init(smem_u32(&c.evtdone), 128);
+        mbar_init(smem_u32(&c.statfull), 1);
+        mbar_init(smem_u32(&c.rowbar), 128);
+        c.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 4) {
+        tmem_alloc(smem_u32(&c.tmem_base), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tbase = c.tmem_base;
+
+    Walk w;
+    const bool has_work = walk_init(p, pair, w);
+    const long long ub = has_work ? w.u : 0;
+    const int Mq = p.T * p.H;
+
+    if (has_work && rank == 0) {
+        // =============================== S-CTA ===============================
+        const uint32_t tq = tbase;              // Q: columns [0, W/2)
+        const uint32_t ts0 = tbase + W / 2;     // S buffers: 2 x 64 columns
+        if (warp < 4) {
+            // ---------------- K loaders: warp k brings block k of every tile
+            const int kb = warp;
+            if (elect_one()) {
+                if (kb == 0) {
+                    tma_prefetch_desc(&tmap);
+                    tma_prefetch_desc(&qmap);
+                    // the first segment's queries: TMA into stages 1 and 2 (free until
+                    // the rows move them to TMEM), while tile 0 goes to stage 0
+                    mbar_arrive_expect_tx(smem_u32(&c.qland), (uint32_t)(NKC * kQChunk));
+                    for (int cc = 0; cc < NKC; ++cc)
+                        tma_load_2d(smem_u32(smem + q_chunk_off(cc)), &qmap, smem_u32(&c.qland),
+                                    cc * 64, w.b * Mq + w.g * 128);
+                }
+                long long i = 0;
+                long long last_issue[kNS];
+                for (int s = 0; s < kNS; ++s) last_issue[s] = -1;
+                for (; w.u < w.u_end; walk_next(p, w), ++i) {
+                    const int s = (int)(i % kNS);
+                    if (!wt.wait(smem_u32(&c.empty[s]), (uint32_t)((i / kNS) & 1) ^ 1)) break;
+                    if (i == 1 || i == 2)  // first use of a stage that held the queries
+                        if (!wt.wait(smem_u32(&c.qfree), 0)) break;
+                    if (kb == 0 && i > 0 && w.tile == 0) {
+                        // a later segment: warm L2 with its queries for the row threads
+                        const int rows = min(128, Mq - w.g * 128);
+                        prefetch_l2_bulk(p.q_abs + ((long long)w.b * Mq + w.g * 128) * W,
+                                         (uint32_t)(rows * W * 2));
+                    }
+                    const bool have = kb < valid_blocks(w);
+                    mbar_arrive_expect_tx(smem_u32(&c.full[s]), have ? (uint32_t)(NKC * 2048) : 0u);
+                    last_issue[s] = i;
+                    if (have) {
+                        int32_t blk = p.block_table[(long long)w.b * p.max_blocks + w.tile * 4 + kb];
+                        if (blk < 0 || blk >= p.num_blocks) {
+                            // load a valid stand-in; the row threads void the segment
+                            if (p.dev_err) atomicOr(p.dev_err, (int32_t)MLA_DEVERR_BAD_BLOCK);
+                            blk = 0;
+                        }
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch)
+                            tma_load_3d(smem_u32(smem + s * kStage + ch * kChunk + kb * 2048),
+                                        &tmap, smem_u32(&c.full[s]), ch * 64, 0, blk);
+                        if (NKC == 9)
+                            tma_load_3d(smem_u32(smem + kSideOff + s * kChunk + kb * 2048), &tmap,
+                                        smem_u32(&c.full[s]), 512, 0, blk);
+                    }
+                }
+                // drain: the copies issued into each stage must have landed
+                if (kb == 0) mbar_wait(smem_u32(&c.qland), 0, kWaitLimit);
+                for (int s = 0; s < kNS; ++s)
+                    if (last_issue[s] >= 0)
+                        mbar_wait(smem_u32(&c.full[s]), (uint32_t)((last_issue[s] / kNS) & 1),
+                                  kWaitLimit);
+            }
+        } else if (warp == 4) {
+            // ---------------- MMA issuer: S = Q K^T
+            if (elect_one()) {
+                constexpr uint32_t idesc = idesc_bf16_f32(128, kTok, 0, 0);
+                long long i = 0;
+                int seg = 0;
+                for (; w.u < w.u_end; walk_next(p, w), ++i) {
+                    const int s = (int)(i % kNS);
+                    const int buf = (int)(i & 1);
+                    if (seg_first(w, ub)) {
+                        if (!wt.wait(smem_u32(&c.qready), (uint32_t)(seg & 1))) break;
+                        ++seg;
+                    }
+                    if (!wt.wait(smem_u32(&c.full[s]), (uint32_t)((i / kNS) & 1))) break;
+                    if (!wt.wait(smem_u32(&c.sfree[buf]), (uint32_t)((i >> 1) & 1) ^ 1)) break;
+                    tc_fence_after();
+                    const uint32_t d = ts0 + buf * kTok;
+#pragma unroll 1
+                    for (int kc = 0; kc < NKC; ++kc) {
+                        const uint32_t base = kc < 8 ? smem_u32(smem + s * kStage + kc * kChunk)
+                                                     : smem_u32(smem + kSideOff + s * kChunk);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ts(d, tq + kc * 32 + kk * 8, sdesc_sw128(base + kk * 32, 16, 1024),
+                                   idesc, (kc | kk) != 0);
+                    }
+                    mma_commit(smem_u32(&c.sfull[buf]));
+                    mma_commit(smem_u32(&c.empty[s]));
+                }
+            }
+        } else if (warp >= 5) {
+            // ---------------- softmax rows (warps 5..8), one query row per thread
+            const int q = warp & 3;
+            const int r = q * 32 + lane;
+            const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+            const uint32_t pslot_remote = mapa(smem_u32(smem + kSideOff), 1);
+            const uint32_t alpha_remote = mapa(smem_u32(&c.alpha[0][0]), 1);
+            const uint32_t flags_remote = mapa(smem_u32(&c.flags[0][0]), 1);
+            const uint32_t pfull_remote = mapa(smem_u32(&c.pfull[0]), 1);
+            const uint32_t mstat_remote = mapa(smem_u32(&c.mstat[0]), 1);
+            const uint32_t lstat_remote = mapa(smem_u32(&c.lstat[0]), 1);
+            const uint32_t bad_remote = mapa(smem_u32(&c.bad), 1);
+            const uint32_t statfull_remote = mapa(smem_u32(&c.statfull), 1);
+            const float sl2 = p.scale_log2;
+            long long i = 0;
+            int seg = 0;
+            uint32_t rphase = 0;
+            float m_used = -INFINITY, l = 0.f;
+            int horizon = 0, bad = 0, seg_tile0 = 0;
+            bool row_ok = false;
+            for (; w.u < w.u_end; walk_next(p, w), ++i) {
+                const int buf = (int)(i & 1);
+                const bool first_tile = seg_first(w, ub);
+                if (first_tile) {
+                    seg_tile0 = w.tile;
+                    const int grow = w.g * 128 + r;
+                    row_ok = grow < Mq;
+                    const int t = row_ok ? grow / p.H : 0;
+                    horizon = row_ok ? w.S - p.T + t + 1 : 0;
+                    m_used = -INFINITY;
+                    l = 0.f;
+                    bad = 0;
+                    if (seg == 0) {
+                        // queries landed in shared memory by TMA: move this row to TMEM
+                        if (!wt.wait_warp(smem_u32(&c.qland), 0)) break;
+#pragma unroll 1
+                        for (int cc = 0; cc < NKC; ++cc) {
+                            const uint32_t rowa = smem_u32(smem + q_chunk_off(cc)) + r * 128;
+                            uint32_t v[32];
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) {
+                                const uint4 x = ld_shared_v4(rowa + ((u ^ (r & 7)) << 4));
+                                v[4 * u] = row_ok ? x.x : 0u;
+                                v[4 * u + 1] = row_ok ? x.y : 0u;
+                                v[4 * u + 2] = row_ok ? x.z : 0u;
+                                v[4 * u + 3] = row_ok ? x.w : 0u;
+                            }
+                            tmem_st32(tq + lane_off + cc * 32, v);
+                        }
+                        tmem_wait_st();
+                        mbar_arrive(smem_u32(&c.qfree));  // stages 1 and 2 may be refilled
+                    } else {
+                        // later segments: from global memory (warmed in L2 by the producer)
+                        const uint4* src = reinterpret_cast<const uint4*>(
+                            p.q_abs + ((long long)w.b * Mq + (row_ok ? grow : 0)) * W);
+#pragma unroll 1
+                        for (int cc0 = 0; cc0 < NKC; cc0 += 3) {
+                            uint4 x[3][8];
+#pragma unroll
+                            for (int k = 0; k < 3; ++k)
+#pragma unroll
+                                for (int j = 0; j < 8; ++j)
+                                    x[k][j] = (row_ok && cc0 + k < NKC) ? src[(cc0 + k) * 8 + j]
+                                                                       : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                            for (int k = 0; k < 3; ++k) {
+                                if (cc0 + k >= NKC) break;
+                                uint32_t v[32];
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) {
+                                    v[4 * j] = x[k][j].x;
+                                    v[4 * j + 1] = x[k][j].y;
+                                    v[4 * j + 2] = x[k][j].z;
+                                    v[4 * j + 3] = x[k][j].w;
+                                }
+                                tmem_st32(tq + lane_off + (cc0 + k) * 32, v);
+                            }
+                        }
+                        tmem_wait_st();
+                    }
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(&c.qready));
+                }
+                if (!wt.wait_warp(smem_u32(&c.sfull[buf]), (uint32_t)((i >> 1) & 1))) break;
+                tc_fence_after();
+                float x[kTok];
+                {
+                    uint32_t v0[32], v1[32];
+                    tmem_ld32(ts0 + buf * kTok + lane_off, v0);
+                    tmem_ld32(ts0 + buf * kTok + 32 + lane_off, v1);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        x[j] = __uint_as_float(v0[j]) * sl2;
+                        x[32 + j] = __uint_as_float(v1[j]) * sl2;
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(smem_u32(&c.sfree[buf]));
+                // keys past this row's horizon (only near the request's end)
+                const int j0 = w.tile * kTok;
+                if (j0 + kTok > horizon) {
+#pragma unroll
+                    for (int j = 0; j < kTok; ++j)
+                        if (j0 + j >= horizon) x[j] = -INFINITY;
+                }
+                float mx0 = x[0], mx1 = x[1];
+#pragma unroll
+                for (int j = 2; j < kTok; j += 2) {
+                    mx0 = fmaxf(mx0, x[j]);
+                    mx1 = fmaxf(mx1, x[j + 1]);
+                }
+                const float mx = fmaxf(mx0, mx1);
+                float alpha = 1.f;
+                if (mx > m_used + kRescaleThreshold || (m_used == -INFINITY && mx > -INFINITY)) {
+                    alpha = (m_used == -INFINITY) ? 1.f : ex2_approx(m_used - mx);
+                    m_used = mx;
+                }
+                const float mref = (m_used == -INFINITY) ? 0.f : m_used;
+                uint32_t pk[kTok / 2];
+                float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+                for (int j = 0; j < kTok; j += 2) {
+                    const float a = ex2_approx(x[j] - mref);   // 2^-inf = +0
+                    const float b2 = ex2_approx(x[j + 1] - mref);
+                    ps0 += a;
+                    ps1 += b2;
+                    pk[j / 2] = pack_bf16x2(a, b2);
+                }
+                l = l * alpha + (ps0 + ps1);
+                const int need = (!first_tile && alpha != 1.f) ? 1 : 0;
+                const unsigned any = __ballot_sync(0xffffffffu, need);
+                // P slot free? (the O-CTA's P*V two tiles back)
+                if (!wt.wait_warp(smem_u32(&c.pempty[buf]), (uint32_t)((i >> 1) & 1) ^ 1)) break;
+                const uint32_t pbar = pfull_remote + buf * 8;
+                const uint32_t prow = pslot_remote + buf * kPBytes + r * 128;
+                if (row_ok) {  // rows past the group are never read back
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        st_async_v4(prow + ((u ^ (r & 7)) << 4), pk[4 * u], pk[4 * u + 1],
+                                    pk[4 * u + 2], pk[4 * u + 3], pbar);
+                    st_async_b32(alpha_remote + (buf * 128 + r) * 4, __float_as_uint(alpha), pbar);
+                }
+                if (lane == 0) st_async_b32(flags_remote + (buf * 4 + q) * 4, any ? 1u : 0u, pbar);
+                if (seg_last(w)) {
+                    // invalid block ids anywhere in the segment void it (the producer
+                    // loaded a stand-in block): the row threads scan its table slice
+                    {
+                        const int blk0 = seg_tile0 * 4;
+                        const int blk1 = min(w.tile * 4 + 4, (w.S + 15) / 16);
+                        const int32_t* bt = p.block_table + (long long)w.b * p.max_blocks;
+                        int b_any = 0;
+                        for (int k = blk0 + r; k < blk1; k += 128) {
+                            const int32_t blk = bt[k];
+                            b_any |= (blk < 0 || blk >= p.num_blocks);
+                        }
+                        b_any = __any_sync(0xffffffffu, b_any);
+                        if (lane == 0) c.badw[q] = b_any;
+                    }
+                    if (!rows_sync(wt, smem_u32(&c.rowbar), rphase)) break;
+                    bad = c.badw[0] | c.badw[1] | c.badw[2] | c.badw[3];
+                    // hand the row statistics to the O-CTA
+                    if (seg > 0 && !wt.wait_warp(smem_u32(&c.statack), (uint32_t)((seg - 1) & 1))) break;
+                    st_cluster_f32(mstat_remote + r * 4, row_ok ? m_used : -INFINITY);
+                    st_cluster_f32(lstat_remote + r * 4, row_ok ? l : 0.f);
+                    if (r == 0)
+                        asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(bad_remote), "r"(bad)
+                                     : "memory");
+                    if (!rows_sync(wt, smem_u32(&c.rowbar), rphase)) break;
+                    if (r == 0) mbar_arrive_remote(statfull_remote);
+                    ++seg;
+                }
+            }
+        }
+    } else if (has_work) {
+        // =============================== O-CTA ===============================
+        if (warp == 0) {
+            // ---------------- V loader: one 4-D box [8 chunks][16 rows][64 cols] per block
+            if (elect_one()) {
+                tma_prefetch_desc(&vmap);
+                long long i = 0;
+                long long last_issue[kNS];
+                for (int s = 0; s < kNS; ++s) last_issue[s] = -1;
+                for (; w.u < w.u_end; walk_next(p, w), ++i) {
+                    const int s = (int)(i % kNS);
+                    if (!wt.wait(smem_u32(&c.empty[s]), (uint32_t)((i / kNS) & 1) ^ 1)) break;
+                    const int nb = valid_blocks(w);
+                    const int32_t* bt = p.block_table + (long long)w.b * p.max_blocks + w.tile * 4;
+                    mbar_arrive_expect_tx(smem_u32(&c.full[s]), (uint32_t)(nb * kVBlock));
+                    last_issue[s] = i;
+                    for (int k = 0; k < nb; ++k) {
+                        int32_t blk = bt[k];
+                        if (blk < 0 || blk >= p.num_blocks) blk = 0;  // voided by the S-CTA rows
+                        tma_load_4d(smem_u32(smem + s * kStage + k * kVBlock), &vmap,
+                                    smem_u32(&c.full[s]), 0, 0, 0, blk);
+                    }
+                }
+                for (int s = 0; s < kNS; ++s)
+                    if (last_issue[s] >= 0)
+                        mbar_wait(smem_u32(&c.full[s]), (uint32_t)((last_issue[s] / kNS) & 1),
+                                  kWaitLimit);
+            }
+        } else if (warp == 1) {
+            // ---------------- V landing: rows past the request are zeroed (P there
+            // is 0, but 0 * NaN would still poison the accumulator)
+            long long i = 0;
+            for (; w.u < w.u_end; walk_next(p, w), ++i) {
+                const int s = (int)(i % kNS);
+                if (!wt.wait_warp(smem_u32(&c.full[s]), (uint32_t)((i / kNS) & 1))) break;
+                const int nvalid = min(kTok, w.S - w.tile * kTok);
+                if (nvalid < kTok) {
+                    const int rows = kTok - nvalid;
+                    for (int e = lane; e < rows * 8 * 8; e += 32) {
+                        const int ch = e / (rows * 8);
+                        const int rr = nvalid + (e / 8) % rows;
+                        const int u = e % 8;
+                        *reinterpret_cast<uint4*>(smem + s * kStage + (rr >> 4) * kVBlock +
+                                                  ch * 2048 + (rr & 15) * 128 + u * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&c.vready[s]));
+            }
+        } else if (warp == 4) {
+            // ---------------- MMA issuer: O += P V
+            if (elect_one()) {
+                constexpr uint32_t idesc = idesc_bf16_f32(128, 256, 0, 1);
+                long long i = 0;
+                int nevt = 0, ndone = 0;
+                for (; w.u < w.u_end; walk_next(p, w), ++i) {
+                    const int s = (int)(i % kNS);
+                    const int slot = (int)(i & 1);
+                    // this tile's P rows, alphas and flags arrive by st.async (complete_tx)
+                    {
+                        const int grows = min(128, Mq - w.g * 128);
+                        mbar_arrive_expect_tx(smem_u32(&c.pfull[slot]),
+                                              (uint32_t)(grows * (128 + 4) + 4 * 4));
+                    }
+                    if (!wt.wait(smem_u32(&c.vready[s]), (uint32_t)((i / kNS) & 1))) break;
+                    if (!wt.wait(smem_u32(&c.pfull[slot]), (uint32_t)((i >> 1) & 1))) break;
+                    const bool first = seg_first(w, ub);
+                    const volatile int32_t* fl = c.flags[slot];
+                    if (!first && (fl[0] | fl[1] | fl[2] | fl[3])) {
+                        // rows whose max moved: rescale O once the issued P*V is done
+                        mma_commit(smem_u32(&c.odone));
+                        if (!wt.wait(smem_u32(&c.odone), (uint32_t)(ndone & 1))) break;
+                        ++ndone;
+                        c.evt_type = 1;
+                        c.evt_slot = slot;
+                        mbar_arrive(smem_u32(&c.evt));
+                        if (!wt.wait(smem_u32(&c.evtdone), (uint32_t)(nevt & 1))) break;
+                        ++nevt;
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_after();
+                    const uint32_t pa = smem_u32(smem + kSideOff + slot * kPBytes);
+                    const uint32_t va = smem_u32(smem + s * kStage);
+                    // V: K-step kk is cache block kk of the tile; its latent columns
+                    // sit in 8 chunks of [16 rows][128 B] at a 2 KB stride
+#pragma unroll
+                    for (int half = 0; half < 2; ++half)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ss(tbase + half * 256, sdesc_sw128(pa + kk * 32, 16, 1024),
+                                   sdesc_sw128(va + kk * kVBlock + half * 4 * 2048, 2048, 1024),
+                                   idesc, !(first && kk == 0));
+                    mma_commit(smem_u32(&c.empty[s]));
+                    mma_commit_mc(smem_u32(&c.pempty[slot]), 0x1);
+                    if (seg_last(w)) {
+                        mma_commit(smem_u32(&c.odone));
+                        if (!wt.wait(smem_u32(&c.odone), (uint32_t)(ndone & 1))) break;
+                        ++ndone;
+                        c.evt_type = 2;
+                        c.evt_slot = 0;
+                        mbar_arrive(smem_u32(&c.evt));
+                        if (!wt.wait(smem_u32(&c.evtdone), (uint32_t)(nevt & 1))) break;
+                        ++nevt;
+                    }
+                }
+            }
+        } else if (warp >= 5) {
+            // ---------------- row warps: rescale and epilogue
+            const int q = warp & 3;
+            const int r = q * 32 + lane;
+            const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+            const uint32_t statack_remote = mapa(smem_u32(&c.statack), 0);
+            int nevt = 0, seg = 0;
+            uint32_t rphase = 0;
+            int seg_tile0 = w.tile;
+            bool done = false;
+            while (!done) {
+                if (!wt.wait_warp(smem_u32(&c.evt), (uint32_t)(nevt & 1))) break;
+                ++nevt;
+                tc_fence_after();
+                const int type = *(volatile int32_t*)&c.evt_type;
+                if (type == 1) {
+                    const int slot = *(volatile int32_t*)&c.evt_slot;
+                    const float a = c.alpha[slot][r];
+                    if (a != 1.f) {
+#pragma unroll 1
+                        for (int cc = 0; cc < 512; cc += 32) {
+                            uint32_t v[32];
+                            tmem_ld32(tbase + lane_off + cc, v);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                v[j] = __float_as_uint(__uint_as_float(v[j]) * a);
+                            tmem_st32(tbase + lane_off + cc, v);
+                        }
+                        tmem_wait_st();
+                    }
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(&c.evtdone));
+                    continue;
+                }
+                // segment epilogue: locate the segment (advance the walk to its end)
+                while (!seg_last(w)) walk_next(p, w);
+                if (!wt.wait_warp(smem_u32(&c.statfull), (uint32_t)(seg & 1))) break;
+                const float m = c.mstat[r];
+                const float lsum = c.lstat[r];
+                const int seg_bad = *(volatile int32_t*)&c.bad;
+                // statistics consumed: the S-CTA may send the next segment's
+                if (!rows_sync(wt, smem_u32(&c.rowbar), rphase)) break;
+                if (r == 0) mbar_arrive_remote(statack_remote);
+                const int grow = w.g * 128 + r;
+                const bool row_ok = grow < Mq;
+                const bool full_seg = (seg_tile0 == 0) && (w.tile + 1 == w.ntiles);
+                const bool empty = seg_bad || !(lsum > 0.f);
+                const float inv = empty ? 0.f : 1.f / lsum;
+                const float lse_v = empty ? -INFINITY : (m + log2f(lsum)) * 0.69314718055994531f;
+                if (row_ok) {
+                    if (full_seg) {
+                        __nv_bfloat16* dst = p.out + ((long long)w.b * Mq + grow) * 512;
+#pragma unroll 1
+                        for (int cc = 0; cc < 512; cc += 32) {
+                            uint32_t v[32];
+                            tmem_ld32(tbase + lane_off + cc, v);
+                            tmem_wait_ld();
+                            uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                d4[j] = make_uint4(
+                                    pack_bf16x2(__uint_as_float(v[8 * j]) * inv,
+                                                __uint_as_float(v[8 * j + 1]) * inv),
+                                    pack_bf16x2(__uint_as_float(v[8 * j + 2]) * inv,
+                                                __uint_as_float(v[8 * j + 3]) * inv),
+                                    pack_bf16x2(__uint_as_float(v[8 * j + 4]) * inv,
+                                                __uint_as_float(v[8 * j + 5]) * inv),
+                                    pack_bf16x2(__uint_as_float(v[8 * j + 6]) * inv,
+                                                __uint_as_float(v[8 * j + 7]) * inv));
+                        }
+                        if (p.lse) p.lse[(long long)w.b * Mq + grow] = lse_v;
+                    } else {
+                        const int slot = pair * 2 + (seg == 0 ? 0 : 1);
+                        float* dst = p.ws_o + ((long long)slot * 128 + r) * 512;
+#pragma unroll 1
+                        for (int cc = 0; cc < 512; cc += 32) {
+                            uint32_t v[32];
+                            tmem_ld32(tbase + lane_off + cc, v);
+                            tmem_wait_ld();
+                            float4* d4 = reinterpret_cast<float4*>(dst + cc);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                d4[j] = make_float4(__uint_as_float(v[4 * j]) * inv,
+                                                    __uint_as_float(v[4 * j + 1]) * inv,
+                                                    __uint_as_float(v[4 * j + 2]) * inv,
+                                                    __uint_as_float(v[4 * j + 3]) * inv);
+                        }
+                        p.ws_lse[(long long)slot * 128 + r] =
+                            seg_bad ? __int_as_float(0x7fc00000) : lse_v;  // NaN marks bad
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(smem_u32(&c.evtdone));
+                ++seg;
+                if (w.u + 1 >= w.u_end) {
+                    done = true;
+                } else {
+                    walk_next(p, w);
+                    seg_tile0 = w.tile;
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncwarp();
+    cluster_sync();
+    tc_fence_after();
+    if (warp == 4) tmem_dealloc(tbase, 512);
+}
+
+// ------------------------------------------------------------------ combine
+// One warp per query row of every (request, row group): merges the partial
+// segments of row groups that were split across pairs (LSE-weighted, in pair
+// order), and writes the rows of empty or invalid requests.
+constexpr int kCombineWarps = 8;
+
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Params p) {
+    const int lane = threadIdx.x & 31;
+    const long long gw = (long long)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+    const int Mq = p.T * p.H;
+    const int G = (Mq + 127) / 128;
+    const long long bg = gw / 128;
+    const int rr = (int)(gw % 128);
+    if (bg >= (long long)p.B * G) return;
+    const int b = (int)(bg / G), g = (int)(bg % G);
+    const int rows = min(128, Mq - g * 128);
+    if (rr >= rows) return;
+    const long long orow = (long long)b * Mq + g * 128 + rr;
+    const int S = p.seq_lens[b];
+    const int nt = ntiles_of(S, p.T, p.max_blocks);
+    __nv_bfloat16* dst = p.out + orow * 512;
+    if (nt == 0) {
+        if (g == 0 && rr == 0 && lane == 0 && p.dev_err) {
+            if (S < 0 || (S > 0 && S < p.T)) atomicOr(p.dev_err, (int32_t)MLA_DEVERR_SEQ_SHORT);
+            else if (S > p.max_blocks * 16) atomicOr(p.dev_err, (int32_t)MLA_DEVERR_SEQ_TOO_LONG);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            reinterpret_cast<uint4*>(dst)[lane + 32 * j] = make_uint4(0, 0, 0, 0);
+        if (lane == 0 && p.lse) p.lse[orow] = -INFINITY;
+        return;
+    }
+    // the unit range of (b, g) and the total, as the decode kernel partitions
+    long long U = 0, before = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+        const int bb = b0 + lane;
+        long long v = bb < p.B ? (long long)ntiles_of(p.seq_lens[bb], p.T, p.max_blocks) * G : 0;
+        long long vb = bb < b ? v : 0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            v += __shfl_xor_sync(0xffffffffu, v, o);
+            vb += __shfl_xor_sync(0xffffffffu, vb, o);
+        }
+        U += v;
+        before += vb;
+    }
+    const long long u0 = before + (long long)g * nt, u1 = u0 + nt;
+    int np = p.NP;
+    const long long cap = (U + p.min_units - 1) / p.min_units;
+    if (cap < np) np = (int)(cap > 0 ? cap : 1);
+    auto owner = [&](long long u) {  // pair whose range holds unit u
+        long long pp = (u * np) / U;
+        while (pp + 1 < np && U * (pp + 1) / np <= u) ++pp;
+        while (pp > 0 && U * pp / np > u) --pp;
+        return (int)pp;
+    };
+    const int pf = owner(u0), pl = owner(u1 - 1);
+    if (pf == pl) return;  // one pair held the whole row group and wrote it
+    const int nparts = pl - pf + 1;
+    auto slot_of = [&](int k) {
+        const int pp = pf + k;
+        return pp * 2 + ((U * pp / np) >= u0 ? 0 : 1);  // first or last segment of pp
+    };
+    // part LSEs: lane k holds parts k, k + 32, ...
+    float M = -INFINITY;
+    int bad = 0;
+    for (int k = lane; k < nparts; k += 32) {
+        const float ls = p.ws_lse[(long long)slot_of(k) * 128 + rr];
+        bad |= (ls != ls);
+        M = fmaxf(M, ls);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+    }
+    float acc[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+    float wsum = 0.f;
+    if (!bad && M > -INFINITY) {
+        for (int k0 = 0; k0 < nparts; k0 += 4) {
+            float4 v[4][4];
+            float wk[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int k = k0 + q;
+                wk[q] = 0.f;
+                if (k < nparts) {
+                    const long long slot = slot_of(k);
+                    const float ls = p.ws_lse[slot * 128 + rr];
+                    wk[q] = (ls == -INFINITY) ? 0.f : expf(ls - M);
+                    const float4* src = reinterpret_cast<const float4*>(p.ws_o + (slot * 128 + rr) * 512);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) v[q][j] = src[lane + 32 * j];
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) v[q][j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                wsum += wk[q];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    acc[4 * j] += wk[q] * v[q][j].x;
+                    acc[4 * j + 1] += wk[q] * v[q][j].y;
+                    acc[4 * j + 2] += wk[q] * v[q][j].z;
+                    acc[4 * j + 3] += wk[q] * v[q][j].w;
+                }
+            }
+        }
+    }
+    const bool empty = bad || !(wsum > 0.f);
+    const float inv = empty ? 0.f : 1.f / wsum;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint2 o;
+        o.x = pack_bf16x2(acc[4 * j] * inv, acc[4 * j + 1] * inv);
+        o.y = pack_bf16x2(acc[4 * j + 2] * inv, acc[4 * j + 3] * inv);
+        reinterpret_cast<uint2*>(dst)[lane + 32 * j] = o;
+    }
+    if (lane == 0 && p.lse) p.lse[orow] = empty ? -INFINITY : M + logf(wsum);
+}
+
+// ------------------------------------------------------------------ host
+struct DeviceInfo {
+    int max_pairs = 0;
+};
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+cudaError_t get_encode(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_encode) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess) return e;
+        if (q != cudaDriverEntryPointSuccess || !f) return cudaErrorNotSupported;
+        g_encode = (PFN_cuTensorMapEncodeTiled_v12000)f;
+    }
+    *fn = g_encode;
+    return cudaSuccess;
+}
+
+template <int W>
+cudaError_t setup_kernel(int dev, int* max_pairs) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo& di = g_dev[dev & 63];
+    static bool attr_set[2][64] = {};
+    const int wi = W == 576 ? 0 : 1;
+    if (!attr_set[wi][dev & 63]) {
+        cudaError_t e = cudaFuncSetAttribute(decode_pair_kernel<W>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set[wi][dev & 63] = true;
+    }
+    if (di.max_pairs == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&n, decode_pair_kernel<W>, &cfg);
+        if (e != cudaSuccess) return e;
+        if (n <= 0) return cudaErrorNotSupported;
+        di.max_pairs = n;
+    }
+    *max_pairs = di.max_pairs;
+    return cudaSuccess;
+}
+
+int max_pairs_for(const mla_dims& d, cudaError_t* err) {
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess) return 0;
+    int n = 0;
+    *err = (d.kv_rank + d.d_rope == 576) ? setup_kernel<576>(dev, &n) : setup_kernel<512>(dev, &n);
+    return n;
+}
+
+}  // namespace
+
+bool tc_decode_supported(const mla_dims& d) {
+    const int W = d.kv_rank + d.d_rope;
+    return d.dtype == MLA_BF16 && d.kv_rank == 512 && (W == 576 || W == 512) &&
+           d.block_size == 16 && d.t_q * d.n_head <= 1 << 20;
+}
+
+cudaError_t tc_decode_workspace(int32_t batch, int32_t max_blocks, const mla_dims& d,
+                                size_t* bytes) {
+    (void)batch;
+    (void)max_blocks;
+    cudaError_t e;
+    const int np = max_pairs_for(d, &e);
+    if (e != cudaSuccess) return e;
+    const size_t o = (size_t)2 * np * 128 * 512 * sizeof(float);
+    const size_t l = (size_t)2 * np * 128 * sizeof(float);
+    *bytes = o + l;
+    return cudaSuccess;
+}
+
+cudaError_t launch_decode_tc(void* out, float* lse, const void* q_abs, const void* kv_cache,
+                             const int32_t* block_table, const int32_t* seq_lens,
+                             int32_t batch, int32_t max_blocks, int32_t num_blocks,
+                             const mla_dims& d, float scale, void* workspace,
+                             int32_t* dev_err, cudaStream_t s) {
+    const int W = d.kv_rank + d.d_rope;
+    cudaError_t e;
+    const int np = max_pairs_for(d, &e);
+    if (e != cudaSuccess) return e;
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    if ((e = get_encode(&enc)) != cudaSuccess) return e;
+    CUtensorMap tmap;
+    cuuint64_t dims[3] = {(cuuint64_t)W, 16, (cuuint64_t)num_blocks};
+    cuuint64_t strides[2] = {(cuuint64_t)W * 2, (cuuint64_t)16 * W * 2};
+    cuuint32_t box[3] = {64, 16, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult cr = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(kv_cache),
+                      dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) {
+        set_error("cuTensorMapEncodeTiled failed (%d)", (int)cr);
+        return cudaErrorInvalidValue;
+    }
+    CUtensorMap qmap;
+    {
+        cuuint64_t qdims[2] = {(cuuint64_t)W, (cuuint64_t)batch * d.t_q * d.n_head};
+        cuuint64_t qstrides[1] = {(cuuint64_t)W * 2};
+        cuuint32_t qbox[2] = {64, 128};
+        cuuint32_t qes[2] = {1, 1};
+        cr = enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q_abs), qdims,
+                 qstrides, qbox, qes, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr != CUDA_SUCCESS) {
+            set_error("cuTensorMapEncodeTiled (queries) failed (%d)", (int)cr);
+            return cudaErrorInvalidValue;
+        }
+    }
+    CUtensorMap vmap;
+    {
+        // 4-D view of the cache: {64 columns, 16 rows, 8 column chunks, blocks}
+        cuuint64_t vdims[4] = {64, 16, 8, (cuuint64_t)num_blocks};
+        cuuint64_t vstrides[3] = {(cuuint64_t)W * 2, 128, (cuuint64_t)16 * W * 2};
+        cuuint32_t vbox[4] = {64, 16, 8, 1};
+        cuuint32_t ves[4] = {1, 1, 1, 1};
+        cr = enc(&vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(kv_cache), vdims,
+                 vstrides, vbox, ves, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr != CUDA_SUCCESS) {
+            set_error("cuTensorMapEncodeTiled (values) failed (%d)", (int)cr);
+            return cudaErrorInvalidValue;
+        }
+    }
+    Params p;
+    p.q_abs = (const __nv_bfloat16*)q_abs;
+    p.kv = (const __nv_bfloat16*)kv_cache;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.out = (__nv_bfloat16*)out;
+    p.lse = lse;
+    p.ws_o = (float*)workspace;
+    p.ws_lse = (float*)((char*)workspace + (size_t)2 * np * 128 * 512 * sizeof(float));
+    p.dev_err = dev_err;
+    p.B = batch;
+    p.T = d.t_q;
+    p.H = d.n_head;
+    p.W = W;
+    p.max_blocks = max_blocks;
+    p.num_blocks = num_blocks;
+    p.NP = np;
+    p.min_units = 2;
+    p.scale_log2 = scale * 1.4426950408889634f;
+
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * np, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (W == 576)
+        e = cudaLaunchKernelEx(&cfg, decode_pair_kernel<576>, tmap, qmap, vmap, p);
+    else
+        e = cudaLaunchKernelEx(&cfg, decode_pair_kernel<512>, tmap, qmap, vmap, p);
+    if (e != cudaSuccess) return e;
+    const long long G = (d.t_q * d.n_head + 127) / 128;
+    const long long warps = (long long)batch * G * 128;
+    combine_kernel<<<(unsigned)((warps + kCombineWarps - 1) / kCombineWarps), kCombineWarps * 32,
+                     0, s>>>(p);
+    return cudaGetLastError();
+}
+
 bool tc_gemm_supported(const mla_dims&, int32_t, bool) { return false; }
 cudaError_t launch_absorb_tc(void*, const void*, const void*, const void*, int32_t,
                              const mla_dims&, cudaStream_t) {
