@@ -1091,14 +1091,4 @@ cudaError_t launch_decode_tc(void* out, float* lse, const void* q_abs, const voi
     return cudaGetLastError();
 }
 
-bool tc_gemm_supported(const mla_dims&, int32_t, bool) { return false; }
-cudaError_t launch_absorb_tc(void*, const void*, const void*, const void*, int32_t,
-                             const mla_dims&, cudaStream_t) {
-    return cudaErrorNotSupported;
-}
-cudaError_t launch_decompress_tc(void*, const void*, const void*, int32_t, const mla_dims&,
-                                 cudaStream_t) {
-    return cudaErrorNotSupported;
-}
-
 }  // namespace mla
