@@ -53,6 +53,11 @@ constexpr int kPBytes = 128 * 128;            // P [128 rows x 64 tokens] bf16
 constexpr int kCtrlOff = kSideOff + 2 * kPBytes;
 constexpr int kQChunk = 128 * 128;            // 128 query rows x 64 columns of bf16
 constexpr int kVBlock = 8 * 2048;             // O-CTA: one block's V as [8 chunks][16 rows][128 B]
+// S-CTA: P rows 0..63 are staged in [216 KB, 224 KB) (unused in the S-CTA) and
+// shipped by one bulk copy; rows 64..127 go by st.async. Both paths share the
+// SM-to-SM bandwidth (about 40 GB/s); splitting them keeps each short.
+constexpr int kStg0Off = kSideOff + 3 * kChunk;
+static_assert(kStg0Off + 64 * 128 <= kCtrlOff, "staging region");
 // the first segment's queries sit in stages 1-2 (latent chunks 0..7) and in
 // the rope chunks of stages 1-2 (chunk 8); tile 0 uses stage 0 meanwhile
 __host__ __device__ constexpr int q_chunk_off(int cc) {
@@ -62,6 +67,7 @@ static_assert(kSideOff + kChunk + kQChunk <= kSideOff + 3 * kChunk, "q chunk 8 p
 constexpr int kThreads = 288;                 // see the role map in the kernel
 constexpr uint64_t kWaitLimit = 2000000000ull;  // ns before a wait gives up
 constexpr float kRescaleThreshold = 8.0f;     // lazy rescale, log2 units
+constexpr int kPrefetchAhead = 6;             // tiles the L2 prefetcher runs ahead of V landing
 
 struct Ctrl {
     uint64_t full[kNS];     // both: this CTA's part of the tile landed (complete_tx)
@@ -80,6 +86,8 @@ struct Ctrl {
     uint64_t evtdone;       // O: row warps -> MMA warp (128)
     uint64_t statfull;      // O: segment statistics written (1 remote)
     uint64_t rowbar;        // both: barrier among the 128 row threads
+    uint64_t stg_rdy;       // S: rows 0..63 of P are staged (64 arrivals)
+    uint64_t stg_free;      // S: the previous bulk copy has read the staging region
     uint32_t tmem_base;
     int32_t abort;
     int32_t evt_type;       // 1 = rescale slot evt_slot, 2 = segment epilogue
@@ -87,6 +95,7 @@ struct Ctrl {
     int32_t flags[2][4];    // O: per softmax warp, some row needs a rescale
     int32_t bad;            // O: the segment met an invalid block id
     int32_t badw[4];        // S: per row warp, the segment met an invalid block id
+    int32_t landed;         // O: tiles whose V has landed (paces the L2 prefetcher)
     float alpha[2][128];    // O: per-row rescale factors of the P slot
     float mstat[128];       // O: segment max (log2 units) per row
     float lstat[128];       // O: segment sum per row
@@ -240,9 +249,10 @@ __device__ __forceinline__ int valid_blocks(const Walk& w) {
 // Role map (9 warps per CTA):
 //   S-CTA  warps 0-3  K loaders: warp k brings block k of each tile (3-D boxes)
 //          warp 4     S = Q K^T MMA issuer; owns the TMEM allocation
-//          warps 5-8  softmax, one query row per thread
+//          warps 5-8  softmax, one query row per thread; send P to the O-CTA
 //   O-CTA  warp 0     V loader: one 4-D box per cache block
 //          warp 1     V landing: zeroes rows past the request, releases the stage
+//          warp 2     L2 prefetcher of upcoming cache blocks
 //          warp 4     O += P V MMA issuer; owns the TMEM allocation
 //          warps 5-8  rescale and epilogue, one query row per thread
 template <int W>
@@ -282,7 +292,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(&c.evtdone), 128);
         mbar_init(smem_u32(&c.statfull), 1);
         mbar_init(smem_u32(&c.rowbar), 128);
+        mbar_init(smem_u32(&c.stg_rdy), 64);
+        mbar_init(smem_u32(&c.stg_free), 1);
         c.abort = 0;
+        c.landed = 0;
         fence_mbar_init();
     }
     if (warp == 4) {
@@ -522,14 +535,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 // P slot free? (the O-CTA's P*V two tiles back)
                 if (!wt.wait_warp(smem_u32(&c.pempty[buf]), (uint32_t)((i >> 1) & 1) ^ 1)) break;
                 const uint32_t pbar = pfull_remote + buf * 8;
-                const uint32_t prow = pslot_remote + buf * kPBytes + r * 128;
-                if (row_ok) {  // rows past the group are never read back
+                if (r >= 64) {
+                    if (row_ok) {  // rows past the group are never read back
+                        const uint32_t prow = pslot_remote + buf * kPBytes + r * 128;
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            st_async_v4(prow + ((u ^ (r & 7)) << 4), pk[4 * u], pk[4 * u + 1],
+                                        pk[4 * u + 2], pk[4 * u + 3], pbar);
+                    }
+                } else {
+                    // rows 0..63: stage locally, then one bulk copy to the P slot
+                    const uint32_t stg = smem_u32(smem + kStg0Off);
+                    if (r == 0) {
+                        bulk_wait_read_all();  // the previous copy has left the region
+                        mbar_arrive(smem_u32(&c.stg_free));
+                    }
+                    __syncwarp();
+                    if (!wt.wait_warp(smem_u32(&c.stg_free), (uint32_t)(i & 1))) break;
 #pragma unroll
                     for (int u = 0; u < 8; ++u)
-                        st_async_v4(prow + ((u ^ (r & 7)) << 4), pk[4 * u], pk[4 * u + 1],
-                                    pk[4 * u + 2], pk[4 * u + 3], pbar);
-                    st_async_b32(alpha_remote + (buf * 128 + r) * 4, __float_as_uint(alpha), pbar);
+                        st_shared_v4(stg + r * 128 + ((u ^ (r & 7)) << 4), pk[4 * u],
+                                     pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                    fence_proxy_async_smem();
+                    mbar_arrive(smem_u32(&c.stg_rdy));
+                    if (r == 0) {
+                        const int grows = min(128, Mq - w.g * 128);
+                        const int nrows = min(64, grows);
+                        if (wt.wait(smem_u32(&c.stg_rdy), (uint32_t)(i & 1)) && nrows > 0) {
+                            bulk_s2cluster(pslot_remote + buf * kPBytes, stg,
+                                           (uint32_t)(nrows * 128), pbar);
+                            bulk_commit();
+                        }
+                    }
+                    __syncwarp();
                 }
+                if (row_ok)
+                    st_async_b32(alpha_remote + (buf * 128 + r) * 4, __float_as_uint(alpha), pbar);
                 if (lane == 0) st_async_b32(flags_remote + (buf * 4 + q) * 4, any ? 1u : 0u, pbar);
                 if (seg_last(w)) {
                     // invalid block ids anywhere in the segment void it (the producer
@@ -560,6 +601,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     ++seg;
                 }
             }
+            // the bulk copies must finish before the CTA may exit
+            if (r == 0) bulk_wait_all();
+            __syncwarp();
         }
     } else if (has_work) {
         // =============================== O-CTA ===============================
@@ -610,7 +654,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     fence_proxy_async_smem();
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&c.vready[s]));
+                if (lane == 0) {
+                    mbar_arrive(smem_u32(&c.vready[s]));
+                    *(volatile int32_t*)&c.landed = (int32_t)(i + 1);
+                }
+            }
+        } else if (warp == 2) {
+            // ---------------- L2 prefetcher: pulls the cache blocks of the tiles
+            // kPrefetchAhead past the V landing point into L2 (plain prefetches,
+            // so the TMA queues of both CTAs only carry the real loads)
+            long long i = 0;
+            const uint64_t t_start = globaltimer_ns();
+            for (; w.u < w.u_end; walk_next(p, w), ++i) {
+                while (i > *(volatile int32_t*)&c.landed + kPrefetchAhead) {
+                    if (c.abort || globaltimer_ns() - t_start > 4 * kWaitLimit) break;
+                    __nanosleep(200);
+                }
+                if (c.abort) break;
+                const int nb = valid_blocks(w);
+                const int32_t* bt = p.block_table + (long long)w.b * p.max_blocks + w.tile * 4;
+                constexpr int kLines = 16 * W * 2 / 128;  // 128-byte lines in one block
+                for (int k = 0; k < nb; ++k) {
+                    const int32_t blk = bt[k];
+                    if (blk < 0 || blk >= p.num_blocks) continue;
+                    const char* base = reinterpret_cast<const char*>(p.kv + (long long)blk * 16 * W);
+                    for (int ln = lane; ln < kLines; ln += 32) prefetch_l2_line(base + ln * 128);
+                }
             }
         } else if (warp == 4) {
             // ---------------- MMA issuer: O += P V
