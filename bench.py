@@ -19,6 +19,7 @@ import argparse
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -41,6 +42,27 @@ def load_peaks():
             d = json.load(f)
         return d, "measured"
     return dict(FALLBACK_PEAKS), "fallback"
+
+
+def profiled_traffic(config_name):
+    """DRAM bytes (read + write) per launch of the pair decode kernel from the
+    committed ncu summary of this workload, or None when there is none or the
+    kernel source has changed since it was captured (the summary records the
+    sha1 of tc_decode.cu it was taken on)."""
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", f"decode_pair_{config_name}.md")
+    src = os.path.join(ROOT, "mla_latent_cache_absorbed_gb300", "csrc", "tc_decode.cu")
+    if not (os.path.exists(prof) and os.path.exists(src)):
+        return None
+    text = open(prof).read()
+    m_t = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    m_h = re.search(r"kernel_source_sha1:\s*([0-9a-f]+)", text)
+    if not (m_t and m_h):
+        return None
+    sha = hashlib.sha1(open(src, "rb").read()).hexdigest()
+    if not sha.startswith(m_h.group(1)):
+        return None
+    return int(m_t.group(1))
 
 
 def dist_env():
@@ -347,7 +369,7 @@ def run_ours(args, wl):
         roof = {"bound": "hbm", "achieved": dom_bytes / dom_s / 1e9, "peak": hbm_peak,
                 "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = profiled_traffic(wl.name) if dominant == "decode" else None
     roof["kernel"] = dominant
     roof["peak_source"] = f"{peaks_src} (MEASURED_PEAKS.json)" if peaks_src == "measured" \
         else "fallback (profiling recipe)"
