@@ -72,6 +72,30 @@ def dist_env():
     return rank, world, local
 
 
+def rank_seed(rank):
+    """Workload seed of a rank: rank 0 runs the named workload itself, every
+    other rank an independent batch of the same shape (weak scaling: requests
+    shard across GPUs, nothing is exchanged)."""
+    return None if rank == 0 else 1000 + rank
+
+
+def max_over_ranks(ms, device):
+    """The slowest rank's time (the job ends when the last rank ends)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(ms)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(rows_per_rank, world, steps, ms_total):
+    """Decode tokens per second of the whole job: every rank decodes its own
+    rows_per_rank query rows per step."""
+    return rows_per_rank * world * steps / (ms_total / 1e3)
+
+
 # ---------------------------------------------------------------- workload facts
 def algorithmic(wl):
     """Algorithmic bytes and flops of one step (per unit definitions).
@@ -332,13 +356,10 @@ def run_ours(args, wl):
     ms_total = ev0.elapsed_time(ev1)
     clocks = sampler.stop()
     if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+        ms_total = max_over_ranks(ms_total, dev)
         dist.barrier()
     ms_per_step = ms_total / steps
-    tokens = wl.rows * world * steps
-    value = tokens / (ms_total / 1e3)
+    value = whole_job_rate(wl.rows, world, steps, ms_total)
 
     # per-stage kernel times (same layers, same launch configuration)
     stage_ms = {}
@@ -468,7 +489,7 @@ def main():
     args = ap.parse_args()
     from mla_latent_cache_absorbed_gb300 import workloads as W
     rank, world, _ = dist_env()
-    wl = W.make_workload(args.config, seed=None if rank == 0 else 1000 + rank)
+    wl = W.make_workload(args.config, seed=rank_seed(rank))
     if args.impl == "reference":
         if args.steps == 0:
             args.steps = 3

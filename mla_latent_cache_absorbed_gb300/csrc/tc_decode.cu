@@ -53,9 +53,11 @@ constexpr int kPBytes = 128 * 128;            // P [128 rows x 64 tokens] bf16
 constexpr int kCtrlOff = kSideOff + 2 * kPBytes;
 constexpr int kQChunk = 128 * 128;            // 128 query rows x 64 columns of bf16
 constexpr int kVBlock = 8 * 2048;             // O-CTA: one block's V as [8 chunks][16 rows][128 B]
-// S-CTA: P rows 0..63 are staged in [216 KB, 224 KB) (unused in the S-CTA) and
-// shipped by one bulk copy; rows 64..127 go by st.async. Both paths share the
-// SM-to-SM bandwidth (about 40 GB/s); splitting them keeps each short.
+// S-CTA: P rows 0..63 are staged in [216 KB, 224 KB) (unused in the S-CTA)
+// and shipped by the sender warp's bulk copy; rows 64..127 go straight from
+// their threads by st.async. Both paths share the SM-to-SM bandwidth (about
+// 40 GB/s); splitting them keeps each short, and the staging leaves the cache
+// pipeline's stages alone.
 constexpr int kStg0Off = kSideOff + 3 * kChunk;
 static_assert(kStg0Off + 64 * 128 <= kCtrlOff, "staging region");
 // the first segment's queries sit in stages 1-2 (latent chunks 0..7) and in
@@ -64,12 +66,21 @@ __host__ __device__ constexpr int q_chunk_off(int cc) {
     return cc < 8 ? kStage + cc * kQChunk : kSideOff + kChunk;
 }
 static_assert(kSideOff + kChunk + kQChunk <= kSideOff + 3 * kChunk, "q chunk 8 placement");
-constexpr int kThreads = 288;                 // see the role map in the kernel
+constexpr int kThreads = 320;                 // see the role map in the kernel
 constexpr uint64_t kWaitLimit = 2000000000ull;  // ns before a wait gives up
+constexpr uint32_t kSuspendHintNs = 1000;     // longest suspension of one wait poll
 constexpr float kRescaleThreshold = 8.0f;     // lazy rescale, log2 units
 constexpr int kPrefetchAhead = 6;             // tiles the L2 prefetcher runs ahead of V landing
 
+// per-tile rescale message from the S-CTA's softmax to the O-CTA (one bulk copy)
+struct __align__(16) AlphaMsg {
+    float alpha[128];       // per-row rescale factors of the P slot
+    int32_t flags[4];       // per softmax warp, some row needs a rescale
+};
+
 struct Ctrl {
+    AlphaMsg amsg[2];       // O: the messages of the two P slots
+    AlphaMsg astg;          // S: staging of the current tile's message
     uint64_t full[kNS];     // both: this CTA's part of the tile landed (complete_tx)
     uint64_t empty[kNS];    // both: stage free (own QK / P*V commit)
     uint64_t sfull[2];      // S: scores ready (QK commit)
@@ -86,17 +97,15 @@ struct Ctrl {
     uint64_t evtdone;       // O: row warps -> MMA warp (128)
     uint64_t statfull;      // O: segment statistics written (1 remote)
     uint64_t rowbar;        // both: barrier among the 128 row threads
-    uint64_t stg_rdy;       // S: rows 0..63 of P are staged (64 arrivals)
-    uint64_t stg_free;      // S: the previous bulk copy has read the staging region
+    uint64_t stg_rdy;       // S: the tile's P is staged (128 arrivals)
+    uint64_t stg_free;      // S: the previous tile's P has landed in the O-CTA (1 remote arrival)
     uint32_t tmem_base;
     int32_t abort;
     int32_t evt_type;       // 1 = rescale slot evt_slot, 2 = segment epilogue
     int32_t evt_slot;
-    int32_t flags[2][4];    // O: per softmax warp, some row needs a rescale
     int32_t bad;            // O: the segment met an invalid block id
     int32_t badw[4];        // S: per row warp, the segment met an invalid block id
     int32_t landed;         // O: tiles whose V has landed (paces the L2 prefetcher)
-    float alpha[2][128];    // O: per-row rescale factors of the P slot
     float mstat[128];       // O: segment max (log2 units) per row
     float lstat[128];       // O: segment sum per row
 };
@@ -110,7 +119,7 @@ struct Params {
     const int32_t* seq_lens;      // [B]
     __nv_bfloat16* out;           // [B][T][H][512]
     float* lse;                   // [B][T][H] or null
-    float* ws_o;                  // [2*NP][128][512]
+    float* ws_o;                  // [2*NP slots][128 column quads][128 rows][4]
     float* ws_lse;                // [2*NP][128]
     int32_t* dev_err;
     int B, T, H, W, max_blocks, num_blocks;
@@ -215,7 +224,7 @@ struct Waiter {
         if (mbar_try_wait(bar, parity)) return true;
         const uint64_t t0 = globaltimer_ns();
         for (uint32_t i = 1;; ++i) {
-            if (mbar_try_wait(bar, parity)) return true;
+            if (mbar_try_wait_hint(bar, parity, kSuspendHintNs)) return true;
             if ((i & 255) == 0) {
                 if (*abort) return false;
                 if (globaltimer_ns() - t0 > kWaitLimit) break;
@@ -246,19 +255,23 @@ __device__ __forceinline__ int valid_blocks(const Walk& w) {
 }
 
 // ------------------------------------------------------------------ kernel
-// Role map (9 warps per CTA):
+// Role map (10 warps per CTA):
 //   S-CTA  warps 0-3  K loaders: warp k brings block k of each tile (3-D boxes)
 //          warp 4     S = Q K^T MMA issuer; owns the TMEM allocation
-//          warps 5-8  softmax, one query row per thread; send P to the O-CTA
+//          warps 5-8  softmax, one query row per thread; stage P
+//          warp 9     P sender: bulk copies of the staged P to the O-CTA
 //   O-CTA  warp 0     V loader: one 4-D box per cache block
 //          warp 1     V landing: zeroes rows past the request, releases the stage
 //          warp 2     L2 prefetcher of upcoming cache blocks
 //          warp 4     O += P V MMA issuer; owns the TMEM allocation
 //          warps 5-8  rescale and epilogue, one query row per thread
+//          warp 3     P landed: tells the S-CTA its P staging may be refilled
+//          warp 9     idle
 template <int W>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_pair_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap qmap,
-                       const __grid_constant__ CUtensorMap vmap, const Params p) {
+                       const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
+                       const Params p) {
     constexpr int NKC = W / 64;  // 64-column chunks in a cache row (9 or 8)
     extern __shared__ __align__(1024) unsigned char smem[];
     Ctrl& c = *reinterpret_cast<Ctrl*>(smem + kCtrlOff);
@@ -267,6 +280,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int pair = blockIdx.x >> 1;
     Waiter wt{&c.abort, p.dev_err};
 
+    grid_dependents_launch();  // the combine kernel may be scheduled (it waits for this grid)
     if ((smem_u32(smem) & 1023) != 0) {  // swizzled operands need 1 KB alignment
         if (tid == 0 && p.dev_err) atomicOr(p.dev_err, (int32_t)MLA_DEVERR_TIMEOUT);
         return;  // both CTAs take this path together (same layout)
@@ -292,7 +306,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(&c.evtdone), 128);
         mbar_init(smem_u32(&c.statfull), 1);
         mbar_init(smem_u32(&c.rowbar), 128);
-        mbar_init(smem_u32(&c.stg_rdy), 64);
+        mbar_init(smem_u32(&c.stg_rdy), 128);
         mbar_init(smem_u32(&c.stg_free), 1);
         c.abort = 0;
         c.landed = 0;
@@ -400,14 +414,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     mma_commit(smem_u32(&c.empty[s]));
                 }
             }
+        } else if (warp == 9) {
+            // ---------------- P sender: ships the staged rows 0..63 of each tile's P
+            // and its rescale message by bulk copies once the O-CTA's P slot is free
+            if (elect_one()) {
+                const uint32_t pslot_remote = mapa(smem_u32(smem + kSideOff), 1);
+                const uint32_t amsg_remote = mapa(smem_u32(&c.amsg[0]), 1);
+                const uint32_t pfull_remote = mapa(smem_u32(&c.pfull[0]), 1);
+                long long i = 0;
+                for (; w.u < w.u_end; walk_next(p, w), ++i) {
+                    const int buf = (int)(i & 1);
+                    if (!wt.wait(smem_u32(&c.stg_rdy), (uint32_t)(i & 1))) break;
+                    // P slot free? (the O-CTA's P*V two tiles back)
+                    if (!wt.wait(smem_u32(&c.pempty[buf]), (uint32_t)((i >> 1) & 1) ^ 1)) break;
+                    const int grows = min(128, Mq - w.g * 128);
+                    const uint32_t pbar = pfull_remote + buf * 8;
+                    bulk_s2cluster(pslot_remote + buf * kPBytes, smem_u32(smem + kStg0Off),
+                                   (uint32_t)(min(64, grows) * 128), pbar);
+                    bulk_s2cluster(amsg_remote + buf * (uint32_t)sizeof(AlphaMsg), smem_u32(&c.astg),
+                                   (uint32_t)sizeof(AlphaMsg), pbar);
+                }
+                // (the staging is released by the O-CTA once the copies have landed:
+                // a copy into another CTA's shared memory completes on the
+                // destination's barrier, so nothing here can tell when it has read)
+            }
         } else if (warp >= 5) {
             // ---------------- softmax rows (warps 5..8), one query row per thread
             const int q = warp & 3;
             const int r = q * 32 + lane;
             const uint32_t lane_off = (uint32_t)(q * 32) << 16;
             const uint32_t pslot_remote = mapa(smem_u32(smem + kSideOff), 1);
-            const uint32_t alpha_remote = mapa(smem_u32(&c.alpha[0][0]), 1);
-            const uint32_t flags_remote = mapa(smem_u32(&c.flags[0][0]), 1);
             const uint32_t pfull_remote = mapa(smem_u32(&c.pfull[0]), 1);
             const uint32_t mstat_remote = mapa(smem_u32(&c.mstat[0]), 1);
             const uint32_t lstat_remote = mapa(smem_u32(&c.lstat[0]), 1);
@@ -532,46 +568,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 l = l * alpha + (ps0 + ps1);
                 const int need = (!first_tile && alpha != 1.f) ? 1 : 0;
                 const unsigned any = __ballot_sync(0xffffffffu, need);
-                // P slot free? (the O-CTA's P*V two tiles back)
-                if (!wt.wait_warp(smem_u32(&c.pempty[buf]), (uint32_t)((i >> 1) & 1) ^ 1)) break;
-                const uint32_t pbar = pfull_remote + buf * 8;
                 if (r >= 64) {
+                    // rows 64..127: straight into the O-CTA's P slot once it is free
+                    if (!wt.wait_warp(smem_u32(&c.pempty[buf]), (uint32_t)((i >> 1) & 1) ^ 1)) break;
                     if (row_ok) {  // rows past the group are never read back
                         const uint32_t prow = pslot_remote + buf * kPBytes + r * 128;
 #pragma unroll
                         for (int u = 0; u < 8; ++u)
                             st_async_v4(prow + ((u ^ (r & 7)) << 4), pk[4 * u], pk[4 * u + 1],
-                                        pk[4 * u + 2], pk[4 * u + 3], pbar);
+                                        pk[4 * u + 2], pk[4 * u + 3], pfull_remote + buf * 8);
                     }
-                } else {
-                    // rows 0..63: stage locally, then one bulk copy to the P slot
-                    const uint32_t stg = smem_u32(smem + kStg0Off);
-                    if (r == 0) {
-                        bulk_wait_read_all();  // the previous copy has left the region
-                        mbar_arrive(smem_u32(&c.stg_free));
-                    }
-                    __syncwarp();
-                    if (!wt.wait_warp(smem_u32(&c.stg_free), (uint32_t)(i & 1))) break;
+                }
+                // the staging (rows 0..63 and the rescale message) is free once the
+                // previous tile's copies have landed in the O-CTA
+                if (!wt.wait_warp(smem_u32(&c.stg_free), (uint32_t)(i & 1) ^ 1)) break;
+                if (r < 64) {
+                    const uint32_t stg = smem_u32(smem + kStg0Off) + r * 128;
 #pragma unroll
                     for (int u = 0; u < 8; ++u)
-                        st_shared_v4(stg + r * 128 + ((u ^ (r & 7)) << 4), pk[4 * u],
-                                     pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-                    fence_proxy_async_smem();
-                    mbar_arrive(smem_u32(&c.stg_rdy));
-                    if (r == 0) {
-                        const int grows = min(128, Mq - w.g * 128);
-                        const int nrows = min(64, grows);
-                        if (wt.wait(smem_u32(&c.stg_rdy), (uint32_t)(i & 1)) && nrows > 0) {
-                            bulk_s2cluster(pslot_remote + buf * kPBytes, stg,
-                                           (uint32_t)(nrows * 128), pbar);
-                            bulk_commit();
-                        }
-                    }
-                    __syncwarp();
+                        st_shared_v4(stg + ((u ^ (r & 7)) << 4), pk[4 * u], pk[4 * u + 1],
+                                     pk[4 * u + 2], pk[4 * u + 3]);
                 }
-                if (row_ok)
-                    st_async_b32(alpha_remote + (buf * 128 + r) * 4, __float_as_uint(alpha), pbar);
-                if (lane == 0) st_async_b32(flags_remote + (buf * 4 + q) * 4, any ? 1u : 0u, pbar);
+                c.astg.alpha[r] = alpha;
+                if (lane == 0) c.astg.flags[q] = any ? 1 : 0;
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(&c.stg_rdy));
                 if (seg_last(w)) {
                     // invalid block ids anywhere in the segment void it (the producer
                     // loaded a stand-in block): the row threads scan its table slice
@@ -601,9 +622,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     ++seg;
                 }
             }
-            // the bulk copies must finish before the CTA may exit
-            if (r == 0) bulk_wait_all();
-            __syncwarp();
         }
     } else if (has_work) {
         // =============================== O-CTA ===============================
@@ -659,6 +677,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     *(volatile int32_t*)&c.landed = (int32_t)(i + 1);
                 }
             }
+        } else if (warp == 3) {
+            // ---------------- P landed: arms each tile's pfull with the bytes the
+            // S-CTA sends (bulk copies and st.async, complete_tx); once the phase
+            // completes, tells the S-CTA it may refill the staging they read
+            if (elect_one()) {
+                const uint32_t stg_free_remote = mapa(smem_u32(&c.stg_free), 0);
+                long long i = 0;
+                for (; w.u < w.u_end; walk_next(p, w), ++i) {
+                    const int slot = (int)(i & 1);
+                    const int grows = min(128, Mq - w.g * 128);
+                    mbar_arrive_expect_tx(smem_u32(&c.pfull[slot]),
+                                          (uint32_t)(grows * 128 + sizeof(AlphaMsg)));
+                    if (!wt.wait(smem_u32(&c.pfull[slot]), (uint32_t)((i >> 1) & 1))) break;
+                    mbar_arrive_remote(stg_free_remote);
+                }
+            }
         } else if (warp == 2) {
             // ---------------- L2 prefetcher: pulls the cache blocks of the tiles
             // kPrefetchAhead past the V landing point into L2 (plain prefetches,
@@ -690,16 +724,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (; w.u < w.u_end; walk_next(p, w), ++i) {
                     const int s = (int)(i % kNS);
                     const int slot = (int)(i & 1);
-                    // this tile's P rows, alphas and flags arrive by st.async (complete_tx)
-                    {
-                        const int grows = min(128, Mq - w.g * 128);
-                        mbar_arrive_expect_tx(smem_u32(&c.pfull[slot]),
-                                              (uint32_t)(grows * (128 + 4) + 4 * 4));
-                    }
+                    // (this tile's P rows and rescale message: pfull, armed by warp 3)
                     if (!wt.wait(smem_u32(&c.vready[s]), (uint32_t)((i / kNS) & 1))) break;
                     if (!wt.wait(smem_u32(&c.pfull[slot]), (uint32_t)((i >> 1) & 1))) break;
                     const bool first = seg_first(w, ub);
-                    const volatile int32_t* fl = c.flags[slot];
+                    const volatile int32_t* fl = c.amsg[slot].flags;
                     if (!first && (fl[0] | fl[1] | fl[2] | fl[3])) {
                         // rows whose max moved: rescale O once the issued P*V is done
                         mma_commit(smem_u32(&c.odone));
@@ -724,21 +753,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             mma_ss(tbase + half * 256, sdesc_sw128(pa + kk * 32, 16, 1024),
                                    sdesc_sw128(va + kk * kVBlock + half * 4 * 2048, 2048, 1024),
                                    idesc, !(first && kk == 0));
-                    mma_commit(smem_u32(&c.empty[s]));
+                    const bool last = seg_last(w);
+                    // the last tile of a segment keeps its stage: the epilogue stages
+                    // the output there, then releases it
+                    if (!last) mma_commit(smem_u32(&c.empty[s]));
                     mma_commit_mc(smem_u32(&c.pempty[slot]), 0x1);
-                    if (seg_last(w)) {
+                    if (last) {
                         mma_commit(smem_u32(&c.odone));
                         if (!wt.wait(smem_u32(&c.odone), (uint32_t)(ndone & 1))) break;
                         ++ndone;
                         c.evt_type = 2;
-                        c.evt_slot = 0;
+                        c.evt_slot = s;
                         mbar_arrive(smem_u32(&c.evt));
                         if (!wt.wait(smem_u32(&c.evtdone), (uint32_t)(nevt & 1))) break;
                         ++nevt;
+                        mbar_arrive(smem_u32(&c.empty[s]));
                     }
                 }
             }
-        } else if (warp >= 5) {
+        } else if (warp >= 5 && warp <= 8) {
             // ---------------- row warps: rescale and epilogue
             const int q = warp & 3;
             const int r = q * 32 + lane;
@@ -755,7 +788,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const int type = *(volatile int32_t*)&c.evt_type;
                 if (type == 1) {
                     const int slot = *(volatile int32_t*)&c.evt_slot;
-                    const float a = c.alpha[slot][r];
+                    const float a = c.amsg[slot].alpha[r];
                     if (a != 1.f) {
 #pragma unroll 1
                         for (int cc = 0; cc < 512; cc += 32) {
@@ -775,6 +808,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 // segment epilogue: locate the segment (advance the walk to its end)
                 while (!seg_last(w)) walk_next(p, w);
+                const int stage = *(volatile int32_t*)&c.evt_slot;
                 if (!wt.wait_warp(smem_u32(&c.statfull), (uint32_t)(seg & 1))) break;
                 const float m = c.mstat[r];
                 const float lsum = c.lstat[r];
@@ -788,48 +822,70 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const bool empty = seg_bad || !(lsum > 0.f);
                 const float inv = empty ? 0.f : 1.f / lsum;
                 const float lse_v = empty ? -INFINITY : (m + log2f(lsum)) * 0.69314718055994531f;
-                if (row_ok) {
-                    if (full_seg) {
-                        __nv_bfloat16* dst = p.out + ((long long)w.b * Mq + grow) * 512;
+                bool ok = true;
+                if (full_seg) {
+                    // bf16 rows through the freed V stage: four [128 rows][64 columns]
+                    // swizzled boxes per pass, stored by TMA (rows past the request's
+                    // query rows fall outside the output map and are not written)
+                    const uint32_t stg = smem_u32(smem + stage * kStage);
 #pragma unroll 1
-                        for (int cc = 0; cc < 512; cc += 32) {
-                            uint32_t v[32];
-                            tmem_ld32(tbase + lane_off + cc, v);
+                    for (int pass = 0; pass < 2 && ok; ++pass) {
+#pragma unroll 1
+                        for (int k = 0; k < 4; ++k) {
+                            const int cb = pass * 4 + k;
+                            uint32_t v0[32], v1[32];
+                            tmem_ld32(tbase + lane_off + cb * 64, v0);
+                            tmem_ld32(tbase + lane_off + cb * 64 + 32, v1);
                             tmem_wait_ld();
-                            uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
+                            const uint32_t rowa = stg + k * kQChunk + r * 128;
 #pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                d4[j] = make_uint4(
-                                    pack_bf16x2(__uint_as_float(v[8 * j]) * inv,
-                                                __uint_as_float(v[8 * j + 1]) * inv),
-                                    pack_bf16x2(__uint_as_float(v[8 * j + 2]) * inv,
-                                                __uint_as_float(v[8 * j + 3]) * inv),
-                                    pack_bf16x2(__uint_as_float(v[8 * j + 4]) * inv,
-                                                __uint_as_float(v[8 * j + 5]) * inv),
-                                    pack_bf16x2(__uint_as_float(v[8 * j + 6]) * inv,
-                                                __uint_as_float(v[8 * j + 7]) * inv));
+                            for (int u = 0; u < 8; ++u) {
+                                const uint32_t* x = u < 4 ? &v0[8 * u] : &v1[8 * (u - 4)];
+                                st_shared_v4(rowa + ((u ^ (r & 7)) << 4),
+                                             pack_bf16x2(__uint_as_float(x[0]) * inv, __uint_as_float(x[1]) * inv),
+                                             pack_bf16x2(__uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv),
+                                             pack_bf16x2(__uint_as_float(x[4]) * inv, __uint_as_float(x[5]) * inv),
+                                             pack_bf16x2(__uint_as_float(x[6]) * inv, __uint_as_float(x[7]) * inv));
+                            }
                         }
-                        if (p.lse) p.lse[(long long)w.b * Mq + grow] = lse_v;
-                    } else {
-                        const int slot = pair * 2 + (seg == 0 ? 0 : 1);
-                        float* dst = p.ws_o + ((long long)slot * 128 + r) * 512;
+                        fence_proxy_async_smem();
+                        if (!rows_sync(wt, smem_u32(&c.rowbar), rphase)) { ok = false; break; }
+                        if (r == 0) {
 #pragma unroll 1
-                        for (int cc = 0; cc < 512; cc += 32) {
-                            uint32_t v[32];
-                            tmem_ld32(tbase + lane_off + cc, v);
-                            tmem_wait_ld();
-                            float4* d4 = reinterpret_cast<float4*>(dst + cc);
+                            for (int k = 0; k < 4; ++k)
+                                tma_store_3d(&omap, stg + k * kQChunk, (pass * 4 + k) * 64, w.g * 128, w.b);
+                            bulk_commit();
+                            bulk_wait_read_all();
+                        }
+                        if (!rows_sync(wt, smem_u32(&c.rowbar), rphase)) { ok = false; break; }
+                    }
+                    if (row_ok && p.lse) p.lse[(long long)w.b * Mq + grow] = lse_v;
+                } else if (row_ok) {
+                    // f32 partial; layout [slot][column quad][128 rows][4], so the 32
+                    // lanes of a store write 512 contiguous bytes. TMEM is read four
+                    // 32-column blocks at a time (one wait per 128 columns).
+                    const int slot = pair * 2 + (seg == 0 ? 0 : 1);
+                    float4* dst = reinterpret_cast<float4*>(p.ws_o + (long long)slot * 128 * 512) + r;
+#pragma unroll 1
+                    for (int cc = 0; cc < 512; cc += 128) {
+                        uint32_t v[4][32];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) tmem_ld32(tbase + lane_off + cc + 32 * k, v[k]);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
 #pragma unroll
                             for (int j = 0; j < 8; ++j)
-                                d4[j] = make_float4(__uint_as_float(v[4 * j]) * inv,
-                                                    __uint_as_float(v[4 * j + 1]) * inv,
-                                                    __uint_as_float(v[4 * j + 2]) * inv,
-                                                    __uint_as_float(v[4 * j + 3]) * inv);
-                        }
-                        p.ws_lse[(long long)slot * 128 + r] =
-                            seg_bad ? __int_as_float(0x7fc00000) : lse_v;  // NaN marks bad
+                                dst[((cc + 32 * k) / 4 + j) * 128] =
+                                    make_float4(__uint_as_float(v[k][4 * j]) * inv,
+                                                __uint_as_float(v[k][4 * j + 1]) * inv,
+                                                __uint_as_float(v[k][4 * j + 2]) * inv,
+                                                __uint_as_float(v[k][4 * j + 3]) * inv);
                     }
+                    p.ws_lse[(long long)slot * 128 + r] =
+                        seg_bad ? __int_as_float(0x7fc00000) : lse_v;  // NaN marks bad
                 }
+                if (!ok) break;
                 tc_fence_before();
                 mbar_arrive(smem_u32(&c.evtdone));
                 ++seg;
@@ -840,6 +896,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     seg_tile0 = w.tile;
                 }
             }
+            if (r == 0) bulk_wait_all();  // the epilogue's TMA stores have completed
+            __syncwarp();
         }
     }
 
@@ -851,52 +909,73 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ combine
-// One warp per query row of every (request, row group): merges the partial
-// segments of row groups that were split across pairs (LSE-weighted, in pair
-// order), and writes the rows of empty or invalid requests.
-constexpr int kCombineWarps = 8;
+// Merges the partial segments of row groups that were split across pairs
+// (LSE-weighted, in pair order) and writes the rows of empty or invalid
+// requests. One CTA per (request, row group, 16-column slice); thread t takes
+// row t % 128 and column quad t / 128 of the slice, so a warp reads 32
+// consecutive rows of one quad (512 contiguous bytes). A thread loads the LSEs
+// and its quads of up to kCombineBatch parts at once, then merges them with a
+// running maximum: one memory round trip per batch of parts.
+//
+// Launched as a programmatic dependent of the decode kernel: everything up to
+// the partials' first read overlaps the decode kernel's tail.
+constexpr int kCombineThreads = 512;
+constexpr int kCombineSlices = 32;
+constexpr int kCombineBatch = 16;
 
-__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Params p) {
-    const int lane = threadIdx.x & 31;
-    const long long gw = (long long)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const Params p) {
+    __shared__ long long sh_u[2];
+    const int tid = threadIdx.x, lane = tid & 31;
     const int Mq = p.T * p.H;
     const int G = (Mq + 127) / 128;
-    const long long bg = gw / 128;
-    const int rr = (int)(gw % 128);
+    const int slice = (int)(blockIdx.x % kCombineSlices);
+    const long long bg = blockIdx.x / kCombineSlices;
     if (bg >= (long long)p.B * G) return;
     const int b = (int)(bg / G), g = (int)(bg % G);
     const int rows = min(128, Mq - g * 128);
-    if (rr >= rows) return;
-    const long long orow = (long long)b * Mq + g * 128 + rr;
+    const int r = tid & 127;
+    const int quad = tid >> 7;                 // 0..3
+    const int col = slice * 16 + quad * 4;
     const int S = p.seq_lens[b];
     const int nt = ntiles_of(S, p.T, p.max_blocks);
-    __nv_bfloat16* dst = p.out + orow * 512;
+    const long long orow = (long long)b * Mq + g * 128 + r;
+    // the unit range of (b, g) and the total, as the decode kernel partitions
+    if (tid < 32 && nt > 0) {
+        long long U = 0, before = 0;
+        for (int b0 = 0; b0 < p.B; b0 += 32) {
+            const int bb = b0 + lane;
+            long long v = bb < p.B ? (long long)ntiles_of(p.seq_lens[bb], p.T, p.max_blocks) * G : 0;
+            long long vb = bb < b ? v : 0;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                v += __shfl_xor_sync(0xffffffffu, v, o);
+                vb += __shfl_xor_sync(0xffffffffu, vb, o);
+            }
+            U += v;
+            before += vb;
+        }
+        if (lane == 0) {
+            sh_u[0] = U;
+            sh_u[1] = before;
+        }
+    }
+    // from here on the decode kernel's results (and the output rows it may
+    // also write) are touched: wait for it to complete
+    grid_dependency_wait();
     if (nt == 0) {
-        if (g == 0 && rr == 0 && lane == 0 && p.dev_err) {
+        if (slice == 0 && g == 0 && tid == 0 && p.dev_err) {
             if (S < 0 || (S > 0 && S < p.T)) atomicOr(p.dev_err, (int32_t)MLA_DEVERR_SEQ_SHORT);
             else if (S > p.max_blocks * 16) atomicOr(p.dev_err, (int32_t)MLA_DEVERR_SEQ_TOO_LONG);
         }
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-            reinterpret_cast<uint4*>(dst)[lane + 32 * j] = make_uint4(0, 0, 0, 0);
-        if (lane == 0 && p.lse) p.lse[orow] = -INFINITY;
+        if (r < rows) {
+            *reinterpret_cast<uint2*>(p.out + orow * 512 + col) = make_uint2(0u, 0u);
+            if (slice == 0 && quad == 0 && p.lse) p.lse[orow] = -INFINITY;
+        }
         return;
     }
-    // the unit range of (b, g) and the total, as the decode kernel partitions
-    long long U = 0, before = 0;
-    for (int b0 = 0; b0 < p.B; b0 += 32) {
-        const int bb = b0 + lane;
-        long long v = bb < p.B ? (long long)ntiles_of(p.seq_lens[bb], p.T, p.max_blocks) * G : 0;
-        long long vb = bb < b ? v : 0;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            v += __shfl_xor_sync(0xffffffffu, v, o);
-            vb += __shfl_xor_sync(0xffffffffu, vb, o);
-        }
-        U += v;
-        before += vb;
-    }
-    const long long u0 = before + (long long)g * nt, u1 = u0 + nt;
+    __syncthreads();
+    const long long U = sh_u[0];
+    const long long u0 = sh_u[1] + (long long)g * nt, u1 = u0 + nt;
     int np = p.NP;
     const long long cap = (U + p.min_units - 1) / p.min_units;
     if (cap < np) np = (int)(cap > 0 ? cap : 1);
@@ -907,72 +986,53 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Param
         return (int)pp;
     };
     const int pf = owner(u0), pl = owner(u1 - 1);
-    if (pf == pl) return;  // one pair held the whole row group and wrote it
+    if (pf == pl || r >= rows) return;  // one pair held the whole row group and wrote it
     const int nparts = pl - pf + 1;
-    auto slot_of = [&](int k) {
-        const int pp = pf + k;
-        return pp * 2 + ((U * pp / np) >= u0 ? 0 : 1);  // first or last segment of pp
-    };
-    // part LSEs: lane k holds parts k, k + 32, ...
-    float M = -INFINITY;
-    int bad = 0;
-    for (int k = lane; k < nparts; k += 32) {
-        const float ls = p.ws_lse[(long long)slot_of(k) * 128 + rr];
-        bad |= (ls != ls);
-        M = fmaxf(M, ls);
-    }
+    // part k is pair pf + k's first segment, or its last one when that pair's
+    // range starts before this row group (only pair pf can)
+    float m = -INFINITY, wsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    bool bad = false;
+    for (int k0 = 0; k0 < nparts; k0 += kCombineBatch) {
+        const int nk = min(kCombineBatch, nparts - k0);
+        float ls[kCombineBatch];
+        float4 v[kCombineBatch];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        bad |= __shfl_xor_sync(0xffffffffu, bad, o);
-    }
-    float acc[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-    float wsum = 0.f;
-    if (!bad && M > -INFINITY) {
-        for (int k0 = 0; k0 < nparts; k0 += 4) {
-            float4 v[4][4];
-            float wk[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int k = k0 + q;
-                wk[q] = 0.f;
-                if (k < nparts) {
-                    const long long slot = slot_of(k);
-                    const float ls = p.ws_lse[slot * 128 + rr];
-                    wk[q] = (ls == -INFINITY) ? 0.f : expf(ls - M);
-                    const float4* src = reinterpret_cast<const float4*>(p.ws_o + (slot * 128 + rr) * 512);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) v[q][j] = src[lane + 32 * j];
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) v[q][j] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
+        for (int j = 0; j < kCombineBatch; ++j) {
+            if (j < nk) {
+                const int pp = pf + k0 + j;
+                const long long slot = pp * 2 + ((U * pp / np) >= u0 ? 0 : 1);
+                ls[j] = p.ws_lse[slot * 128 + r];
+                v[j] = reinterpret_cast<const float4*>(p.ws_o)[(slot * 128 + slice * 4 + quad) * 128 + r];
             }
+        }
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                wsum += wk[q];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    acc[4 * j] += wk[q] * v[q][j].x;
-                    acc[4 * j + 1] += wk[q] * v[q][j].y;
-                    acc[4 * j + 2] += wk[q] * v[q][j].z;
-                    acc[4 * j + 3] += wk[q] * v[q][j].w;
+        for (int j = 0; j < kCombineBatch; ++j) {
+            if (j < nk) {
+                bad |= (ls[j] != ls[j]);
+                if (ls[j] > m) {  // a new maximum: rescale what has been summed
+                    const float a = (m == -INFINITY) ? 0.f : expf(m - ls[j]);
+                    wsum *= a;
+                    acc.x *= a;
+                    acc.y *= a;
+                    acc.z *= a;
+                    acc.w *= a;
+                    m = ls[j];
                 }
+                const float wk = (ls[j] == -INFINITY) ? 0.f : expf(ls[j] - m);
+                wsum += wk;
+                acc.x += wk * v[j].x;
+                acc.y += wk * v[j].y;
+                acc.z += wk * v[j].z;
+                acc.w += wk * v[j].w;
             }
         }
     }
     const bool empty = bad || !(wsum > 0.f);
     const float inv = empty ? 0.f : 1.f / wsum;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        uint2 o;
-        o.x = pack_bf16x2(acc[4 * j] * inv, acc[4 * j + 1] * inv);
-        o.y = pack_bf16x2(acc[4 * j + 2] * inv, acc[4 * j + 3] * inv);
-        reinterpret_cast<uint2*>(dst)[lane + 32 * j] = o;
-    }
-    if (lane == 0 && p.lse) p.lse[orow] = empty ? -INFINITY : M + logf(wsum);
+    *reinterpret_cast<uint2*>(p.out + orow * 512 + col) =
+        make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+    if (slice == 0 && quad == 0 && p.lse) p.lse[orow] = empty ? -INFINITY : m + logf(wsum);
 }
 
 // ------------------------------------------------------------------ host
@@ -1116,6 +1176,23 @@ cudaError_t launch_decode_tc(void* out, float* lse, const void* q_abs, const voi
             return cudaErrorInvalidValue;
         }
     }
+    CUtensorMap omap;
+    {
+        // output rows as {512 columns, t_q * n_head rows, batch}: a 128-row box of
+        // one request never spills into the next request's rows
+        const int Mq = d.t_q * d.n_head;
+        cuuint64_t odims[3] = {512, (cuuint64_t)Mq, (cuuint64_t)batch};
+        cuuint64_t ostrides[2] = {512 * 2, (cuuint64_t)Mq * 512 * 2};
+        cuuint32_t obox[3] = {64, (cuuint32_t)(Mq < 128 ? Mq : 128), 1};
+        cuuint32_t oes[3] = {1, 1, 1};
+        cr = enc(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out, odims, ostrides, obox, oes,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr != CUDA_SUCCESS) {
+            set_error("cuTensorMapEncodeTiled (output) failed (%d)", (int)cr);
+            return cudaErrorInvalidValue;
+        }
+    }
     Params p;
     p.q_abs = (const __nv_bfloat16*)q_abs;
     p.kv = (const __nv_bfloat16*)kv_cache;
@@ -1149,14 +1226,23 @@ cudaError_t launch_decode_tc(void* out, float* lse, const void* q_abs, const voi
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (W == 576)
-        e = cudaLaunchKernelEx(&cfg, decode_pair_kernel<576>, tmap, qmap, vmap, p);
+        e = cudaLaunchKernelEx(&cfg, decode_pair_kernel<576>, tmap, qmap, vmap, omap, p);
     else
-        e = cudaLaunchKernelEx(&cfg, decode_pair_kernel<512>, tmap, qmap, vmap, p);
+        e = cudaLaunchKernelEx(&cfg, decode_pair_kernel<512>, tmap, qmap, vmap, omap, p);
     if (e != cudaSuccess) return e;
     const long long G = (d.t_q * d.n_head + 127) / 128;
-    const long long warps = (long long)batch * G * 128;
-    combine_kernel<<<(unsigned)((warps + kCombineWarps - 1) / kCombineWarps), kCombineWarps * 32,
-                     0, s>>>(p);
+    cudaLaunchConfig_t ccfg = {};
+    cudaLaunchAttribute cattr[1];
+    cattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    cattr[0].val.programmaticStreamSerializationAllowed = 1;
+    ccfg.gridDim = dim3((unsigned)((long long)batch * G * kCombineSlices), 1, 1);
+    ccfg.blockDim = dim3(kCombineThreads, 1, 1);
+    ccfg.dynamicSmemBytes = 0;
+    ccfg.stream = s;
+    ccfg.attrs = cattr;
+    ccfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&ccfg, combine_kernel, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
