@@ -53,38 +53,31 @@ constexpr int kPBytes = 128 * 128;            // P [128 rows x 64 tokens] bf16
 constexpr int kCtrlOff = kSideOff + 2 * kPBytes;
 constexpr int kQChunk = 128 * 128;            // 128 query rows x 64 columns of bf16
 constexpr int kVBlock = 8 * 2048;             // O-CTA: one block's V as [8 chunks][16 rows][128 B]
-// S-CTA: P rows 0..63 are staged in [216 KB, 224 KB) (unused in the S-CTA)
-// and shipped by the sender warp's bulk copy; rows 64..127 go straight from
-// their threads by st.async. Both paths share the SM-to-SM bandwidth (about
-// 40 GB/s); splitting them keeps each short, and the staging leaves the cache
-// pipeline's stages alone.
-constexpr int kStg0Off = kSideOff + 3 * kChunk;
-static_assert(kStg0Off + 64 * 128 <= kCtrlOff, "staging region");
 // the first segment's queries sit in stages 1-2 (latent chunks 0..7) and in
 // the rope chunks of stages 1-2 (chunk 8); tile 0 uses stage 0 meanwhile
 __host__ __device__ constexpr int q_chunk_off(int cc) {
     return cc < 8 ? kStage + cc * kQChunk : kSideOff + kChunk;
 }
 static_assert(kSideOff + kChunk + kQChunk <= kSideOff + 3 * kChunk, "q chunk 8 placement");
-constexpr int kThreads = 320;                 // see the role map in the kernel
+constexpr int kThreads = 416;                 // see the role map in the kernel
+constexpr int kSmxWarps = 8;                  // S-CTA softmax warps: two threads per query row
 constexpr uint64_t kWaitLimit = 2000000000ull;  // ns before a wait gives up
 constexpr uint32_t kSuspendHintNs = 1000;     // longest suspension of one wait poll
 constexpr float kRescaleThreshold = 8.0f;     // lazy rescale, log2 units
 constexpr int kPrefetchAhead = 6;             // tiles the L2 prefetcher runs ahead of V landing
 
-// per-tile rescale message from the S-CTA's softmax to the O-CTA (one bulk copy)
+// per-tile rescale message from the S-CTA's softmax to the O-CTA (st.async)
 struct __align__(16) AlphaMsg {
-    float alpha[128];       // per-row rescale factors of the P slot
-    int32_t flags[4];       // per softmax warp, some row needs a rescale
+    float alpha[128];           // per-row rescale factors of the P slot
+    int32_t flags[kSmxWarps];   // per softmax warp, some row needs a rescale
 };
 
 struct Ctrl {
     AlphaMsg amsg[2];       // O: the messages of the two P slots
-    AlphaMsg astg;          // S: staging of the current tile's message
     uint64_t full[kNS];     // both: this CTA's part of the tile landed (complete_tx)
     uint64_t empty[kNS];    // both: stage free (own QK / P*V commit)
     uint64_t sfull[2];      // S: scores ready (QK commit)
-    uint64_t sfree[2];      // S: scores read (128 softmax threads)
+    uint64_t sfree[2];      // S: scores read (the 256 softmax threads)
     uint64_t pempty[2];     // S: P slot consumed (O-CTA PV commit)
     uint64_t qready;        // S: Q stored in TMEM (128 threads)
     uint64_t qland;         // S: first segment's queries landed in shared memory (TMA)
@@ -96,15 +89,13 @@ struct Ctrl {
     uint64_t evt;           // O: MMA warp -> row warps event
     uint64_t evtdone;       // O: row warps -> MMA warp (128)
     uint64_t statfull;      // O: segment statistics written (1 remote)
-    uint64_t rowbar;        // both: barrier among the 128 row threads
-    uint64_t stg_rdy;       // S: the tile's P is staged (128 arrivals)
-    uint64_t stg_free;      // S: the previous tile's P has landed in the O-CTA (1 remote arrival)
+    uint64_t rowbar;        // both: barrier among the row threads (S: 256, O: 128)
     uint32_t tmem_base;
     int32_t abort;
     int32_t evt_type;       // 1 = rescale slot evt_slot, 2 = segment epilogue
     int32_t evt_slot;
     int32_t bad;            // O: the segment met an invalid block id
-    int32_t badw[4];        // S: per row warp, the segment met an invalid block id
+    int32_t badw[kSmxWarps];  // S: per softmax warp, the segment met an invalid block id
     int32_t landed;         // O: tiles whose V has landed (paces the L2 prefetcher)
     float mstat[128];       // O: segment max (log2 units) per row
     float lstat[128];       // O: segment sum per row
@@ -255,18 +246,17 @@ __device__ __forceinline__ int valid_blocks(const Walk& w) {
 }
 
 // ------------------------------------------------------------------ kernel
-// Role map (10 warps per CTA):
+// Role map (13 warps per CTA):
 //   S-CTA  warps 0-3  K loaders: warp k brings block k of each tile (3-D boxes)
 //          warp 4     S = Q K^T MMA issuer; owns the TMEM allocation
-//          warps 5-8  softmax, one query row per thread; stage P
-//          warp 9     P sender: bulk copies of the staged P to the O-CTA
+//          warps 5-12 softmax, two threads per query row (32 score columns
+//                     each); P goes to the O-CTA by st.async
 //   O-CTA  warp 0     V loader: one 4-D box per cache block
 //          warp 1     V landing: zeroes rows past the request, releases the stage
 //          warp 2     L2 prefetcher of upcoming cache blocks
 //          warp 4     O += P V MMA issuer; owns the TMEM allocation
 //          warps 5-8  rescale and epilogue, one query row per thread
-//          warp 3     P landed: tells the S-CTA its P staging may be refilled
-//          warp 9     idle
+//          warps 3, 9-12 idle
 template <int W>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_pair_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap qmap,
@@ -293,7 +283,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&c.sfull[i]), 1);
-            mbar_init(smem_u32(&c.sfree[i]), 128);
+            mbar_init(smem_u32(&c.sfree[i]), kSmxWarps * 32);
             mbar_init(smem_u32(&c.pempty[i]), 1);
             mbar_init(smem_u32(&c.pfull[i]), 1);
         }
@@ -305,9 +295,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(&c.evt), 1);
         mbar_init(smem_u32(&c.evtdone), 128);
         mbar_init(smem_u32(&c.statfull), 1);
-        mbar_init(smem_u32(&c.rowbar), 128);
-        mbar_init(smem_u32(&c.stg_rdy), 128);
-        mbar_init(smem_u32(&c.stg_free), 1);
+        mbar_init(smem_u32(&c.rowbar), rank == 0 ? kSmxWarps * 32 : 128);
         c.abort = 0;
         c.landed = 0;
         fence_mbar_init();
@@ -414,37 +402,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     mma_commit(smem_u32(&c.empty[s]));
                 }
             }
-        } else if (warp == 9) {
-            // ---------------- P sender: ships the staged rows 0..63 of each tile's P
-            // and its rescale message by bulk copies once the O-CTA's P slot is free
-            if (elect_one()) {
-                const uint32_t pslot_remote = mapa(smem_u32(smem + kSideOff), 1);
-                const uint32_t amsg_remote = mapa(smem_u32(&c.amsg[0]), 1);
-                const uint32_t pfull_remote = mapa(smem_u32(&c.pfull[0]), 1);
-                long long i = 0;
-                for (; w.u < w.u_end; walk_next(p, w), ++i) {
-                    const int buf = (int)(i & 1);
-                    if (!wt.wait(smem_u32(&c.stg_rdy), (uint32_t)(i & 1))) break;
-                    // P slot free? (the O-CTA's P*V two tiles back)
-                    if (!wt.wait(smem_u32(&c.pempty[buf]), (uint32_t)((i >> 1) & 1) ^ 1)) break;
-                    const int grows = min(128, Mq - w.g * 128);
-                    const uint32_t pbar = pfull_remote + buf * 8;
-                    bulk_s2cluster(pslot_remote + buf * kPBytes, smem_u32(smem + kStg0Off),
-                                   (uint32_t)(min(64, grows) * 128), pbar);
-                    bulk_s2cluster(amsg_remote + buf * (uint32_t)sizeof(AlphaMsg), smem_u32(&c.astg),
-                                   (uint32_t)sizeof(AlphaMsg), pbar);
-                }
-                // (the staging is released by the O-CTA once the copies have landed:
-                // a copy into another CTA's shared memory completes on the
-                // destination's barrier, so nothing here can tell when it has read)
-            }
         } else if (warp >= 5) {
-            // ---------------- softmax rows (warps 5..8), one query row per thread
+            // ---------------- softmax (warps 5..12): warp w reads the 16 TMEM lanes
+            // 32 (w % 4) + 16 h (h = 0 for warps 5..8, 1 for 9..12) with the 16x64b
+            // shape; the two threads of a query row hold its even and odd score
+            // columns, share the row max by one shuffle and swap halves so each
+            // packs 32 adjacent columns of P
             const int q = warp & 3;
-            const int r = q * 32 + lane;
-            const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+            const int h = warp >= 9 ? 1 : 0;
+            const int sw = warp - 5;                                  // 0..7
+            const int R = q * 32 + h * 16 + (lane >> 2) + 8 * (lane & 1);  // query row
+            const int par = (lane >> 1) & 1;                          // odd columns
+            const uint32_t lane_base16 = (uint32_t)(q * 32 + h * 16) << 16;
+            const uint32_t lane_off = (uint32_t)(q * 32) << 16;      // Q moves: warps 5..8
+            const int rq = q * 32 + lane;                             // their row
             const uint32_t pslot_remote = mapa(smem_u32(smem + kSideOff), 1);
             const uint32_t pfull_remote = mapa(smem_u32(&c.pfull[0]), 1);
+            const uint32_t amsg_remote = mapa(smem_u32(&c.amsg[0]), 1);
             const uint32_t mstat_remote = mapa(smem_u32(&c.mstat[0]), 1);
             const uint32_t lstat_remote = mapa(smem_u32(&c.lstat[0]), 1);
             const uint32_t bad_remote = mapa(smem_u32(&c.bad), 1);
@@ -461,164 +435,163 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const bool first_tile = seg_first(w, ub);
                 if (first_tile) {
                     seg_tile0 = w.tile;
-                    const int grow = w.g * 128 + r;
+                    const int grow = w.g * 128 + R;
                     row_ok = grow < Mq;
                     const int t = row_ok ? grow / p.H : 0;
                     horizon = row_ok ? w.S - p.T + t + 1 : 0;
                     m_used = -INFINITY;
                     l = 0.f;
                     bad = 0;
-                    if (seg == 0) {
-                        // queries landed in shared memory by TMA: move this row to TMEM
-                        if (!wt.wait_warp(smem_u32(&c.qland), 0)) break;
+                    if (h == 0) {
+                        // warps 5..8 move the segment's queries into TMEM, a row each
+                        const int growq = w.g * 128 + rq;
+                        const bool rq_ok = growq < Mq;
+                        if (seg == 0) {
+                            // landed in shared memory by TMA
+                            if (!wt.wait_warp(smem_u32(&c.qland), 0)) break;
 #pragma unroll 1
-                        for (int cc = 0; cc < NKC; ++cc) {
-                            const uint32_t rowa = smem_u32(smem + q_chunk_off(cc)) + r * 128;
-                            uint32_t v[32];
+                            for (int cc = 0; cc < NKC; ++cc) {
+                                const uint32_t rowa = smem_u32(smem + q_chunk_off(cc)) + rq * 128;
+                                uint32_t v[32];
 #pragma unroll
-                            for (int u = 0; u < 8; ++u) {
-                                const uint4 x = ld_shared_v4(rowa + ((u ^ (r & 7)) << 4));
-                                v[4 * u] = row_ok ? x.x : 0u;
-                                v[4 * u + 1] = row_ok ? x.y : 0u;
-                                v[4 * u + 2] = row_ok ? x.z : 0u;
-                                v[4 * u + 3] = row_ok ? x.w : 0u;
+                                for (int u = 0; u < 8; ++u) {
+                                    const uint4 x = ld_shared_v4(rowa + ((u ^ (rq & 7)) << 4));
+                                    v[4 * u] = rq_ok ? x.x : 0u;
+                                    v[4 * u + 1] = rq_ok ? x.y : 0u;
+                                    v[4 * u + 2] = rq_ok ? x.z : 0u;
+                                    v[4 * u + 3] = rq_ok ? x.w : 0u;
+                                }
+                                tmem_st32(tq + lane_off + cc * 32, v);
                             }
-                            tmem_st32(tq + lane_off + cc * 32, v);
-                        }
-                        tmem_wait_st();
-                        mbar_arrive(smem_u32(&c.qfree));  // stages 1 and 2 may be refilled
-                    } else {
-                        // later segments: from global memory (warmed in L2 by the producer)
-                        const uint4* src = reinterpret_cast<const uint4*>(
-                            p.q_abs + ((long long)w.b * Mq + (row_ok ? grow : 0)) * W);
+                            tmem_wait_st();
+                            mbar_arrive(smem_u32(&c.qfree));  // stages 1 and 2 may be refilled
+                        } else {
+                            // later segments: from global memory (warmed in L2 by the loader)
+                            const uint4* src = reinterpret_cast<const uint4*>(
+                                p.q_abs + ((long long)w.b * Mq + (rq_ok ? growq : 0)) * W);
 #pragma unroll 1
-                        for (int cc0 = 0; cc0 < NKC; cc0 += 3) {
-                            uint4 x[3][8];
-#pragma unroll
-                            for (int k = 0; k < 3; ++k)
+                            for (int cc = 0; cc < NKC; ++cc) {
+                                uint4 x[8];
 #pragma unroll
                                 for (int j = 0; j < 8; ++j)
-                                    x[k][j] = (row_ok && cc0 + k < NKC) ? src[(cc0 + k) * 8 + j]
-                                                                       : make_uint4(0, 0, 0, 0);
-#pragma unroll
-                            for (int k = 0; k < 3; ++k) {
-                                if (cc0 + k >= NKC) break;
+                                    x[j] = rq_ok ? src[cc * 8 + j] : make_uint4(0, 0, 0, 0);
                                 uint32_t v[32];
 #pragma unroll
                                 for (int j = 0; j < 8; ++j) {
-                                    v[4 * j] = x[k][j].x;
-                                    v[4 * j + 1] = x[k][j].y;
-                                    v[4 * j + 2] = x[k][j].z;
-                                    v[4 * j + 3] = x[k][j].w;
+                                    v[4 * j] = x[j].x;
+                                    v[4 * j + 1] = x[j].y;
+                                    v[4 * j + 2] = x[j].z;
+                                    v[4 * j + 3] = x[j].w;
                                 }
-                                tmem_st32(tq + lane_off + (cc0 + k) * 32, v);
+                                tmem_st32(tq + lane_off + cc * 32, v);
                             }
+                            tmem_wait_st();
                         }
-                        tmem_wait_st();
+                        tc_fence_before();
+                        mbar_arrive(smem_u32(&c.qready));
                     }
-                    tc_fence_before();
-                    mbar_arrive(smem_u32(&c.qready));
                 }
                 if (!wt.wait_warp(smem_u32(&c.sfull[buf]), (uint32_t)((i >> 1) & 1))) break;
                 tc_fence_after();
-                float x[kTok];
+                float x[32];  // columns 2 j + par
                 {
-                    uint32_t v0[32], v1[32];
-                    tmem_ld32(ts0 + buf * kTok + lane_off, v0);
-                    tmem_ld32(ts0 + buf * kTok + 32 + lane_off, v1);
+                    uint32_t v[32];
+                    tmem_ld16x64(ts0 + buf * kTok + lane_base16, v);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        x[j] = __uint_as_float(v0[j]) * sl2;
-                        x[32 + j] = __uint_as_float(v1[j]) * sl2;
-                    }
+                    for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]) * sl2;
                 }
                 tc_fence_before();
                 mbar_arrive(smem_u32(&c.sfree[buf]));
                 // keys past this row's horizon (only near the request's end)
-                const int j0 = w.tile * kTok;
-                if (j0 + kTok > horizon) {
+                const int j0 = w.tile * kTok + par;
+                if (w.tile * kTok + kTok > horizon) {
 #pragma unroll
-                    for (int j = 0; j < kTok; ++j)
-                        if (j0 + j >= horizon) x[j] = -INFINITY;
+                    for (int j = 0; j < 32; ++j)
+                        if (j0 + 2 * j >= horizon) x[j] = -INFINITY;
                 }
                 float mx0 = x[0], mx1 = x[1];
 #pragma unroll
-                for (int j = 2; j < kTok; j += 2) {
+                for (int j = 2; j < 32; j += 2) {
                     mx0 = fmaxf(mx0, x[j]);
                     mx1 = fmaxf(mx1, x[j + 1]);
                 }
-                const float mx = fmaxf(mx0, mx1);
+                float mx = fmaxf(mx0, mx1);
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
                 float alpha = 1.f;
                 if (mx > m_used + kRescaleThreshold || (m_used == -INFINITY && mx > -INFINITY)) {
                     alpha = (m_used == -INFINITY) ? 1.f : ex2_approx(m_used - mx);
                     m_used = mx;
                 }
                 const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-                uint32_t pk[kTok / 2];
                 float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-                for (int j = 0; j < kTok; j += 2) {
-                    const float a = ex2_approx(x[j] - mref);   // 2^-inf = +0
-                    const float b2 = ex2_approx(x[j + 1] - mref);
-                    ps0 += a;
-                    ps1 += b2;
-                    pk[j / 2] = pack_bf16x2(a, b2);
+                for (int j = 0; j < 32; j += 2) {
+                    x[j] = ex2_approx(x[j] - mref);  // 2^-inf = +0
+                    x[j + 1] = ex2_approx(x[j + 1] - mref);
+                    ps0 += x[j];
+                    ps1 += x[j + 1];
                 }
-                l = l * alpha + (ps0 + ps1);
+                l = l * alpha + (ps0 + ps1);  // this thread's columns; the pair adds at the end
+                // swap halves: the even thread keeps columns 0..31, the odd one 32..63
+                uint32_t pk[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float mine_lo = x[k], mine_hi = x[16 + k];
+                    const float got = __shfl_xor_sync(0xffffffffu, par ? mine_lo : mine_hi, 2);
+                    pk[k] = par ? pack_bf16x2(got, mine_hi) : pack_bf16x2(mine_lo, got);
+                }
                 const int need = (!first_tile && alpha != 1.f) ? 1 : 0;
                 const unsigned any = __ballot_sync(0xffffffffu, need);
-                if (r >= 64) {
-                    // rows 64..127: straight into the O-CTA's P slot once it is free
-                    if (!wt.wait_warp(smem_u32(&c.pempty[buf]), (uint32_t)((i >> 1) & 1) ^ 1)) break;
-                    if (row_ok) {  // rows past the group are never read back
-                        const uint32_t prow = pslot_remote + buf * kPBytes + r * 128;
+                // P slot free? (the O-CTA's P*V two tiles back)
+                if (!wt.wait_warp(smem_u32(&c.pempty[buf]), (uint32_t)((i >> 1) & 1) ^ 1)) break;
+                const uint32_t pbar = pfull_remote + buf * 8;
+                if (row_ok) {  // rows past the group are never read back
+                    const uint32_t prow = pslot_remote + buf * kPBytes + R * 128;
 #pragma unroll
-                        for (int u = 0; u < 8; ++u)
-                            st_async_v4(prow + ((u ^ (r & 7)) << 4), pk[4 * u], pk[4 * u + 1],
-                                        pk[4 * u + 2], pk[4 * u + 3], pfull_remote + buf * 8);
+                    for (int u = 0; u < 4; ++u) {
+                        const int cu = 4 * par + u;  // 16-byte chunk of the row
+                        st_async_v4(prow + ((cu ^ (R & 7)) << 4), pk[4 * u], pk[4 * u + 1],
+                                    pk[4 * u + 2], pk[4 * u + 3], pbar);
                     }
+                    if (par == 0)
+                        st_async_b32(amsg_remote + buf * (uint32_t)sizeof(AlphaMsg) + R * 4,
+                                     __float_as_uint(alpha), pbar);
                 }
-                // the staging (rows 0..63 and the rescale message) is free once the
-                // previous tile's copies have landed in the O-CTA
-                if (!wt.wait_warp(smem_u32(&c.stg_free), (uint32_t)(i & 1) ^ 1)) break;
-                if (r < 64) {
-                    const uint32_t stg = smem_u32(smem + kStg0Off) + r * 128;
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        st_shared_v4(stg + ((u ^ (r & 7)) << 4), pk[4 * u], pk[4 * u + 1],
-                                     pk[4 * u + 2], pk[4 * u + 3]);
-                }
-                c.astg.alpha[r] = alpha;
-                if (lane == 0) c.astg.flags[q] = any ? 1 : 0;
-                fence_proxy_async_smem();
-                mbar_arrive(smem_u32(&c.stg_rdy));
+                if (lane == 0)
+                    st_async_b32(amsg_remote + buf * (uint32_t)sizeof(AlphaMsg) + 512 + sw * 4,
+                                 any ? 1u : 0u, pbar);
                 if (seg_last(w)) {
-                    // invalid block ids anywhere in the segment void it (the producer
-                    // loaded a stand-in block): the row threads scan its table slice
+                    const float l_row = l + __shfl_xor_sync(0xffffffffu, l, 2);
+                    // invalid block ids anywhere in the segment void it (the loader
+                    // loaded a stand-in block): the softmax threads scan its table slice
                     {
                         const int blk0 = seg_tile0 * 4;
                         const int blk1 = min(w.tile * 4 + 4, (w.S + 15) / 16);
                         const int32_t* bt = p.block_table + (long long)w.b * p.max_blocks;
                         int b_any = 0;
-                        for (int k = blk0 + r; k < blk1; k += 128) {
+                        for (int k = blk0 + sw * 32 + lane; k < blk1; k += kSmxWarps * 32) {
                             const int32_t blk = bt[k];
                             b_any |= (blk < 0 || blk >= p.num_blocks);
                         }
                         b_any = __any_sync(0xffffffffu, b_any);
-                        if (lane == 0) c.badw[q] = b_any;
+                        if (lane == 0) c.badw[sw] = b_any;
                     }
                     if (!rows_sync(wt, smem_u32(&c.rowbar), rphase)) break;
-                    bad = c.badw[0] | c.badw[1] | c.badw[2] | c.badw[3];
+                    bad = 0;
+#pragma unroll
+                    for (int k = 0; k < kSmxWarps; ++k) bad |= c.badw[k];
                     // hand the row statistics to the O-CTA
                     if (seg > 0 && !wt.wait_warp(smem_u32(&c.statack), (uint32_t)((seg - 1) & 1))) break;
-                    st_cluster_f32(mstat_remote + r * 4, row_ok ? m_used : -INFINITY);
-                    st_cluster_f32(lstat_remote + r * 4, row_ok ? l : 0.f);
-                    if (r == 0)
+                    if (par == 0) {
+                        st_cluster_f32(mstat_remote + R * 4, row_ok ? m_used : -INFINITY);
+                        st_cluster_f32(lstat_remote + R * 4, row_ok ? l_row : 0.f);
+                    }
+                    if (sw == 0 && lane == 0)
                         asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(bad_remote), "r"(bad)
                                      : "memory");
                     if (!rows_sync(wt, smem_u32(&c.rowbar), rphase)) break;
-                    if (r == 0) mbar_arrive_remote(statfull_remote);
+                    if (sw == 0 && lane == 0) mbar_arrive_remote(statfull_remote);
                     ++seg;
                 }
             }
@@ -677,22 +650,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     *(volatile int32_t*)&c.landed = (int32_t)(i + 1);
                 }
             }
-        } else if (warp == 3) {
-            // ---------------- P landed: arms each tile's pfull with the bytes the
-            // S-CTA sends (bulk copies and st.async, complete_tx); once the phase
-            // completes, tells the S-CTA it may refill the staging they read
-            if (elect_one()) {
-                const uint32_t stg_free_remote = mapa(smem_u32(&c.stg_free), 0);
-                long long i = 0;
-                for (; w.u < w.u_end; walk_next(p, w), ++i) {
-                    const int slot = (int)(i & 1);
-                    const int grows = min(128, Mq - w.g * 128);
-                    mbar_arrive_expect_tx(smem_u32(&c.pfull[slot]),
-                                          (uint32_t)(grows * 128 + sizeof(AlphaMsg)));
-                    if (!wt.wait(smem_u32(&c.pfull[slot]), (uint32_t)((i >> 1) & 1))) break;
-                    mbar_arrive_remote(stg_free_remote);
-                }
-            }
         } else if (warp == 2) {
             // ---------------- L2 prefetcher: pulls the cache blocks of the tiles
             // kPrefetchAhead past the V landing point into L2 (plain prefetches,
@@ -724,12 +681,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (; w.u < w.u_end; walk_next(p, w), ++i) {
                     const int s = (int)(i % kNS);
                     const int slot = (int)(i & 1);
-                    // (this tile's P rows and rescale message: pfull, armed by warp 3)
+                    // this tile's P rows, rescale factors and flags arrive by st.async
+                    {
+                        const int grows = min(128, Mq - w.g * 128);
+                        mbar_arrive_expect_tx(smem_u32(&c.pfull[slot]),
+                                              (uint32_t)(grows * (128 + 4) + kSmxWarps * 4));
+                    }
                     if (!wt.wait(smem_u32(&c.vready[s]), (uint32_t)((i / kNS) & 1))) break;
                     if (!wt.wait(smem_u32(&c.pfull[slot]), (uint32_t)((i >> 1) & 1))) break;
                     const bool first = seg_first(w, ub);
                     const volatile int32_t* fl = c.amsg[slot].flags;
-                    if (!first && (fl[0] | fl[1] | fl[2] | fl[3])) {
+                    int any_flag = 0;
+#pragma unroll
+                    for (int k = 0; k < kSmxWarps; ++k) any_flag |= fl[k];
+                    if (!first && any_flag) {
                         // rows whose max moved: rescale O once the issued P*V is done
                         mma_commit(smem_u32(&c.odone));
                         if (!wt.wait(smem_u32(&c.odone), (uint32_t)(ndone & 1))) break;
@@ -862,18 +827,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (row_ok && p.lse) p.lse[(long long)w.b * Mq + grow] = lse_v;
                 } else if (row_ok) {
                     // f32 partial; layout [slot][column quad][128 rows][4], so the 32
-                    // lanes of a store write 512 contiguous bytes. TMEM is read four
-                    // 32-column blocks at a time (one wait per 128 columns).
+                    // lanes of a store write 512 contiguous bytes. TMEM is read two
+                    // 32-column blocks at a time (one wait per 64 columns).
                     const int slot = pair * 2 + (seg == 0 ? 0 : 1);
                     float4* dst = reinterpret_cast<float4*>(p.ws_o + (long long)slot * 128 * 512) + r;
 #pragma unroll 1
-                    for (int cc = 0; cc < 512; cc += 128) {
-                        uint32_t v[4][32];
+                    for (int cc = 0; cc < 512; cc += 64) {
+                        uint32_t v[2][32];
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) tmem_ld32(tbase + lane_off + cc + 32 * k, v[k]);
+                        for (int k = 0; k < 2; ++k) tmem_ld32(tbase + lane_off + cc + 32 * k, v[k]);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
+                        for (int k = 0; k < 2; ++k)
 #pragma unroll
                             for (int j = 0; j < 8; ++j)
                                 dst[((cc + 32 * k) / 4 + j) * 128] =
