@@ -75,6 +75,8 @@ struct __align__(16) AlphaMsg {
 struct Ctrl {
     AlphaMsg amsg[2];       // O: the messages of the two P slots
     uint64_t full[kNS];     // both: this CTA's part of the tile landed (complete_tx)
+    uint64_t kfree[kNS];    // O: the S-CTA's stage is free (its QK commit, multicast)
+    uint64_t qmoved;        // O: the S-CTA's first queries have left stages 1-2 (1 remote)
     uint64_t empty[kNS];    // both: stage free (own QK / P*V commit)
     uint64_t sfull[2];      // S: scores ready (QK commit)
     uint64_t sfree[2];      // S: scores read (the 256 softmax threads)
@@ -247,7 +249,8 @@ __device__ __forceinline__ int valid_blocks(const Walk& w) {
 
 // ------------------------------------------------------------------ kernel
 // Role map (13 warps per CTA):
-//   S-CTA  warps 0-3  K loaders: warp k brings block k of each tile (3-D boxes)
+//   S-CTA  warps 0-3  K loaders: warp k expects block k of each tile; warps 0-1
+//                     load blocks 0-1 (3-D boxes), the O-CTA's warp 3 blocks 2-3
 //          warp 4     S = Q K^T MMA issuer; owns the TMEM allocation
 //          warps 5-12 softmax, two threads per query row (32 score columns
 //                     each); P goes to the O-CTA by st.async
@@ -256,7 +259,9 @@ __device__ __forceinline__ int valid_blocks(const Walk& w) {
 //          warp 2     L2 prefetcher of upcoming cache blocks
 //          warp 4     O += P V MMA issuer; owns the TMEM allocation
 //          warps 5-8  rescale and epilogue, one query row per thread
-//          warps 3, 9-12 idle
+//          warp 3     K helper: loads blocks 2-3 of each S-CTA tile (multicast
+//                     to the S-CTA only), so both TMA units share the boxes
+//          warps 9-12 idle
 template <int W>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_pair_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap qmap,
@@ -280,6 +285,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&c.full[s]), rank == 0 ? 4 : 1);  // S: one per K loader
             mbar_init(smem_u32(&c.empty[s]), 1);
             mbar_init(smem_u32(&c.vready[s]), 1);
+            mbar_init(smem_u32(&c.kfree[s]), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&c.sfull[i]), 1);
@@ -289,6 +295,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         mbar_init(smem_u32(&c.qready), 128);
         mbar_init(smem_u32(&c.qland), 1);
+        mbar_init(smem_u32(&c.qmoved), 1);
         mbar_init(smem_u32(&c.qfree), 128);
         mbar_init(smem_u32(&c.statack), 1);
         mbar_init(smem_u32(&c.odone), 1);
@@ -349,7 +356,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const bool have = kb < valid_blocks(w);
                     mbar_arrive_expect_tx(smem_u32(&c.full[s]), have ? (uint32_t)(NKC * 2048) : 0u);
                     last_issue[s] = i;
-                    if (have) {
+                    if (have && kb < 2) {
                         int32_t blk = p.block_table[(long long)w.b * p.max_blocks + w.tile * 4 + kb];
                         if (blk < 0 || blk >= p.num_blocks) {
                             // load a valid stand-in; the row threads void the segment
@@ -383,6 +390,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const int buf = (int)(i & 1);
                     if (seg_first(w, ub)) {
                         if (!wt.wait(smem_u32(&c.qready), (uint32_t)(seg & 1))) break;
+                        if (seg == 0) mbar_arrive_remote(mapa(smem_u32(&c.qmoved), 1));
                         ++seg;
                     }
                     if (!wt.wait(smem_u32(&c.full[s]), (uint32_t)((i / kNS) & 1))) break;
@@ -400,6 +408,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     mma_commit(smem_u32(&c.sfull[buf]));
                     mma_commit(smem_u32(&c.empty[s]));
+                    mma_commit_mc(smem_u32(&c.kfree[s]), 0x2);  // the O-CTA's helper
                 }
             }
         } else if (warp >= 5) {
@@ -650,6 +659,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     *(volatile int32_t*)&c.landed = (int32_t)(i + 1);
                 }
             }
+        } else if (warp == 3) {
+            // ---------------- K helper: blocks 2-3 of each tile into the S-CTA's
+            // stage (multicast with only the S-CTA in the mask; its full[s]
+            // receives the bytes), once the S-CTA's QK has freed the stage
+            if (elect_one()) {
+                long long i = 0;
+                for (; w.u < w.u_end; walk_next(p, w), ++i) {
+                    const int s = (int)(i % kNS);
+                    if (!wt.wait(smem_u32(&c.kfree[s]), (uint32_t)((i / kNS) & 1) ^ 1)) break;
+                    if (i == 1 || i == 2)  // stages 1-2 held the S-CTA's first queries
+                        if (!wt.wait(smem_u32(&c.qmoved), 0)) break;
+                    const int nb = valid_blocks(w);
+                    const int32_t* bt = p.block_table + (long long)w.b * p.max_blocks + w.tile * 4;
+                    for (int kb = 2; kb < nb; ++kb) {
+                        int32_t blk = bt[kb];
+                        if (blk < 0 || blk >= p.num_blocks) {
+                            // load a valid stand-in; the softmax threads void the segment
+                            if (p.dev_err) atomicOr(p.dev_err, (int32_t)MLA_DEVERR_BAD_BLOCK);
+                            blk = 0;
+                        }
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch)
+                            tma_load_3d_mc(smem_u32(smem + s * kStage + ch * kChunk + kb * 2048), &tmap,
+                                           smem_u32(&c.full[s]), ch * 64, 0, blk, 0x1);
+                        if (NKC == 9)
+                            tma_load_3d_mc(smem_u32(smem + kSideOff + s * kChunk + kb * 2048), &tmap,
+                                           smem_u32(&c.full[s]), 512, 0, blk, 0x1);
+                    }
+                }
+            }
         } else if (warp == 2) {
             // ---------------- L2 prefetcher: pulls the cache blocks of the tiles
             // kPrefetchAhead past the V landing point into L2 (plain prefetches,
@@ -876,20 +915,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------ combine
 // Merges the partial segments of row groups that were split across pairs
 // (LSE-weighted, in pair order) and writes the rows of empty or invalid
-// requests. One CTA per (request, row group, 16-column slice); thread t takes
-// row t % 128 and column quad t / 128 of the slice, so a warp reads 32
-// consecutive rows of one quad (512 contiguous bytes). A thread loads the LSEs
-// and its quads of up to kCombineBatch parts at once, then merges them with a
-// running maximum: one memory round trip per batch of parts.
+// requests. One CTA per (request, row group, 64-column slice); thread t takes
+// row t % 128 and the four column quads 4 (t / 128) .. + 3 of the slice, so a
+// warp reads 32 consecutive rows of one quad (512 contiguous bytes). A thread
+// loads the LSEs and quads of kCombineBatch parts at once and merges them with
+// a running maximum: one memory round trip per batch of parts.
 //
 // Launched as a programmatic dependent of the decode kernel: everything up to
 // the partials' first read overlaps the decode kernel's tail.
 constexpr int kCombineThreads = 512;
-constexpr int kCombineSlices = 32;
-constexpr int kCombineBatch = 16;
+constexpr int kCombineSlices = 8;
+constexpr int kCombineBatch = 4;
 
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const Params p) {
-    __shared__ long long sh_u[2];
+__global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(const Params p) {
+    __shared__ int sh_parts[3];  // first pair, part count, first part's slot offset
     const int tid = threadIdx.x, lane = tid & 31;
     const int Mq = p.T * p.H;
     const int G = (Mq + 127) / 128;
@@ -899,12 +938,12 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const Params p
     const int b = (int)(bg / G), g = (int)(bg % G);
     const int rows = min(128, Mq - g * 128);
     const int r = tid & 127;
-    const int quad = tid >> 7;                 // 0..3
-    const int col = slice * 16 + quad * 4;
+    const int q0 = slice * 16 + (tid >> 7) * 4;   // first of this thread's 4 column quads
     const int S = p.seq_lens[b];
     const int nt = ntiles_of(S, p.T, p.max_blocks);
     const long long orow = (long long)b * Mq + g * 128 + r;
-    // the unit range of (b, g) and the total, as the decode kernel partitions
+    // which pairs hold this row group, from seq_lens alone (as the decode
+    // kernel partitions the units); one warp works it out for the CTA
     if (tid < 32 && nt > 0) {
         long long U = 0, before = 0;
         for (int b0 = 0; b0 < p.B; b0 += 32) {
@@ -920,8 +959,22 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const Params p
             before += vb;
         }
         if (lane == 0) {
-            sh_u[0] = U;
-            sh_u[1] = before;
+            const long long u0 = before + (long long)g * nt, u1 = u0 + nt;
+            int np = p.NP;
+            const long long cap = (U + p.min_units - 1) / p.min_units;
+            if (cap < np) np = (int)(cap > 0 ? cap : 1);
+            auto owner = [&](long long u) {  // pair whose range holds unit u
+                long long pp = (u * np) / U;
+                while (pp + 1 < np && U * (pp + 1) / np <= u) ++pp;
+                while (pp > 0 && U * pp / np > u) --pp;
+                return (int)pp;
+            };
+            const int pf = owner(u0), pl = owner(u1 - 1);
+            sh_parts[0] = pf;
+            sh_parts[1] = pl - pf + 1;
+            // part 0 is pair pf's first segment when its range starts at u0, else
+            // its last one; every later part is that pair's first segment
+            sh_parts[2] = (U * pf / np) >= u0 ? 0 : 1;
         }
     }
     // from here on the decode kernel's results (and the output rows it may
@@ -933,42 +986,33 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const Params p
             else if (S > p.max_blocks * 16) atomicOr(p.dev_err, (int32_t)MLA_DEVERR_SEQ_TOO_LONG);
         }
         if (r < rows) {
-            *reinterpret_cast<uint2*>(p.out + orow * 512 + col) = make_uint2(0u, 0u);
-            if (slice == 0 && quad == 0 && p.lse) p.lse[orow] = -INFINITY;
+            uint2* dst = reinterpret_cast<uint2*>(p.out + orow * 512 + q0 * 4);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) dst[k] = make_uint2(0u, 0u);
+            if (slice == 0 && q0 == 0 && p.lse) p.lse[orow] = -INFINITY;
         }
         return;
     }
     __syncthreads();
-    const long long U = sh_u[0];
-    const long long u0 = sh_u[1] + (long long)g * nt, u1 = u0 + nt;
-    int np = p.NP;
-    const long long cap = (U + p.min_units - 1) / p.min_units;
-    if (cap < np) np = (int)(cap > 0 ? cap : 1);
-    auto owner = [&](long long u) {  // pair whose range holds unit u
-        long long pp = (u * np) / U;
-        while (pp + 1 < np && U * (pp + 1) / np <= u) ++pp;
-        while (pp > 0 && U * pp / np > u) --pp;
-        return (int)pp;
-    };
-    const int pf = owner(u0), pl = owner(u1 - 1);
-    if (pf == pl || r >= rows) return;  // one pair held the whole row group and wrote it
-    const int nparts = pl - pf + 1;
-    // part k is pair pf + k's first segment, or its last one when that pair's
-    // range starts before this row group (only pair pf can)
+    const int pf = sh_parts[0], nparts = sh_parts[1], slot0_off = sh_parts[2];
+    if (nparts <= 1 || r >= rows) return;  // one pair held the whole row group and wrote it
     float m = -INFINITY, wsum = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
     bool bad = false;
+    const float4* ws4 = reinterpret_cast<const float4*>(p.ws_o);
     for (int k0 = 0; k0 < nparts; k0 += kCombineBatch) {
         const int nk = min(kCombineBatch, nparts - k0);
         float ls[kCombineBatch];
-        float4 v[kCombineBatch];
+        float4 v[kCombineBatch][4];
 #pragma unroll
         for (int j = 0; j < kCombineBatch; ++j) {
             if (j < nk) {
-                const int pp = pf + k0 + j;
-                const long long slot = pp * 2 + ((U * pp / np) >= u0 ? 0 : 1);
+                const long long slot = (long long)(pf + k0 + j) * 2 + (k0 + j == 0 ? slot0_off : 0);
                 ls[j] = p.ws_lse[slot * 128 + r];
-                v[j] = reinterpret_cast<const float4*>(p.ws_o)[(slot * 128 + slice * 4 + quad) * 128 + r];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) v[j][q] = ws4[(slot * 128 + q0 + q) * 128 + r];
             }
         }
 #pragma unroll
@@ -978,26 +1022,37 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const Params p
                 if (ls[j] > m) {  // a new maximum: rescale what has been summed
                     const float a = (m == -INFINITY) ? 0.f : expf(m - ls[j]);
                     wsum *= a;
-                    acc.x *= a;
-                    acc.y *= a;
-                    acc.z *= a;
-                    acc.w *= a;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc[q].x *= a;
+                        acc[q].y *= a;
+                        acc[q].z *= a;
+                        acc[q].w *= a;
+                    }
                     m = ls[j];
                 }
                 const float wk = (ls[j] == -INFINITY) ? 0.f : expf(ls[j] - m);
                 wsum += wk;
-                acc.x += wk * v[j].x;
-                acc.y += wk * v[j].y;
-                acc.z += wk * v[j].z;
-                acc.w += wk * v[j].w;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    acc[q].x += wk * v[j][q].x;
+                    acc[q].y += wk * v[j][q].y;
+                    acc[q].z += wk * v[j][q].z;
+                    acc[q].w += wk * v[j][q].w;
+                }
             }
         }
     }
     const bool empty = bad || !(wsum > 0.f);
     const float inv = empty ? 0.f : 1.f / wsum;
-    *reinterpret_cast<uint2*>(p.out + orow * 512 + col) =
-        make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
-    if (slice == 0 && quad == 0 && p.lse) p.lse[orow] = empty ? -INFINITY : m + logf(wsum);
+    uint4* dst = reinterpret_cast<uint4*>(p.out + orow * 512 + q0 * 4);
+#pragma unroll
+    for (int q = 0; q < 4; q += 2)
+        dst[q / 2] = make_uint4(pack_bf16x2(acc[q].x * inv, acc[q].y * inv),
+                                pack_bf16x2(acc[q].z * inv, acc[q].w * inv),
+                                pack_bf16x2(acc[q + 1].x * inv, acc[q + 1].y * inv),
+                                pack_bf16x2(acc[q + 1].z * inv, acc[q + 1].w * inv));
+    if (slice == 0 && q0 == 0 && p.lse) p.lse[orow] = empty ? -INFINITY : m + logf(wsum);
 }
 
 // ------------------------------------------------------------------ host
