@@ -89,9 +89,9 @@ struct Ctrl {
     uint64_t vready[kNS];   // O: tile tail zeroed (fix warp)
     uint64_t odone;         // O: all issued P*V complete (MMA commit)
     uint64_t evt;           // O: MMA warp -> row warps event
-    uint64_t evtdone;       // O: row warps -> MMA warp (128)
+    uint64_t evtdone;       // O: row warps -> MMA warp (256)
     uint64_t statfull;      // O: segment statistics written (1 remote)
-    uint64_t rowbar;        // both: barrier among the row threads (S: 256, O: 128)
+    uint64_t rowbar;        // both: barrier among the 256 row threads
     uint32_t tmem_base;
     int32_t abort;
     int32_t evt_type;       // 1 = rescale slot evt_slot, 2 = segment epilogue
@@ -258,10 +258,10 @@ __device__ __forceinline__ int valid_blocks(const Walk& w) {
 //          warp 1     V landing: zeroes rows past the request, releases the stage
 //          warp 2     L2 prefetcher of upcoming cache blocks
 //          warp 4     O += P V MMA issuer; owns the TMEM allocation
-//          warps 5-8  rescale and epilogue, one query row per thread
+//          warps 5-12 rescale and epilogue: warp w takes the TMEM lanes of
+//                     its quadrant (w % 4) and half the 512 columns
 //          warp 3     K helper: loads blocks 2-3 of each S-CTA tile (multicast
 //                     to the S-CTA only), so both TMA units share the boxes
-//          warps 9-12 idle
 template <int W>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_pair_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap qmap,
@@ -300,9 +300,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(&c.statack), 1);
         mbar_init(smem_u32(&c.odone), 1);
         mbar_init(smem_u32(&c.evt), 1);
-        mbar_init(smem_u32(&c.evtdone), 128);
+        mbar_init(smem_u32(&c.evtdone), 256);
         mbar_init(smem_u32(&c.statfull), 1);
-        mbar_init(smem_u32(&c.rowbar), rank == 0 ? kSmxWarps * 32 : 128);
+        mbar_init(smem_u32(&c.rowbar), 256);
         c.abort = 0;
         c.landed = 0;
         fence_mbar_init();
@@ -334,10 +334,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tma_prefetch_desc(&qmap);
                     // the first segment's queries: TMA into stages 1 and 2 (free until
                     // the rows move them to TMEM), while tile 0 goes to stage 0
-                    mbar_arrive_expect_tx(smem_u32(&c.qland), (uint32_t)(NKC * kQChunk));
+                    // (a request's rows past t_q * n_head are outside the map: not read)
+                    const int qrows = Mq < 128 ? Mq : 128;
+                    mbar_arrive_expect_tx(smem_u32(&c.qland), (uint32_t)(NKC * qrows * 128));
                     for (int cc = 0; cc < NKC; ++cc)
-                        tma_load_2d(smem_u32(smem + q_chunk_off(cc)), &qmap, smem_u32(&c.qland),
-                                    cc * 64, w.b * Mq + w.g * 128);
+                        tma_load_3d(smem_u32(smem + q_chunk_off(cc)), &qmap, smem_u32(&c.qland),
+                                    cc * 64, w.g * 128, w.b);
                 }
                 long long i = 0;
                 long long last_issue[kNS];
@@ -775,10 +777,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-        } else if (warp >= 5 && warp <= 8) {
-            // ---------------- row warps: rescale and epilogue
+        } else if (warp >= 5) {
+            // ---------------- row warps: rescale and epilogue. Warps 5..8 take
+            // columns 0..255 of their 32 rows, warps 9..12 columns 256..511.
             const int q = warp & 3;
+            const int hc = warp >= 9 ? 1 : 0;
+            const int c_lo = hc * 256;
             const int r = q * 32 + lane;
+            const bool lead = hc == 0;               // writes the per-row values once
             const uint32_t lane_off = (uint32_t)(q * 32) << 16;
             const uint32_t statack_remote = mapa(smem_u32(&c.statack), 0);
             int nevt = 0, seg = 0;
@@ -795,7 +801,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const float a = c.amsg[slot].alpha[r];
                     if (a != 1.f) {
 #pragma unroll 1
-                        for (int cc = 0; cc < 512; cc += 32) {
+                        for (int cc = c_lo; cc < c_lo + 256; cc += 32) {
                             uint32_t v[32];
                             tmem_ld32(tbase + lane_off + cc, v);
                             tmem_wait_ld();
@@ -819,7 +825,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const int seg_bad = *(volatile int32_t*)&c.bad;
                 // statistics consumed: the S-CTA may send the next segment's
                 if (!rows_sync(wt, smem_u32(&c.rowbar), rphase)) break;
-                if (r == 0) mbar_arrive_remote(statack_remote);
+                if (lead && r == 0) mbar_arrive_remote(statack_remote);
                 const int grow = w.g * 128 + r;
                 const bool row_ok = grow < Mq;
                 const bool full_seg = (seg_tile0 == 0) && (w.tile + 1 == w.ntiles);
@@ -829,14 +835,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 bool ok = true;
                 if (full_seg) {
                     // bf16 rows through the freed V stage: four [128 rows][64 columns]
-                    // swizzled boxes per pass, stored by TMA (rows past the request's
-                    // query rows fall outside the output map and are not written)
+                    // swizzled boxes per pass (two from each column half), stored by
+                    // TMA (rows past the request's query rows fall outside the output
+                    // map and are not written)
                     const uint32_t stg = smem_u32(smem + stage * kStage);
 #pragma unroll 1
                     for (int pass = 0; pass < 2 && ok; ++pass) {
 #pragma unroll 1
-                        for (int k = 0; k < 4; ++k) {
-                            const int cb = pass * 4 + k;
+                        for (int k2 = 0; k2 < 2; ++k2) {
+                            const int k = hc * 2 + k2;                 // box slot in the stage
+                            const int cb = hc * 4 + pass * 2 + k2;     // 64-column block
                             uint32_t v0[32], v1[32];
                             tmem_ld32(tbase + lane_off + cb * 64, v0);
                             tmem_ld32(tbase + lane_off + cb * 64 + 32, v1);
@@ -854,16 +862,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         }
                         fence_proxy_async_smem();
                         if (!rows_sync(wt, smem_u32(&c.rowbar), rphase)) { ok = false; break; }
-                        if (r == 0) {
+                        if (lead && r == 0) {
 #pragma unroll 1
                             for (int k = 0; k < 4; ++k)
-                                tma_store_3d(&omap, stg + k * kQChunk, (pass * 4 + k) * 64, w.g * 128, w.b);
+                                tma_store_3d(&omap, stg + k * kQChunk, ((k >> 1) * 4 + pass * 2 + (k & 1)) * 64,
+                                             w.g * 128, w.b);
                             bulk_commit();
                             bulk_wait_read_all();
                         }
                         if (!rows_sync(wt, smem_u32(&c.rowbar), rphase)) { ok = false; break; }
                     }
-                    if (row_ok && p.lse) p.lse[(long long)w.b * Mq + grow] = lse_v;
+                    if (lead && row_ok && p.lse) p.lse[(long long)w.b * Mq + grow] = lse_v;
                 } else if (row_ok) {
                     // f32 partial; layout [slot][column quad][128 rows][4], so the 32
                     // lanes of a store write 512 contiguous bytes. TMEM is read two
@@ -871,7 +880,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const int slot = pair * 2 + (seg == 0 ? 0 : 1);
                     float4* dst = reinterpret_cast<float4*>(p.ws_o + (long long)slot * 128 * 512) + r;
 #pragma unroll 1
-                    for (int cc = 0; cc < 512; cc += 64) {
+                    for (int cc = c_lo; cc < c_lo + 256; cc += 64) {
                         uint32_t v[2][32];
 #pragma unroll
                         for (int k = 0; k < 2; ++k) tmem_ld32(tbase + lane_off + cc + 32 * k, v[k]);
@@ -886,8 +895,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                                 __uint_as_float(v[k][4 * j + 2]) * inv,
                                                 __uint_as_float(v[k][4 * j + 3]) * inv);
                     }
-                    p.ws_lse[(long long)slot * 128 + r] =
-                        seg_bad ? __int_as_float(0x7fc00000) : lse_v;  // NaN marks bad
+                    if (lead)
+                        p.ws_lse[(long long)slot * 128 + r] =
+                            seg_bad ? __int_as_float(0x7fc00000) : lse_v;  // NaN marks bad
                 }
                 if (!ok) break;
                 tc_fence_before();
@@ -900,7 +910,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     seg_tile0 = w.tile;
                 }
             }
-            if (r == 0) bulk_wait_all();  // the epilogue's TMA stores have completed
+            if (lead && r == 0) bulk_wait_all();  // the epilogue's TMA stores have completed
             __syncwarp();
         }
     }
@@ -1169,11 +1179,14 @@ cudaError_t launch_decode_tc(void* out, float* lse, const void* q_abs, const voi
     }
     CUtensorMap qmap;
     {
-        cuuint64_t qdims[2] = {(cuuint64_t)W, (cuuint64_t)batch * d.t_q * d.n_head};
-        cuuint64_t qstrides[1] = {(cuuint64_t)W * 2};
-        cuuint32_t qbox[2] = {64, 128};
-        cuuint32_t qes[2] = {1, 1};
-        cr = enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q_abs), qdims,
+        // queries as {W columns, t_q * n_head rows, batch}: a 128-row box of one
+        // request never reads the next request's rows
+        const int Mq = d.t_q * d.n_head;
+        cuuint64_t qdims[3] = {(cuuint64_t)W, (cuuint64_t)Mq, (cuuint64_t)batch};
+        cuuint64_t qstrides[2] = {(cuuint64_t)W * 2, (cuuint64_t)Mq * W * 2};
+        cuuint32_t qbox[3] = {64, (cuuint32_t)(Mq < 128 ? Mq : 128), 1};
+        cuuint32_t qes[3] = {1, 1, 1};
+        cr = enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q_abs), qdims,
                  qstrides, qbox, qes, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (cr != CUDA_SUCCESS) {
