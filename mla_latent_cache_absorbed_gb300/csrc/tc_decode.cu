@@ -334,6 +334,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tma_prefetch_desc(&qmap);
                     // the first segment's queries: TMA into stages 1 and 2 (free until
                     // the rows move them to TMEM), while tile 0 goes to stage 0
+                    // the queries come from the previous kernel (programmatic launch)
+                    grid_dependency_wait();
                     // (a request's rows past t_q * n_head are outside the map: not read)
                     const int qrows = Mq < 128 ? Mq : 128;
                     mbar_arrive_expect_tx(smem_u32(&c.qland), (uint32_t)(NKC * qrows * 128));
@@ -435,6 +437,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t bad_remote = mapa(smem_u32(&c.bad), 1);
             const uint32_t statfull_remote = mapa(smem_u32(&c.statfull), 1);
             const float sl2 = p.scale_log2;
+            grid_dependency_wait();  // later segments read their queries from global memory
             long long i = 0;
             int seg = 0;
             uint32_t rphase = 0;
@@ -787,6 +790,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const bool lead = hc == 0;               // writes the per-row values once
             const uint32_t lane_off = (uint32_t)(q * 32) << 16;
             const uint32_t statack_remote = mapa(smem_u32(&c.statack), 0);
+            grid_dependency_wait();  // their writes follow the previous kernel's
             int nevt = 0, seg = 0;
             uint32_t rphase = 0;
             int seg_tile0 = w.tile;
@@ -1246,18 +1250,22 @@ cudaError_t launch_decode_tc(void* out, float* lse, const void* q_abs, const voi
     p.min_units = 2;
     p.scale_log2 = scale * 1.4426950408889634f;
 
+    // a programmatic dependent of the kernel before it: the cache pipeline
+    // starts while that kernel finishes; the queries, and every write, wait
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(2 * np, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (W == 576)
         e = cudaLaunchKernelEx(&cfg, decode_pair_kernel<576>, tmap, qmap, vmap, omap, p);
     else

@@ -5,9 +5,15 @@
 //   decompress  out[r, j]    = sum_l o_lat[r, h, l]  * w_uv[h, j, l]   (K = kv_rank)
 // with few query rows (M = batch * t_q), so they stream the weights: each CTA
 // owns one (head, N tile, M tile of 128 rows), brings A and the weight slice
-// in 64-wide K chunks through a TMA ring, accumulates in TMEM (M = 128; rows
-// past M are zero-filled by TMA) and converts to bf16 in the epilogue. The
-// absorb epilogue also copies q_pe into the rope tail of each q_abs row.
+// in 64-wide K chunks through a TMA ring, accumulates in TMEM (M = 128; only
+// the tile's real rows are loaded and stored) and converts to bf16 in the
+// epilogue. The absorb epilogue also copies q_pe into the rope tail of each
+// q_abs row.
+//
+// Both launch as programmatic dependents of the kernel before them on the
+// stream: the weight chunks that fit the ring are requested before waiting
+// for that kernel (they depend on nothing it writes); A and every write come
+// after the wait.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -37,6 +43,7 @@ struct GemmParams {
     int n_tile;                  // output columns per CTA (<= 256)
     int out_stride;              // elements between consecutive (r, h) rows: W or Dv
     int P;                       // absorb: rope width copied from q_pe
+    int a_rows;                  // rows of the A box (the M tile's real rows, multiple of 8)
     int32_t* dev_err;            // optional: timeout bit
 };
 
@@ -52,10 +59,12 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const int nk = p.K / 64;
     const int bchunk = p.n_tile * 128;  // bytes of one B chunk (n_tile x 64 K)
     const int stage_bytes = kAChunk + bchunk;
+    const uint32_t a_bytes = (uint32_t)p.a_rows * 128;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kGStages * stage_bytes);
     uint64_t* empty = full + kGStages;
     uint64_t* done = empty + kGStages;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(done + 1);
+    grid_dependents_launch();  // the next kernel may start its own prologue
     if ((smem_u32(smem) & 1023) != 0) return;
     if (tid == 0) {
         for (int s = 0; s < kGStages; ++s) {
@@ -79,16 +88,11 @@ __global__ void __launch_bounds__(kGThreads, 1)
         if (elect_one()) {
             tma_prefetch_desc(&amap);
             tma_prefetch_desc(&bmap);
-            for (int kc = 0; kc < nk; ++kc) {
+            // weight chunks first (inputs of no earlier kernel), the first ring's
+            // worth before waiting for the previous kernel; A after the wait
+            auto load_b = [&](int kc) {
                 const int s = kc % kGStages;
-                if (!mbar_wait(smem_u32(&empty[s]), ((kc / kGStages) & 1) ^ 1, kGWaitNs)) {
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(smem_u32(&full[s]), (uint32_t)stage_bytes);
                 unsigned char* st = smem + s * stage_bytes;
-                // A: rows m0..m0+127 of head h, K columns kc*64.. (rows past M read 0)
-                tma_load_3d(smem_u32(st), &amap, smem_u32(&full[s]), kc * 64, h, m0);
                 if (kBMnMajor) {
                     // weight [K][N] (N contiguous): n_tile/64 boxes of [64 K rows][64 N]
                     for (int j = 0; j < p.n_tile / 64; ++j)
@@ -99,6 +103,26 @@ __global__ void __launch_bounds__(kGThreads, 1)
                     tma_load_3d(smem_u32(st + kAChunk), &bmap, smem_u32(&full[s]), kc * 64,
                                 n0, h);
                 }
+            };
+            const int early = nk < kGStages ? nk : kGStages;
+            for (int kc = 0; kc < early; ++kc) {
+                mbar_arrive_expect_tx(smem_u32(&full[kc]), (uint32_t)bchunk + a_bytes);
+                load_b(kc);
+            }
+            grid_dependency_wait();
+            for (int kc = 0; kc < nk; ++kc) {
+                const int s = kc % kGStages;
+                if (kc >= early) {
+                    if (!mbar_wait(smem_u32(&empty[s]), ((kc / kGStages) & 1) ^ 1, kGWaitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(smem_u32(&full[s]), (uint32_t)bchunk + a_bytes);
+                    load_b(kc);
+                }
+                // A: the tile's rows m0.. of head h, K columns kc*64..
+                tma_load_3d(smem_u32(smem + s * stage_bytes), &amap, smem_u32(&full[s]), kc * 64, h,
+                            m0);
             }
         }
     } else if (warp == 1) {
@@ -130,6 +154,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         const int r = q * 32 + lane;
         const int row = m0 + r;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        grid_dependency_wait();  // (writes follow the previous kernel)
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(done), 0, kGWaitNs));
         tc_fence_after();
         if (ok) {
@@ -217,8 +242,18 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const GemmParams&
             smem_for(256));
     });
     if (attr_err[kBMnMajor ? 1 : 0] != cudaSuccess) return attr_err[kBMnMajor ? 1 : 0];
-    dim3 grid(p.H, p.N / p.n_tile, (p.rows + 127) / 128);
-    tc_bgemm_kernel<kBMnMajor><<<grid, kGThreads, smem, s>>>(a, b, p);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(p.H, p.N / p.n_tile, (p.rows + 127) / 128);
+    cfg.blockDim = dim3(kGThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, tc_bgemm_kernel<kBMnMajor>, a, b, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -236,9 +271,10 @@ cudaError_t launch_absorb_tc(void* q_abs, const void* q_nope, const void* q_pe,
                              cudaStream_t s) {
     const int H = d.n_head, Dn = d.d_nope, R = d.kv_rank, P = d.d_rope;
     CUtensorMap a, b;
-    // A: q_nope viewed as {Dn, H, rows}; box {64, 1, 128}
+    // A: q_nope viewed as {Dn, H, rows}; box {64, 1, a_rows}
+    const int a_rows = rows >= 128 ? 128 : (rows + 7) / 8 * 8;
     cudaError_t e = make_map(&a, q_nope, Dn, H, rows, (cuuint64_t)Dn * 2, (cuuint64_t)H * Dn * 2,
-                             64, 1, 128);
+                             64, 1, (cuuint32_t)a_rows);
     if (e != cudaSuccess) return e;
     // B: w_uk viewed as {R, Dn, H} (N contiguous); box {64 N, 64 K, 1}
     e = make_map(&b, w_uk, R, Dn, H, (cuuint64_t)R * 2, (cuuint64_t)Dn * R * 2, 64, 64, 1);
@@ -253,6 +289,7 @@ cudaError_t launch_absorb_tc(void* q_abs, const void* q_nope, const void* q_pe,
     p.n_tile = 256;
     p.out_stride = R + P;
     p.P = P;
+    p.a_rows = a_rows;
     p.dev_err = nullptr;
     return launch<true>(a, b, p, s);
 }
@@ -262,9 +299,10 @@ cudaError_t launch_decompress_tc(void* out, const void* o_lat, const void* w_uv,
     const int H = d.n_head, R = d.kv_rank, Dv = d.d_v;
     const int n_tile = Dv == 128 ? 128 : (Dv >= 256 && Dv % 256 == 0 ? 128 : 128);
     CUtensorMap a, b;
-    // A: o_lat viewed as {R, H, rows}; box {64, 1, 128}
+    // A: o_lat viewed as {R, H, rows}; box {64, 1, a_rows}
+    const int a_rows = rows >= 128 ? 128 : (rows + 7) / 8 * 8;
     cudaError_t e = make_map(&a, o_lat, R, H, rows, (cuuint64_t)R * 2, (cuuint64_t)H * R * 2, 64,
-                             1, 128);
+                             1, (cuuint32_t)a_rows);
     if (e != cudaSuccess) return e;
     // B: w_uv viewed as {R, Dv, H} (K contiguous); box {64 K, n_tile N, 1}
     e = make_map(&b, w_uv, R, Dv, H, (cuuint64_t)R * 2, (cuuint64_t)Dv * R * 2, 64,
@@ -280,6 +318,7 @@ cudaError_t launch_decompress_tc(void* out, const void* o_lat, const void* w_uv,
     p.n_tile = n_tile;
     p.out_stride = Dv;
     p.P = 0;
+    p.a_rows = a_rows;
     p.dev_err = nullptr;
     return launch<false>(a, b, p, s);
 }
