@@ -126,34 +126,51 @@ __device__ __forceinline__ int ntiles_of(int S, int T, int max_blocks) {
     return (S + kTok - 1) / kTok;
 }
 
-// Unit sequence: request b, then row group g, then tile. Every warp of both
-// CTAs computes the same walk.
+// Work split. When a request has G > 1 row groups (t_q * n_head > 128), the
+// pairs form G sets of np / G: set g handles row group g of every request, and
+// pair k of each set covers the same (request, tile) range, so the G sets read
+// the same cache tiles at about the same time (one HBM read, the rest from
+// L2). Within a set the unit sequence is request b, then tile; pair k takes
+// units [U k / np_g, U (k + 1) / np_g), U = sum over requests of their tiles.
+// Every warp of both CTAs computes the same walk.
 struct Walk {
     int b, g, tile, ntiles, S;
     long long u, u_end;
-    int G;
 };
 
-// Total units and this pair's range; warp-cooperative, identical result in
-// every lane. Returns false when the pair has no work.
-__device__ bool walk_init(const Params& p, int pair, Walk& w) {
-    const int lane = threadIdx.x & 31;
-    const int Mq = p.T * p.H;
-    const int G = (Mq + 127) / 128;
+// pairs per set (np_g) and the set size cap, as both kernels derive them
+__device__ __forceinline__ int pairs_per_set(const Params& p, int G, long long U) {
+    int np_g = p.NP / G;
+    const long long cap = (U + p.min_units - 1) / p.min_units;
+    if (cap < np_g) np_g = (int)(cap > 0 ? cap : 1);
+    return np_g;
+}
+
+// Total units of one set (warp-cooperative, identical in every lane).
+__device__ long long units_per_set(const Params& p, int lane) {
     long long U = 0;
     for (int b0 = 0; b0 < p.B; b0 += 32) {
         const int b = b0 + lane;
-        long long v = b < p.B ? (long long)ntiles_of(p.seq_lens[b], p.T, p.max_blocks) * G : 0;
+        long long v = b < p.B ? (long long)ntiles_of(p.seq_lens[b], p.T, p.max_blocks) : 0;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
         U += v;
     }
-    int np = p.NP;
-    const long long cap = (U + p.min_units - 1) / p.min_units;
-    if (cap < np) np = (int)(cap > 0 ? cap : 1);
-    w.G = G;
-    if (pair >= np || U == 0) return false;
-    const long long ub = U * pair / np, ue = U * (pair + 1) / np;
+    return U;
+}
+
+// This pair's set and unit range; warp-cooperative. Returns false when the
+// pair has no work.
+__device__ bool walk_init(const Params& p, int pair, Walk& w) {
+    const int lane = threadIdx.x & 31;
+    const int Mq = p.T * p.H;
+    const int G = (Mq + 127) / 128;
+    const long long U = units_per_set(p, lane);
+    if (U == 0) return false;
+    const int np_g = pairs_per_set(p, G, U);
+    const int g = pair / np_g, k = pair % np_g;
+    if (g >= G) return false;
+    const long long ub = U * k / np_g, ue = U * (k + 1) / np_g;
     if (ub >= ue) return false;
     // locate unit ub
     long long base = 0;
@@ -161,7 +178,7 @@ __device__ bool walk_init(const Params& p, int pair, Walk& w) {
     long long found_base = 0;
     for (int b0 = 0; b0 < p.B && found_b < 0; b0 += 32) {
         const int b = b0 + lane;
-        long long v = b < p.B ? (long long)ntiles_of(p.seq_lens[b], p.T, p.max_blocks) * G : 0;
+        long long v = b < p.B ? (long long)ntiles_of(p.seq_lens[b], p.T, p.max_blocks) : 0;
         long long incl = v;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -177,11 +194,10 @@ __device__ bool walk_init(const Params& p, int pair, Walk& w) {
         base += __shfl_sync(0xffffffffu, incl, 31);
     }
     w.b = found_b;
+    w.g = g;
     w.S = p.seq_lens[found_b];
     w.ntiles = ntiles_of(w.S, p.T, p.max_blocks);
-    const long long off = ub - found_base;
-    w.g = (int)(off / w.ntiles);
-    w.tile = (int)(off % w.ntiles);
+    w.tile = (int)(ub - found_base);
     w.u = ub;
     w.u_end = ue;
     return true;
@@ -193,8 +209,6 @@ __device__ __forceinline__ void walk_next(const Params& p, Walk& w) {
     if (w.u >= w.u_end) return;
     if (++w.tile < w.ntiles) return;
     w.tile = 0;
-    if (++w.g < w.G) return;
-    w.g = 0;
     do {
         ++w.b;
         w.S = p.seq_lens[w.b];
@@ -962,7 +976,7 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(const Param
         long long U = 0, before = 0;
         for (int b0 = 0; b0 < p.B; b0 += 32) {
             const int bb = b0 + lane;
-            long long v = bb < p.B ? (long long)ntiles_of(p.seq_lens[bb], p.T, p.max_blocks) * G : 0;
+            long long v = bb < p.B ? (long long)ntiles_of(p.seq_lens[bb], p.T, p.max_blocks) : 0;
             long long vb = bb < b ? v : 0;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
@@ -973,22 +987,20 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(const Param
             before += vb;
         }
         if (lane == 0) {
-            const long long u0 = before + (long long)g * nt, u1 = u0 + nt;
-            int np = p.NP;
-            const long long cap = (U + p.min_units - 1) / p.min_units;
-            if (cap < np) np = (int)(cap > 0 ? cap : 1);
-            auto owner = [&](long long u) {  // pair whose range holds unit u
-                long long pp = (u * np) / U;
-                while (pp + 1 < np && U * (pp + 1) / np <= u) ++pp;
-                while (pp > 0 && U * pp / np > u) --pp;
+            const long long u0 = before, u1 = u0 + nt;  // within row group g's set
+            const int np_g = pairs_per_set(p, G, U);
+            auto owner = [&](long long u) {  // pair of the set whose range holds unit u
+                long long pp = (u * np_g) / U;
+                while (pp + 1 < np_g && U * (pp + 1) / np_g <= u) ++pp;
+                while (pp > 0 && U * pp / np_g > u) --pp;
                 return (int)pp;
             };
-            const int pf = owner(u0), pl = owner(u1 - 1);
-            sh_parts[0] = pf;
-            sh_parts[1] = pl - pf + 1;
-            // part 0 is pair pf's first segment when its range starts at u0, else
+            const int kf = owner(u0), kl = owner(u1 - 1);
+            sh_parts[0] = g * np_g + kf;  // the pairs' global indices
+            sh_parts[1] = kl - kf + 1;
+            // part 0 is pair kf's first segment when its range starts at u0, else
             // its last one; every later part is that pair's first segment
-            sh_parts[2] = (U * pf / np) >= u0 ? 0 : 1;
+            sh_parts[2] = (U * kf / np_g) >= u0 ? 0 : 1;
         }
     }
     // from here on the decode kernel's results (and the output rows it may
