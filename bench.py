@@ -392,6 +392,11 @@ def run_ours(args, wl):
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = profiled_traffic(wl.name) if dominant == "decode" else None
     roof["kernel"] = dominant
+    if dominant == "decode":
+        # the decode stage is the pair kernel plus the split combine; the
+        # committed ncu traffic is the pair kernel's (the combine re-reads the
+        # partials the pair kernel wrote, from L2)
+        roof["traffic_kernel"] = "decode_pair_kernel"
     roof["peak_source"] = f"{peaks_src} (MEASURED_PEAKS.json)" if peaks_src == "measured" \
         else "fallback (profiling recipe)"
     dec_bytes, dec_flops = alg["decode"]
