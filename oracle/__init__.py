@@ -79,10 +79,11 @@ def _declare(lib):
     lib.oracle_rope_interleaved.argtypes = [_P, _I, _F, _F]
     lib.oracle_rope_neox.argtypes = [_P, _I, _F, _F]
     lib.oracle_norm_to_neox_perm.argtypes = [_I, _P]
+    lib.oracle_cache_append.argtypes = [_P, _I, _P, _P, _I, _P, _I, _I64, _I, _I]
     for name in ("oracle_absorb_q", "oracle_decode_range", "oracle_decode_rows",
                  "oracle_decode_paged", "oracle_combine", "oracle_decompress",
                  "oracle_attend_naive", "oracle_attend_absorbed",
-                 "oracle_norm_to_neox_perm"):
+                 "oracle_norm_to_neox_perm", "oracle_cache_append"):
         getattr(lib, name).restype = _I
     lib.oracle_rope_interleaved.restype = None
     lib.oracle_rope_neox.restype = None
@@ -294,3 +295,30 @@ def norm_to_neox_perm(n_dims: int, lib=None) -> np.ndarray:
     p = np.empty(n_dims, np.int32)
     _check(lib.oracle_norm_to_neox_perm(n_dims, _ptr(p)), False)
     return p
+
+
+def cache_append(kv_cache, kv_c, k_pe, slot_mapping, allow_errors=False, lib=None):
+    """The page's do_kv_cache_update: writes [kv_c[n] | k_pe[n]] into flat
+    cache row slot_mapping[n] (cast to the cache's type, round to nearest
+    even for bf16), skipping slots < 0. kv_cache is [num_blocks, bs, W]
+    float32 or uint16 (bf16 bits) and is updated in place on a copy that is
+    returned; kv_c [n, R] and k_pe [n, P] are float32 or uint16 (bf16)."""
+    lib = lib or load()
+    cache = np.array(kv_cache, copy=True, order="C")
+    if cache.dtype not in (np.float32, np.uint16):
+        raise TypeError("cache must be float32 or bf16 bits (uint16)")
+    cdt = BF16 if cache.dtype == np.uint16 else F32
+    kv_c_a, sdt = _elem(np.asarray(kv_c))
+    k_pe_a, sdt2 = _elem(np.asarray(k_pe))
+    if sdt != sdt2:
+        raise TypeError("kv_c and k_pe must share an element type")
+    n, R = kv_c_a.shape
+    P = k_pe_a.shape[1] if k_pe_a.ndim == 2 else 0
+    if cache.shape[-1] != R + P:
+        raise ValueError("cache row width must be kv_rank + d_rope")
+    slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    num_slots = int(np.prod(cache.shape[:-1]))
+    st = lib.oracle_cache_append(_ptr(cache), cdt, _ptr(kv_c_a), _ptr(k_pe_a), sdt, _ptr(slots), n,
+                                 num_slots, R, P)
+    _check(st, allow_errors)
+    return cache

@@ -36,6 +36,9 @@
  *   oracle_rope_interleaved / oracle_rope_neox / oracle_norm_to_neox_perm
  *                          mla.rs, fns rope_interleaved, rope_neox,
  *                          norm_to_neox_perm.
+ *   oracle_cache_append    the vLLM CPU MLA page, CPUMLAImpl.do_kv_cache_update
+ *                          (scatter of [kv_c | k_pe] rows by slot mapping,
+ *                          padding slots -1 skipped, cast to the cache type).
  */
 #include <math.h>
 #include <stdint.h>
@@ -406,6 +409,50 @@ void oracle_rope_neox(float* x, int n_dims, float pos, float base) {
         x[j + half] = a * s + b * c;
         theta *= theta_scale;
     }
+}
+
+/* ------------------------------------------------------------------------- */
+/* cache append (vLLM CPU MLA page, CPUMLAImpl.do_kv_cache_update)            */
+/* ------------------------------------------------------------------------- */
+/* f32 -> bf16 bits, round to nearest with ties to even (the rounding of a
+ * "to(bfloat16)" cast); NaN stays a quiet NaN of the same sign */
+static uint16_t f32_to_bf16_rne(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu) != 0)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    const uint32_t lsb = (u >> 16) & 1u;
+    return (uint16_t)((u + 0x7fffu + lsb) >> 16);
+}
+
+/* Write token n's latent row [kv_c[n] | k_pe[n]] into cache row slot[n] of the
+ * flat cache [num_slots][R + P], cast to the cache's element type; a negative
+ * slot is padding and is skipped (the page's valid mask). A slot at or past
+ * num_slots is an invalid request: skipped and reported (status BAD_BLOCK).
+ * src_dtype / cache_dtype: ORACLE_F32 or ORACLE_BF16 (bf16 as uint16 bits). */
+int oracle_cache_append(void* cache, int cache_dtype, const void* kv_c, const void* k_pe,
+                        int src_dtype, const int64_t* slots, int n_tokens, int64_t num_slots,
+                        int kv_rank, int d_rope) {
+    if (n_tokens < 0 || kv_rank <= 0 || d_rope < 0) return ORACLE_BAD_ARG;
+    const int W = kv_rank + d_rope;
+    int status = ORACLE_OK;
+    for (int n = 0; n < n_tokens; ++n) {
+        const int64_t s = slots[n];
+        if (s < 0) continue;
+        if (s >= num_slots) {
+            status = ORACLE_BAD_BLOCK;
+            continue;
+        }
+        for (int j = 0; j < W; ++j) {
+            const float v = j < kv_rank ? load_elem(kv_c, src_dtype, (int64_t)n * kv_rank + j)
+                                        : load_elem(k_pe, src_dtype, (int64_t)n * d_rope + (j - kv_rank));
+            if (cache_dtype == ORACLE_BF16)
+                ((uint16_t*)cache)[s * W + j] = f32_to_bf16_rne(v);
+            else
+                ((float*)cache)[s * W + j] = v;
+        }
+    }
+    return status;
 }
 
 /* source (interleaved) index -> NEOX index: pi(2j) = j, pi(2j+1) = j + n/2 */

@@ -14,7 +14,11 @@ AssertionError when the oracle disagrees with:
     paged equals contiguous; unused rows never read);
   * the rope facts of the mla.rs rope section (interleaved rope followed by
     the load-time permutation equals the permutation followed by NEOX rope,
-    and roped dot products agree), and the scale of the NoPE geometry.
+    and roped dot products agree), and the scale of the NoPE geometry;
+  * the cache append of the vLLM CPU MLA page (do_kv_cache_update): rows land
+    at their slots unchanged (f32) or as torch's bf16 cast of them, padding
+    slots are skipped, other rows keep their bits, a slot past the cache is
+    reported.
 """
 from __future__ import annotations
 
@@ -431,9 +435,59 @@ def check_rope_against_rotation(lib):
         assert maxdiff(a, b) <= 2e-5, pos
 
 
+def check_cache_append(lib):
+    """do_kv_cache_update (vLLM CPU MLA page): flat[slot] = [kv_c | k_pe] cast
+    to the cache type; slots < 0 skipped. The bf16 cast is torch's (round to
+    nearest, ties to even), checked on values that sit exactly on a tie."""
+    import oracle as O
+    import torch
+    rng = np.random.default_rng(11)
+    R, P, nb, bs = 32, 8, 5, 16
+    n = 9
+    kv = rng.standard_normal((n, R)).astype(np.float32)
+    kp = rng.standard_normal((n, P)).astype(np.float32)
+    # exact ties for the bf16 cast: the 16 dropped bits are 0x8000
+    ties = np.array([0x3f808000, 0x3f818000, 0xbf808000, 0x40008000], np.uint32).view(np.float32)
+    kv[0, :4] = ties
+    kv[1, :3] = [np.inf, -0.0, 3.0e38]
+    slots = np.array([7, -1, 79, 0, -5, 40, 41, 12, 3], np.int64)
+    poison = np.full((nb, bs, R + P), -7.25, np.float32)
+    out = O.cache_append(poison, kv, kp, slots, lib=lib).reshape(-1, R + P)
+    rows = np.concatenate([kv, kp], 1)
+    written = set()
+    for k, s_ in enumerate(slots):
+        if s_ >= 0:
+            assert np.array_equal(out[s_], rows[k]), k
+            written.add(int(s_))
+    for r in range(nb * bs):
+        if r not in written:
+            assert np.all(out[r] == -7.25), r
+    # bf16 cache: torch's cast of the same rows, bit for bit
+    pb = np.full((nb, bs, R + P), 0x1234, np.uint16)
+    outb = O.cache_append(pb, kv, kp, slots, lib=lib).reshape(-1, R + P)
+    ref = torch.from_numpy(rows).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    for k, s_ in enumerate(slots):
+        if s_ >= 0:
+            assert np.array_equal(outb[s_], ref[k]), k
+    assert np.all(outb[1] == 0x1234)
+    # bf16 sources copy exactly
+    kvb = torch.from_numpy(kv).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    kpb = torch.from_numpy(kp).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    outc = O.cache_append(pb, kvb, kpb, slots, lib=lib).reshape(-1, R + P)
+    assert np.array_equal(outc[7], np.concatenate([kvb[0], kpb[0]]))
+    # a slot past the cache is reported and writes nothing
+    bad = O.cache_append(poison, kv[:1], kp[:1], np.array([nb * bs]), allow_errors=True, lib=lib)
+    assert np.all(bad == -7.25)
+    try:
+        O.cache_append(poison, kv[:1], kp[:1], np.array([nb * bs]), lib=lib)
+        raise AssertionError("a slot past the cache must be reported")
+    except O.OracleError:
+        pass
+
+
 QUICK_CHECKS = [check_naive_equals_absorbed, check_paged_chain_equals_naive,
                 check_bruteforce_f64, check_sdpa_reduction, check_closed_forms,
                 check_split_combine, check_paged_equals_contiguous,
                 check_decode_rows_consistent, check_invalid_requests,
                 check_absorb_decompress_unit_weights, check_rope_permutation,
-                check_rope_against_rotation]
+                check_rope_against_rotation, check_cache_append]

@@ -246,3 +246,40 @@ def test_empty_requests_and_batch():
 def test_block_edges(lens):
     """Keys ending exactly on, just before and just after a block boundary."""
     run_stages(W.make_workload("glm52_decode", seq_lens=lens))
+
+
+@pytest.mark.parametrize("name,lens", [
+    ("glm52_decode", None),                                   # every request split over ~10 pairs
+    ("deepseek_decode", [8192, 1, 100, 16, 0, 2049, 3000, 5000]),  # long and short mixed
+])
+def test_back_to_back_steps_are_identical_and_right(name, lens):
+    """Twenty whole steps issued back to back on one stream, with no host
+    synchronisation between them: the kernels of consecutive steps overlap
+    (programmatic launches) and reuse the same buffers and workspace. Every
+    step's latent output and LSE must be bit-identical to the first, and the
+    first must match the oracle. A kernel that released a buffer too early
+    shows here as a step that differs."""
+    import torch
+    wl = W.make_workload(name, seq_lens=lens)
+    g = wl.geom
+    dc = D.upload(wl)
+    H, R, T = g.n_head, g.kv_rank, g.t_q
+    snaps = []
+    for _ in range(20):
+        D.full_step(dc)
+        snaps.append((dc.o_lat.clone(), dc.lse.clone(), dc.out.clone()))
+    torch.cuda.synchronize()
+    assert int(dc.dev_err.item()) == 0
+    first = [t.view(torch.int16) if t.dtype == torch.bfloat16 else t for t in snaps[0]]
+    for k, snap in enumerate(snaps[1:], 1):
+        for a, b in zip(first, snap):
+            b = b.view(torch.int16) if b.dtype == torch.bfloat16 else b
+            assert torch.equal(a, b), f"step {k} differs from step 0"
+    # the first step against the oracle (the chain rounds q_abs and o_lat to bf16)
+    q_abs = W.round_bf16(oracle.absorb_q(wl.q_nope, wl.q_pe, wl.w_uk))
+    o_ref, lse_ref = oracle.decode_paged(q_abs.reshape(wl.batch, T, H, -1), wl.kv_cache,
+                                         wl.block_table, wl.seq_lens, T, R, wl.scale)
+    assert_close(D.device_to_host_f32(snaps[0][0]), o_ref.reshape(-1, H, R), g.dtype,
+                 "back-to-back decode out")
+    assert_lse_close(snaps[0][1].cpu().numpy(), lse_ref.reshape(-1, H), g.dtype,
+                     "back-to-back decode lse")

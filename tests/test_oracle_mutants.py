@@ -51,6 +51,14 @@ MUTANTS = [
     ("rope_neox_sign", "x[j + half] = a * s + b * c;", "x[j + half] = a * s - b * c;", 0),
     ("rope_interleaved_pair", "x[2 * j + 1] = a * s + b * c;", "x[2 * j + 1] = b * c;", 0),
     ("perm_wrong", "perm[2 * j + 1] = j + half;", "perm[2 * j + 1] = n_dims - 1 - j;", 0),
+    ("append_ties_away", "return (uint16_t)((u + 0x7fffu + lsb) >> 16);",
+     "return (uint16_t)((u + 0x8000u) >> 16);", 0),
+    ("append_truncates", "return (uint16_t)((u + 0x7fffu + lsb) >> 16);",
+     "return (uint16_t)(u >> 16);", 0),
+    ("append_writes_padding", "const int64_t s = slots[n];\n        if (s < 0) continue;",
+     "const int64_t s = slots[n] < 0 ? 0 : slots[n];", 0),
+    ("append_rope_from_kv", "(int64_t)n * d_rope + (j - kv_rank));",
+     "(int64_t)n * kv_rank + (j - kv_rank));", 0),
 ]
 
 
