@@ -406,6 +406,9 @@ def run_ours(args, wl):
                        "roofline_us": t_roof * 1e6, "frac": t_roof / dec_s,
                        "bytes": dec_bytes, "flops": dec_flops}
 
+    # the next row of the path: appending new tokens' latent rows to the cache
+    cache_append = measure_cache_append(wl, base, stream, hbm_peak)
+
     # end to end through the C ABI with host buffers
     e2e = run_e2e(args, wl, layers, stream, nl, steps)
 
@@ -427,11 +430,61 @@ def run_ours(args, wl):
             "roofline": roof, "decode_roofline": decode_roofline,
             "stages_ms": stage_ms, "e2e": e2e, "cpu_baseline": cpu,
             "gpu_launches": steps * LAUNCHES_PER_STEP(wl),
-            "clocks": clocks, "layers": nl,
+            "clocks": clocks, "layers": nl, "cache_append": cache_append,
         }
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
+
+
+def measure_cache_append(wl, dc, stream, hbm_peak):
+    """mla_cache_append (the page's do_kv_cache_update) on this workload's
+    cache: one new token per query row (the decode step's append) and a
+    32768-token chunk (a prefill chunk), bf16 rows into the bf16 cache, unique
+    random slots. CUDA-graph replays timed with events; algorithmic bytes =
+    tokens x (W x 2 read + W x 2 written + 8 slot bytes)."""
+    import torch
+    from mla_latent_cache_absorbed_gb300 import _native as N
+    g = wl.geom
+    if g.dtype != "bf16":
+        return None
+    W, R, P = g.width, g.kv_rank, g.d_rope
+    dev = dc.kv_cache.device
+    num_slots = dc.num_blocks * 16
+    res = {}
+    rng = np.random.default_rng(99)
+    # a scratch cache of the same geometry: the measured caches stay intact
+    cache = torch.empty((dc.num_blocks, 16, W), dtype=torch.bfloat16, device=dev)
+    for label, n in (("decode_step", wl.rows), ("chunk_32k", 32768)):
+        n = min(n, num_slots)
+        kv_c = torch.randn(n, R, device=dev).to(torch.bfloat16)
+        k_pe = torch.randn(n, max(P, 1), device=dev).to(torch.bfloat16)
+        slots = torch.from_numpy(rng.choice(num_slots, size=n, replace=False).astype(np.int64)).to(dev)
+        reps = 200 if n < 4096 else 20
+
+        def call():
+            N.mla_cache_append(cache, kv_c, k_pe if P else None, slots, n, dc.num_blocks, 1,
+                               dc.dims, None, stream)
+
+        call()
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for _ in range(reps):
+                call()
+        gr.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        gr.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        nbytes = n * (W * 2 * 2 + 8)
+        res[label] = {"tokens": n, "us": us, "bytes": nbytes,
+                      "achieved_GBps": nbytes / (us * 1e-6) / 1e9,
+                      "frac_of_hbm": nbytes / (us * 1e-6) / 1e9 / hbm_peak}
+    return res
 
 
 def LAUNCHES_PER_STEP(wl):

@@ -7,6 +7,7 @@
  *   mla_decode_paged    all heads attend MQA-style to the shared cache rows
  *                       [c_kv | k_pe], split over the keys, merged by LSE
  *   mla_decompress_out  decompress the latent output once through W_UV
+ *   mla_cache_append    write new tokens' latent rows into the paged cache
  *   mla_rope_norm_to_neox_perm / mla_permute_rope_cols / mla_permute_rope_rows
  *                       the host-side load-time rope permutation
  *
@@ -71,6 +72,7 @@ typedef struct mla_dims {
 #define MLA_DEVERR_SEQ_TOO_LONG 2u  /* seq_len > max_blocks * block_size */
 #define MLA_DEVERR_SEQ_SHORT 4u     /* 0 < seq_len < t_q, or seq_len < 0 */
 #define MLA_DEVERR_TIMEOUT 8u       /* a bounded wait inside a kernel gave up */
+#define MLA_DEVERR_BAD_SLOT 16u     /* mla_cache_append: a slot past the cache */
 
 /*
  * Absorb ("memra_engine/mla.rs source", fn mla_attend_absorbed, absorb step;
@@ -175,6 +177,30 @@ mla_status mla_decode_paged_static(void* out, float* lse, const void* q_abs,
  */
 mla_status mla_decompress_out(void* out, const void* o_lat, const void* w_uv,
                               int32_t rows, const mla_dims* dims, void* stream);
+
+/*
+ * Cache append ("vllm.v1.attention.backends.mla.cpu_mla",
+ * CPUMLAImpl.do_kv_cache_update): the step before decode on every token.
+ * With flat = kv_cache viewed as [num_blocks * 16][R + P], for every token n
+ * whose slot_mapping[n] >= 0:
+ *   flat[slot_mapping[n]] = [kv_c[n][0:R] | k_pe[n][0:P]]   cast to dims->dtype
+ * kv_cache     [num_blocks][16][R+P]  in/out, dims->dtype
+ * kv_c         [n_tokens][R]          in, src_dtype (MLA_F32 or MLA_BF16); the
+ *                                     latent rows, already RMS-normed
+ * k_pe         [n_tokens][P]          in, src_dtype, already roped; may be NULL
+ *                                     only when P == 0
+ * slot_mapping [n_tokens] int64       in; a negative slot is padding and is
+ *                                     skipped (the page's valid mask)
+ * A slot >= num_blocks * 16 is skipped and MLA_DEVERR_BAD_SLOT is OR-ed into
+ * the optional device word dev_err. The cast to bf16 rounds to nearest, ties
+ * to even; a NaN stays a NaN. Slots should be unique: when two tokens name
+ * one slot, the row that lands there is one of theirs, unspecified which.
+ * Buffers 16-byte aligned; n_tokens == 0 is a no-op. Stream-ordered, no sync.
+ */
+mla_status mla_cache_append(void* kv_cache, const void* kv_c, const void* k_pe,
+                            const int64_t* slot_mapping, int32_t n_tokens, int32_t num_blocks,
+                            int32_t src_dtype, const mla_dims* dims, int32_t* dev_err,
+                            void* stream);
 
 /*
  * Load-time rope permutation ("memra_engine/mla.rs source", fn

@@ -26,7 +26,8 @@ DEVERR_TIMEOUT = 8
 
 # Every exported symbol of include/mla.h.
 EXPORTS = ("mla_absorb_q", "mla_decode_workspace_size", "mla_decode_paged",
-           "mla_decode_paged_static", "mla_decompress_out", "mla_rope_norm_to_neox_perm",
+           "mla_decode_paged_static", "mla_decompress_out", "mla_cache_append",
+           "mla_rope_norm_to_neox_perm",
            "mla_permute_rope_cols", "mla_permute_rope_rows", "mla_status_str",
            "mla_last_error")
 
@@ -70,6 +71,7 @@ def load(path: str = LIB_PATH):
                                      ctypes.c_size_t, P, P]
     lib.mla_decode_paged_static.argtypes = [P, P, P, P, P, P, I32, I32, I32, D, F, P, P]
     lib.mla_decompress_out.argtypes = [P, P, P, I32, D, P]
+    lib.mla_cache_append.argtypes = [P, P, P, P, I32, I32, I32, D, P, P]
     lib.mla_rope_norm_to_neox_perm.argtypes = [I32, P]
     lib.mla_permute_rope_cols.argtypes = [P, I32, I64, I64, I32, I32]
     lib.mla_permute_rope_rows.argtypes = [P, I32, I64, I32, I32]
@@ -151,6 +153,14 @@ def mla_decompress_out(out, o_lat, w_uv, rows: int, dims: MlaDims, stream=None):
     _check("mla_decompress_out", load().mla_decompress_out(_ptr(out), _ptr(o_lat), _ptr(w_uv),
                                                            rows, ctypes.byref(dims),
                                                            _stream(stream)))
+
+
+def mla_cache_append(kv_cache, kv_c, k_pe, slot_mapping, n_tokens: int, num_blocks: int,
+                     src_dtype: int, dims: MlaDims, dev_err=None, stream=None):
+    _check("mla_cache_append",
+           load().mla_cache_append(_ptr(kv_cache), _ptr(kv_c), _ptr(k_pe), _ptr(slot_mapping),
+                                   n_tokens, num_blocks, src_dtype, ctypes.byref(dims),
+                                   _ptr(dev_err), _stream(stream)))
 
 
 def mla_rope_norm_to_neox_perm(n_dims: int) -> np.ndarray:

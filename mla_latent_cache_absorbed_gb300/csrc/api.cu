@@ -118,6 +118,32 @@ mla_status mla_absorb_q(void* q_abs, const void* q_nope, const void* q_pe, const
     return MLA_OK;
 }
 
+mla_status mla_cache_append(void* kv_cache, const void* kv_c, const void* k_pe,
+                            const int64_t* slot_mapping, int32_t n_tokens, int32_t num_blocks,
+                            int32_t src_dtype, const mla_dims* dims, int32_t* dev_err,
+                            void* stream) {
+    if (mla_status st = check_dims(dims)) return st;
+    REQUIRE(n_tokens >= 0 && num_blocks >= 0, "n_tokens and num_blocks must be >= 0");
+    REQUIRE(src_dtype == MLA_F32 || src_dtype == MLA_BF16, "src_dtype must be MLA_F32 or MLA_BF16");
+    if (n_tokens == 0) return MLA_OK;
+    REQUIRE(kv_cache && kv_c && slot_mapping, "kv_cache, kv_c and slot_mapping must be non-NULL");
+    REQUIRE(dims->d_rope == 0 || k_pe, "k_pe may be NULL only when d_rope == 0");
+    REQUIRE(aligned16(kv_cache) && aligned16(kv_c) && (!k_pe || aligned16(k_pe)) &&
+                ((uintptr_t)slot_mapping & 7u) == 0,
+            "kv_cache, kv_c and k_pe must be 16-byte aligned, slot_mapping 8-byte aligned");
+    // one 16-byte piece of a cache row never straddles kv_c and k_pe
+    const int piece = dims->dtype == MLA_BF16 ? 8 : 4;
+    if (dims->kv_rank % piece || dims->d_rope % piece) {
+        set_error("cache append: kv_rank and d_rope must be multiples of %d", piece);
+        return MLA_ERR_UNSUPPORTED;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    MLA_CUDA_TRY(launch_cache_append(kv_cache, kv_c, k_pe, slot_mapping, n_tokens, num_blocks,
+                                     src_dtype, *dims, dev_err, s),
+                 "cache append");
+    return MLA_OK;
+}
+
 mla_status mla_decompress_out(void* out, const void* o_lat, const void* w_uv, int32_t rows,
                               const mla_dims* dims, void* stream) {
     g_last_error[0] = 0;

@@ -30,6 +30,10 @@ struct SimtDecodePlan {
 SimtDecodePlan simt_decode_plan(int32_t batch, int32_t max_blocks, const mla_dims& d);
 
 // Launchers (SIMT kernels; any geometry within the documented limits).
+cudaError_t launch_cache_append(void* cache, const void* kv_c, const void* k_pe,
+                                const int64_t* slots, int32_t n_tokens, int32_t num_blocks,
+                                int32_t src_dtype, const mla_dims& d, int32_t* dev_err,
+                                cudaStream_t s);
 cudaError_t launch_absorb_simt(void* q_abs, const void* q_nope, const void* q_pe,
                                const void* w_uk, int32_t rows, const mla_dims& d,
                                cudaStream_t s);
