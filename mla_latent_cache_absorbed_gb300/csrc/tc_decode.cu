@@ -81,9 +81,9 @@ struct Ctrl {
     uint64_t sfull[2];      // S: scores ready (QK commit)
     uint64_t sfree[2];      // S: scores read (the 256 softmax threads)
     uint64_t pempty[2];     // S: P slot consumed (O-CTA PV commit)
-    uint64_t qready;        // S: Q stored in TMEM (128 threads)
+    uint64_t qready;        // S: Q stored in TMEM (256 softmax threads)
     uint64_t qland;         // S: first segment's queries landed in shared memory (TMA)
-    uint64_t qfree;         // S: those queries are in TMEM; stages 1-2 reusable (128)
+    uint64_t qfree;         // S: those queries are in TMEM; stages 1-2 reusable (256)
     uint64_t statack;       // S: O-CTA has read the segment statistics (1 remote)
     uint64_t pfull[2];      // O: P + alpha written (1 remote arrival per tile)
     uint64_t vready[kNS];   // O: tile tail zeroed (fix warp)
@@ -101,6 +101,8 @@ struct Ctrl {
     int32_t landed;         // O: tiles whose V has landed (paces the L2 prefetcher)
     float mstat[128];       // O: segment max (log2 units) per row
     float lstat[128];       // O: segment sum per row
+    long long walk_u, walk_ue;  // both: the pair's unit range (see walk_init)
+    int32_t walk_b, walk_g, walk_tile, walk_S, walk_nt, walk_ok;  // and its first unit
 };
 constexpr int kSmemBytes = kCtrlOff + (int)sizeof(Ctrl);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -112,11 +114,12 @@ struct Params {
     const int32_t* seq_lens;      // [B]
     __nv_bfloat16* out;           // [B][T][H][512]
     float* lse;                   // [B][T][H] or null
-    float* ws_o;                  // [2*NP slots][128 column quads][128 rows][4]
+    __nv_bfloat16* ws_o;          // partial rows: [2*NP slots][128 rows][512]
     float* ws_lse;                // [2*NP][128]
     int32_t* dev_err;
     int B, T, H, W, max_blocks, num_blocks;
     int NP, min_units;
+    int combine_rpt;              // combine: query rows per thread (1, 2 or 4)
     float scale_log2;
 };
 
@@ -146,58 +149,141 @@ __device__ __forceinline__ int pairs_per_set(const Params& p, int G, long long U
     return np_g;
 }
 
-// Total units of one set (warp-cooperative, identical in every lane).
-__device__ long long units_per_set(const Params& p, int lane) {
-    long long U = 0;
-    for (int b0 = 0; b0 < p.B; b0 += 32) {
-        const int b = b0 + lane;
-        long long v = b < p.B ? (long long)ntiles_of(p.seq_lens[b], p.T, p.max_blocks) : 0;
+// One chunk of 32 requests, warp-cooperative: lane l holds request b0 + l's
+// units v (0 past the batch), its seq_len S, and the inclusive prefix of v
+// within the chunk; total is the chunk's sum. Unit counts fit 32 bits (the
+// host requires batch * max_blocks <= 2^33).
+struct ChunkScan {
+    int v, S, incl, total;
+};
+__device__ __forceinline__ ChunkScan scan_chunk(const Params& p, int b0, int lane) {
+    const int b = b0 + lane;
+    ChunkScan c;
+    c.S = b < p.B ? p.seq_lens[b] : 0;
+    c.v = b < p.B ? ntiles_of(c.S, p.T, p.max_blocks) : 0;
+    c.incl = c.v;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        U += v;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, c.incl, o);
+        if (lane >= o) c.incl += t;
     }
-    return U;
+    c.total = __shfl_sync(0xffffffffu, c.incl, 31);
+    return c;
 }
 
-// This pair's set and unit range; warp-cooperative. Returns false when the
+// Request-aligned split. Request b (tiles_b units, prefix_b units before it)
+// gets the pairs [P_b, P_{b+1}) of its set, P_b = round(np_g prefix_b / U),
+// and its units evenly among them, so no pair holds two segments. Used when
+// every non-empty request gets a pair and no pair gets more than two tiles
+// above the even split's ceil(U / np_g): a pair holding two partial segments
+// costs more than that (an extra epilogue and a query reload). It is only
+// tried while a pair's share is small (then the straddling cost dominates)
+// and the arithmetic fits 32 bits.
+constexpr int kAlignedMaxShare = 32;  // tiles per pair
+__device__ __forceinline__ bool aligned_tried(long long U, int np_g) {
+    return U <= (long long)kAlignedMaxShare * np_g && 2 * (long long)np_g * U + U < (1LL << 31);
+}
+__device__ __forceinline__ int aligned_first_pair(long long prefix, long long U, int np_g) {
+    return (int)((2u * (uint32_t)np_g * (uint32_t)prefix + (uint32_t)U) / (2u * (uint32_t)U));
+}
+// Per chunk: lanes whose request gets no pair (bad) and the largest share.
+__device__ __forceinline__ void aligned_check(const ChunkScan& c, int base, long long U, int np_g,
+                                              int& bad, int& worst) {
+    const int n = aligned_first_pair(base + c.incl, U, np_g) -
+                  aligned_first_pair(base + c.incl - c.v, U, np_g);
+    if (c.v > 0) {
+        if (n <= 0) bad = 1;
+        else worst = max(worst, (int)(((uint32_t)c.v + (uint32_t)n - 1u) / (uint32_t)n));
+    }
+}
+__device__ __forceinline__ bool aligned_decide(int bad, int worst, long long U, int np_g) {
+    bad = __any_sync(0xffffffffu, bad);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) worst = max(worst, __shfl_xor_sync(0xffffffffu, worst, o));
+    return !bad && worst <= (U + np_g - 1) / np_g + 2;
+}
+// warp-cooperative; the same answer in every lane
+__device__ bool split_is_aligned(const Params& p, long long U, int np_g, int lane) {
+    if (!aligned_tried(U, np_g)) return false;
+    int base = 0, worst = 0, bad = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+        const ChunkScan c = scan_chunk(p, b0, lane);
+        aligned_check(c, base, U, np_g, bad, worst);
+        base += c.total;
+    }
+    return aligned_decide(bad, worst, U, np_g);
+}
+
+// This pair's set and unit range; warp-cooperative, at most two passes over
+// seq_lens (one load when the batch fits a chunk). Returns false when the
 // pair has no work.
 __device__ bool walk_init(const Params& p, int pair, Walk& w) {
     const int lane = threadIdx.x & 31;
     const int Mq = p.T * p.H;
     const int G = (Mq + 127) / 128;
-    const long long U = units_per_set(p, lane);
+    ChunkScan c0 = scan_chunk(p, 0, lane);
+    int U = c0.total;
+    for (int b0 = 32; b0 < p.B; b0 += 32) U += scan_chunk(p, b0, lane).total;
     if (U == 0) return false;
     const int np_g = pairs_per_set(p, G, U);
     const int g = pair / np_g, k = pair % np_g;
     if (g >= G) return false;
-    const long long ub = U * k / np_g, ue = U * (k + 1) / np_g;
-    if (ub >= ue) return false;
-    // locate unit ub
-    long long base = 0;
-    int found_b = -1;
-    long long found_base = 0;
-    for (int b0 = 0; b0 < p.B && found_b < 0; b0 += 32) {
-        const int b = b0 + lane;
-        long long v = b < p.B ? (long long)ntiles_of(p.seq_lens[b], p.T, p.max_blocks) : 0;
-        long long incl = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            long long t = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += t;
-        }
-        const unsigned hit = __ballot_sync(0xffffffffu, b < p.B && base + incl > ub);
-        if (hit) {
+    const bool tried = aligned_tried(U, np_g);
+    const int ub_even = (int)((long long)U * k / np_g), ue_even = (int)((long long)U * (k + 1) / np_g);
+    // one pass: the even split's first request, the aligned split's request
+    // for pair k, and whether the aligned split is used
+    int base = 0, worst = 0, bad = 0;
+    int ev_b = -1, ev_first = 0, ev_S = 0;
+    int al_b = -1, al_first = 0, al_S = 0, al_v = 0, al_p0 = 0, al_n = 1;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+        const ChunkScan c = b0 == 0 ? c0 : scan_chunk(p, b0, lane);
+        const int excl = base + c.incl - c.v, incl = base + c.incl;
+        const unsigned hit = __ballot_sync(0xffffffffu, incl > ub_even && c.v > 0);
+        if (ev_b < 0 && hit) {
             const int l = __ffs(hit) - 1;
-            found_b = b0 + l;
-            found_base = base + __shfl_sync(0xffffffffu, incl - v, l);
+            ev_b = b0 + l;
+            ev_first = __shfl_sync(0xffffffffu, excl, l);
+            ev_S = __shfl_sync(0xffffffffu, c.S, l);
         }
-        base += __shfl_sync(0xffffffffu, incl, 31);
+        if (tried) {
+            aligned_check(c, base, U, np_g, bad, worst);
+            const int pb = aligned_first_pair(excl, U, np_g), pe = aligned_first_pair(incl, U, np_g);
+            const unsigned ah = __ballot_sync(0xffffffffu, c.v > 0 && pb <= k && k < pe);
+            if (al_b < 0 && ah) {
+                const int l = __ffs(ah) - 1;
+                al_b = b0 + l;
+                al_first = __shfl_sync(0xffffffffu, excl, l);
+                al_S = __shfl_sync(0xffffffffu, c.S, l);
+                al_v = __shfl_sync(0xffffffffu, c.v, l);
+                al_p0 = __shfl_sync(0xffffffffu, pb, l);
+                al_n = __shfl_sync(0xffffffffu, pe - pb, l);
+            }
+        }
+        base += c.total;
     }
-    w.b = found_b;
+    const bool aligned = tried && aligned_decide(bad, worst, U, np_g);
+    int ub, ue, fb, first, S;
+    if (aligned) {
+        if (al_b < 0) return false;
+        ub = al_first + (int)((uint32_t)al_v * (uint32_t)(k - al_p0) / (uint32_t)al_n);
+        ue = al_first + (int)((uint32_t)al_v * (uint32_t)(k - al_p0 + 1) / (uint32_t)al_n);
+        fb = al_b;
+        first = al_first;
+        S = al_S;
+    } else {
+        if (ev_b < 0) return false;
+        ub = ub_even;
+        ue = ue_even;
+        fb = ev_b;
+        first = ev_first;
+        S = ev_S;
+    }
+    if (ub >= ue) return false;
+    w.b = fb;
     w.g = g;
-    w.S = p.seq_lens[found_b];
-    w.ntiles = ntiles_of(w.S, p.T, p.max_blocks);
-    w.tile = (int)(ub - found_base);
+    w.S = S;
+    w.ntiles = ntiles_of(S, p.T, p.max_blocks);
+    w.tile = ub - first;
     w.u = ub;
     w.u_end = ue;
     return true;
@@ -246,19 +332,67 @@ struct Waiter {
     __device__ bool wait_warp(uint32_t bar, uint32_t parity) {
         return __all_sync(0xffffffffu, wait(bar, parity));
     }
+    // the same without suspension hints: for short waits on the critical
+    // path (a barrier among the row warps)
+    __device__ bool spin_warp(uint32_t bar, uint32_t parity) {
+        bool ok = mbar_try_wait(bar, parity);
+        if (!ok) {
+            const uint64_t t0 = globaltimer_ns();
+            for (uint32_t i = 1;; ++i) {
+                if (mbar_try_wait(bar, parity)) { ok = true; break; }
+                if ((i & 255) == 0) {
+                    if (*abort) break;
+                    if (globaltimer_ns() - t0 > kWaitLimit) {
+                        *abort = 1;
+                        if (dev_err) atomicOr(dev_err, (int32_t)MLA_DEVERR_TIMEOUT);
+                        break;
+                    }
+                }
+            }
+        }
+        return __all_sync(0xffffffffu, ok);
+    }
 };
 
-// Bounded barrier among the 128 row threads (warps 2..5) of one CTA; `phase`
+// Bounded barrier among the 256 row threads (warps 5..12) of one CTA; `phase`
 // counts the caller's uses. Returns false on timeout.
 __device__ __forceinline__ bool rows_sync(Waiter& wt, uint32_t bar, uint32_t& phase) {
     mbar_arrive(bar);
-    return wt.wait_warp(bar, (phase++) & 1);
+    return wt.spin_warp(bar, (phase++) & 1);
 }
 
 __device__ __forceinline__ int valid_blocks(const Walk& w) {
     const int rem = w.S - w.tile * kTok;
     const int nb = (rem + 15) / 16;
     return nb < 4 ? nb : 4;
+}
+
+// One epilogue step of a warp: its 32 rows x 64 columns of O (x0, x1: this
+// lane's row, f32), scaled by inv, go out as bf16 through a 4 KB scratch so
+// that each store writes whole 128-byte row pieces (lane l: 16 bytes l % 8 of
+// row 4 i + l / 8; rows from row_lim on are not written).
+__device__ __forceinline__ void epilogue_emit64(uint32_t scr, int lane, const uint32_t (&x0)[32],
+                                                const uint32_t (&x1)[32], float inv,
+                                                __nv_bfloat16* dst0, int col, int row_lim) {
+    const uint32_t rowa = scr + lane * 128;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const uint32_t* x = u < 4 ? &x0[8 * u] : &x1[8 * (u - 4)];
+        st_shared_v4(rowa + ((u ^ (lane & 7)) << 4),
+                     pack_bf16x2(__uint_as_float(x[0]) * inv, __uint_as_float(x[1]) * inv),
+                     pack_bf16x2(__uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv),
+                     pack_bf16x2(__uint_as_float(x[4]) * inv, __uint_as_float(x[5]) * inv),
+                     pack_bf16x2(__uint_as_float(x[6]) * inv, __uint_as_float(x[7]) * inv));
+    }
+    __syncwarp();
+    const int pc = lane & 7;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int rw = 4 * i + (lane >> 3);
+        const uint4 val = ld_shared_v4(scr + rw * 128 + ((pc ^ (rw & 7)) << 4));
+        if (rw < row_lim) *reinterpret_cast<uint4*>(dst0 + (long long)rw * 512 + col + pc * 8) = val;
+    }
+    __syncwarp();
 }
 
 // ------------------------------------------------------------------ kernel
@@ -279,8 +413,7 @@ __device__ __forceinline__ int valid_blocks(const Walk& w) {
 template <int W>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_pair_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap qmap,
-                       const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
-                       const Params p) {
+                       const __grid_constant__ CUtensorMap vmap, const Params p) {
     constexpr int NKC = W / 64;  // 64-column chunks in a cache row (9 or 8)
     extern __shared__ __align__(1024) unsigned char smem[];
     Ctrl& c = *reinterpret_cast<Ctrl*>(smem + kCtrlOff);
@@ -307,10 +440,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&c.pempty[i]), 1);
             mbar_init(smem_u32(&c.pfull[i]), 1);
         }
-        mbar_init(smem_u32(&c.qready), 128);
+        mbar_init(smem_u32(&c.qready), 256);
         mbar_init(smem_u32(&c.qland), 1);
         mbar_init(smem_u32(&c.qmoved), 1);
-        mbar_init(smem_u32(&c.qfree), 128);
+        mbar_init(smem_u32(&c.qfree), 256);
         mbar_init(smem_u32(&c.statack), 1);
         mbar_init(smem_u32(&c.odone), 1);
         mbar_init(smem_u32(&c.evt), 1);
@@ -325,13 +458,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_u32(&c.tmem_base), 512);
         tmem_relinquish();
     }
+    if (warp == 2) {
+        // the pair's unit range, worked out once per CTA while the barriers and
+        // TMEM are set up; every warp starts its walk from it
+        Walk w0;
+        const bool ok = walk_init(p, pair, w0);
+        if (lane == 0) {
+            c.walk_ok = ok ? 1 : 0;
+            if (ok) {
+                c.walk_u = w0.u;
+                c.walk_ue = w0.u_end;
+                c.walk_b = w0.b;
+                c.walk_g = w0.g;
+                c.walk_tile = w0.tile;
+                c.walk_S = w0.S;
+                c.walk_nt = w0.ntiles;
+            }
+        }
+    }
     tc_fence_before();
     cluster_sync();
     tc_fence_after();
     const uint32_t tbase = c.tmem_base;
 
     Walk w;
-    const bool has_work = walk_init(p, pair, w);
+    const bool has_work = c.walk_ok != 0;
+    if (has_work) {
+        w.b = c.walk_b;
+        w.g = c.walk_g;
+        w.tile = c.walk_tile;
+        w.S = c.walk_S;
+        w.ntiles = c.walk_nt;
+        w.u = c.walk_u;
+        w.u_end = c.walk_ue;
+    }
     const long long ub = has_work ? w.u : 0;
     const int Mq = p.T * p.H;
 
@@ -347,10 +507,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tma_prefetch_desc(&tmap);
                     tma_prefetch_desc(&qmap);
                     // the first segment's queries: TMA into stages 1 and 2 (free until
-                    // the rows move them to TMEM), while tile 0 goes to stage 0
-                    // the queries come from the previous kernel (programmatic launch)
+                    // the rows move them to TMEM), while tile 0 goes to stage 0.
+                    // They come from the previous kernel (programmatic launch).
+                    // (a request's rows past t_q * n_head are outside the map)
                     grid_dependency_wait();
-                    // (a request's rows past t_q * n_head are outside the map: not read)
                     const int qrows = Mq < 128 ? Mq : 128;
                     mbar_arrive_expect_tx(smem_u32(&c.qland), (uint32_t)(NKC * qrows * 128));
                     for (int cc = 0; cc < NKC; ++cc)
@@ -441,7 +601,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int R = q * 32 + h * 16 + (lane >> 2) + 8 * (lane & 1);  // query row
             const int par = (lane >> 1) & 1;                          // odd columns
             const uint32_t lane_base16 = (uint32_t)(q * 32 + h * 16) << 16;
-            const uint32_t lane_off = (uint32_t)(q * 32) << 16;      // Q moves: warps 5..8
+            const uint32_t lane_off = (uint32_t)(q * 32) << 16;      // Q moves
             const int rq = q * 32 + lane;                             // their row
             const uint32_t pslot_remote = mapa(smem_u32(smem + kSideOff), 1);
             const uint32_t pfull_remote = mapa(smem_u32(&c.pfull[0]), 1);
@@ -456,13 +616,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int seg = 0;
             uint32_t rphase = 0;
             float m_used = -INFINITY, l = 0.f;
-            int horizon = 0, bad = 0, seg_tile0 = 0;
+            int horizon = 0, bad = 0;
             bool row_ok = false;
             for (; w.u < w.u_end; walk_next(p, w), ++i) {
                 const int buf = (int)(i & 1);
                 const bool first_tile = seg_first(w, ub);
                 if (first_tile) {
-                    seg_tile0 = w.tile;
                     const int grow = w.g * 128 + R;
                     row_ok = grow < Mq;
                     const int t = row_ok ? grow / p.H : 0;
@@ -470,15 +629,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     m_used = -INFINITY;
                     l = 0.f;
                     bad = 0;
-                    if (h == 0) {
-                        // warps 5..8 move the segment's queries into TMEM, a row each
+                    {
+                        // all eight warps move the segment's queries into TMEM, a row
+                        // per thread: warps 5..8 chunks [0, kQSplit), warps 9..12 the rest
+                        constexpr int kQSplit = (NKC + 1) / 2;
+                        const int c0 = h ? kQSplit : 0, c1 = h ? NKC : kQSplit;
                         const int growq = w.g * 128 + rq;
                         const bool rq_ok = growq < Mq;
                         if (seg == 0) {
                             // landed in shared memory by TMA
                             if (!wt.wait_warp(smem_u32(&c.qland), 0)) break;
 #pragma unroll 1
-                            for (int cc = 0; cc < NKC; ++cc) {
+                            for (int cc = c0; cc < c1; ++cc) {
                                 const uint32_t rowa = smem_u32(smem + q_chunk_off(cc)) + rq * 128;
                                 uint32_t v[32];
 #pragma unroll
@@ -494,29 +656,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             tmem_wait_st();
                             mbar_arrive(smem_u32(&c.qfree));  // stages 1 and 2 may be refilled
                         } else {
-                            // later segments: from global memory (warmed in L2 by the loader)
+                            // later segments: from global memory (warmed in L2 by the
+                            // loader), two chunks per round trip
                             const uint4* src = reinterpret_cast<const uint4*>(
                                 p.q_abs + ((long long)w.b * Mq + (rq_ok ? growq : 0)) * W);
 #pragma unroll 1
-                            for (int cc = 0; cc < NKC; ++cc) {
-                                uint4 x[8];
+                            for (int cc = c0; cc < c1; cc += 2) {
+                                const bool two = cc + 1 < c1;
+                                uint4 x[16];
 #pragma unroll
-                                for (int j = 0; j < 8; ++j)
-                                    x[j] = rq_ok ? src[cc * 8 + j] : make_uint4(0, 0, 0, 0);
-                                uint32_t v[32];
+                                for (int j = 0; j < 16; ++j)
+                                    x[j] = (rq_ok && (j < 8 || two)) ? src[cc * 8 + j] : make_uint4(0, 0, 0, 0);
 #pragma unroll
-                                for (int j = 0; j < 8; ++j) {
-                                    v[4 * j] = x[j].x;
-                                    v[4 * j + 1] = x[j].y;
-                                    v[4 * j + 2] = x[j].z;
-                                    v[4 * j + 3] = x[j].w;
+                                for (int k = 0; k < 2; ++k) {
+                                    if (k == 1 && !two) break;
+                                    uint32_t v[32];
+#pragma unroll
+                                    for (int j = 0; j < 8; ++j) {
+                                        v[4 * j] = x[8 * k + j].x;
+                                        v[4 * j + 1] = x[8 * k + j].y;
+                                        v[4 * j + 2] = x[8 * k + j].z;
+                                        v[4 * j + 3] = x[8 * k + j].w;
+                                    }
+                                    tmem_st32(tq + lane_off + (cc + k) * 32, v);
                                 }
-                                tmem_st32(tq + lane_off + cc * 32, v);
                             }
                             tmem_wait_st();
                         }
                         tc_fence_before();
                         mbar_arrive(smem_u32(&c.qready));
+                    }
+                    // invalid block ids anywhere in the segment void it (the loader
+                    // loaded a stand-in block): the softmax warps scan its table
+                    // slice now, while the first QK runs; the segment's end reads it
+                    {
+                        const long long left = w.u_end - 1 - w.u;
+                        const int last_tile = (int)min((long long)w.ntiles - 1, (long long)w.tile + left);
+                        const int blk0 = w.tile * 4;
+                        const int blk1 = min(last_tile * 4 + 4, (w.S + 15) / 16);
+                        const int32_t* bt = p.block_table + (long long)w.b * p.max_blocks;
+                        int b_any = 0;
+                        for (int k = blk0 + sw * 32 + lane; k < blk1; k += kSmxWarps * 32) {
+                            const int32_t blk = bt[k];
+                            b_any |= (blk < 0 || blk >= p.num_blocks);
+                        }
+                        b_any = __any_sync(0xffffffffu, b_any);
+                        if (lane == 0) c.badw[sw] = b_any;
                     }
                 }
                 if (!wt.wait_warp(smem_u32(&c.sfull[buf]), (uint32_t)((i >> 1) & 1))) break;
@@ -591,20 +776,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                  any ? 1u : 0u, pbar);
                 if (seg_last(w)) {
                     const float l_row = l + __shfl_xor_sync(0xffffffffu, l, 2);
-                    // invalid block ids anywhere in the segment void it (the loader
-                    // loaded a stand-in block): the softmax threads scan its table slice
-                    {
-                        const int blk0 = seg_tile0 * 4;
-                        const int blk1 = min(w.tile * 4 + 4, (w.S + 15) / 16);
-                        const int32_t* bt = p.block_table + (long long)w.b * p.max_blocks;
-                        int b_any = 0;
-                        for (int k = blk0 + sw * 32 + lane; k < blk1; k += kSmxWarps * 32) {
-                            const int32_t blk = bt[k];
-                            b_any |= (blk < 0 || blk >= p.num_blocks);
-                        }
-                        b_any = __any_sync(0xffffffffu, b_any);
-                        if (lane == 0) c.badw[sw] = b_any;
-                    }
                     if (!rows_sync(wt, smem_u32(&c.rowbar), rphase)) break;
                     bad = 0;
 #pragma unroll
@@ -850,74 +1021,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const bool empty = seg_bad || !(lsum > 0.f);
                 const float inv = empty ? 0.f : 1.f / lsum;
                 const float lse_v = empty ? -INFINITY : (m + log2f(lsum)) * 0.69314718055994531f;
-                bool ok = true;
-                if (full_seg) {
-                    // bf16 rows through the freed V stage: four [128 rows][64 columns]
-                    // swizzled boxes per pass (two from each column half), stored by
-                    // TMA (rows past the request's query rows fall outside the output
-                    // map and are not written)
-                    const uint32_t stg = smem_u32(smem + stage * kStage);
+                // bf16 rows: each warp takes its 32 rows and its half of the
+                // columns, 64 at a time, through a private 4 KB scratch in the
+                // freed V stage, and writes whole 128-byte row pieces (lane l
+                // stores piece l % 8 of row 4 i + l / 8). A full segment writes
+                // the output rows, a partial one its workspace slot, which the
+                // combine merges.
+                const int slot = pair * 2 + (seg == 0 ? 0 : 1);
+                {
+                    const uint32_t scr = smem_u32(smem + stage * kStage) + (uint32_t)(warp - 5) * 4096;
+                    __nv_bfloat16* dst0 = full_seg ? p.out + ((long long)w.b * Mq + w.g * 128 + q * 32) * 512
+                                                   : p.ws_o + ((long long)slot * 128 + q * 32) * 512;
+                    const int row_lim = min(32, min(128, Mq - w.g * 128) - q * 32);  // valid rows
 #pragma unroll 1
-                    for (int pass = 0; pass < 2 && ok; ++pass) {
-#pragma unroll 1
-                        for (int k2 = 0; k2 < 2; ++k2) {
-                            const int k = hc * 2 + k2;                 // box slot in the stage
-                            const int cb = hc * 4 + pass * 2 + k2;     // 64-column block
-                            uint32_t v0[32], v1[32];
-                            tmem_ld32(tbase + lane_off + cb * 64, v0);
-                            tmem_ld32(tbase + lane_off + cb * 64 + 32, v1);
-                            tmem_wait_ld();
-                            const uint32_t rowa = stg + k * kQChunk + r * 128;
-#pragma unroll
-                            for (int u = 0; u < 8; ++u) {
-                                const uint32_t* x = u < 4 ? &v0[8 * u] : &v1[8 * (u - 4)];
-                                st_shared_v4(rowa + ((u ^ (r & 7)) << 4),
-                                             pack_bf16x2(__uint_as_float(x[0]) * inv, __uint_as_float(x[1]) * inv),
-                                             pack_bf16x2(__uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv),
-                                             pack_bf16x2(__uint_as_float(x[4]) * inv, __uint_as_float(x[5]) * inv),
-                                             pack_bf16x2(__uint_as_float(x[6]) * inv, __uint_as_float(x[7]) * inv));
-                            }
-                        }
-                        fence_proxy_async_smem();
-                        if (!rows_sync(wt, smem_u32(&c.rowbar), rphase)) { ok = false; break; }
-                        if (lead && r == 0) {
-#pragma unroll 1
-                            for (int k = 0; k < 4; ++k)
-                                tma_store_3d(&omap, stg + k * kQChunk, ((k >> 1) * 4 + pass * 2 + (k & 1)) * 64,
-                                             w.g * 128, w.b);
-                            bulk_commit();
-                            bulk_wait_read_all();
-                        }
-                        if (!rows_sync(wt, smem_u32(&c.rowbar), rphase)) { ok = false; break; }
-                    }
-                    if (lead && row_ok && p.lse) p.lse[(long long)w.b * Mq + grow] = lse_v;
-                } else if (row_ok) {
-                    // f32 partial; layout [slot][column quad][128 rows][4], so the 32
-                    // lanes of a store write 512 contiguous bytes. TMEM is read two
-                    // 32-column blocks at a time (one wait per 64 columns).
-                    const int slot = pair * 2 + (seg == 0 ? 0 : 1);
-                    float4* dst = reinterpret_cast<float4*>(p.ws_o + (long long)slot * 128 * 512) + r;
-#pragma unroll 1
-                    for (int cc = c_lo; cc < c_lo + 256; cc += 64) {
-                        uint32_t v[2][32];
-#pragma unroll
-                        for (int k = 0; k < 2; ++k) tmem_ld32(tbase + lane_off + cc + 32 * k, v[k]);
+                    for (int cb = c_lo; cb < c_lo + 256; cb += 64) {
+                        uint32_t v0[32], v1[32];
+                        tmem_ld32(tbase + lane_off + cb, v0);
+                        tmem_ld32(tbase + lane_off + cb + 32, v1);
                         tmem_wait_ld();
-#pragma unroll
-                        for (int k = 0; k < 2; ++k)
-#pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                dst[((cc + 32 * k) / 4 + j) * 128] =
-                                    make_float4(__uint_as_float(v[k][4 * j]) * inv,
-                                                __uint_as_float(v[k][4 * j + 1]) * inv,
-                                                __uint_as_float(v[k][4 * j + 2]) * inv,
-                                                __uint_as_float(v[k][4 * j + 3]) * inv);
+                        epilogue_emit64(scr, lane, v0, v1, inv, dst0, cb, row_lim);
                     }
-                    if (lead)
+                    // the scratch is in a stage the async proxy refills next
+                    fence_proxy_async_smem();
+                }
+                if (lead && row_ok) {
+                    if (full_seg) {
+                        if (p.lse) p.lse[(long long)w.b * Mq + grow] = lse_v;
+                    } else {
                         p.ws_lse[(long long)slot * 128 + r] =
                             seg_bad ? __int_as_float(0x7fc00000) : lse_v;  // NaN marks bad
+                    }
                 }
-                if (!ok) break;
                 tc_fence_before();
                 mbar_arrive(smem_u32(&c.evtdone));
                 ++seg;
@@ -928,7 +1062,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     seg_tile0 = w.tile;
                 }
             }
-            if (lead && r == 0) bulk_wait_all();  // the epilogue's TMA stores have completed
             __syncwarp();
         }
     }
@@ -942,37 +1075,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ combine
 // Merges the partial segments of row groups that were split across pairs
-// (LSE-weighted, in pair order) and writes the rows of empty or invalid
-// requests. One CTA per (request, row group, 64-column slice); thread t takes
-// row t % 128 and the four column quads 4 (t / 128) .. + 3 of the slice, so a
-// warp reads 32 consecutive rows of one quad (512 contiguous bytes). A thread
-// loads the LSEs and quads of kCombineBatch parts at once and merges them with
-// a running maximum: one memory round trip per batch of parts.
+// (LSE-weighted: out = sum_k exp(lse_k - lse) o_k with lse = log sum_k
+// exp(lse_k)) and writes the rows of empty or invalid requests. One CTA per
+// (request, row group, 4 * rpt query rows), rpt = 1, 2, 4 or 8 picked by the
+// host so that the CTAs holding rows fit in one wave. Thread t takes the eight columns 8 (t % 64) .. + 7
+// of rows t / 64 + 4 j (j < rpt), so a warp reads 512 contiguous bytes of one
+// partial row. Its (row, part) items are walked row by row, kCombineBatch
+// loads in flight at a time, so a request split into a few parts costs one
+// memory round trip for all the thread's rows. The parts' LSEs of all the
+// CTA's rows are loaded together while the first loads are in flight; one
+// warp per row then works out its weights.
 //
 // Launched as a programmatic dependent of the decode kernel: everything up to
 // the partials' first read overlaps the decode kernel's tail.
-constexpr int kCombineThreads = 512;
-constexpr int kCombineSlices = 8;
-constexpr int kCombineBatch = 4;
+constexpr int kCombineThreads = 256;
+constexpr int kCombineBatch = 16;     // loads in flight per thread
+constexpr int kCombineMaxRpt = 8;     // rows per thread
+constexpr int kCombineMaxParts = 256; // parts per row group (pairs of a set)
 
-__global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(const Params p) {
+__device__ __forceinline__ uint4 load_part(const Params& p, long long slot, int r, int c8) {
+    return reinterpret_cast<const uint4*>(p.ws_o + (slot * 128 + r) * 512)[c8];
+}
+
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const Params p) {
     __shared__ int sh_parts[3];  // first pair, part count, first part's slot offset
-    const int tid = threadIdx.x, lane = tid & 31;
+    __shared__ float sh_w[4 * kCombineMaxRpt][kCombineMaxParts];
+    __shared__ float sh_lse[4 * kCombineMaxRpt];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Mq = p.T * p.H;
     const int G = (Mq + 127) / 128;
-    const int slice = (int)(blockIdx.x % kCombineSlices);
-    const long long bg = blockIdx.x / kCombineSlices;
+    const int rpt = p.combine_rpt;
+    const int cr = 4 * rpt;                 // rows per CTA
+    const int nq = 128 / cr;                // CTAs per row group
+    const int quad = (int)(blockIdx.x % nq);
+    const long long bg = blockIdx.x / nq;
     if (bg >= (long long)p.B * G) return;
     const int b = (int)(bg / G), g = (int)(bg % G);
     const int rows = min(128, Mq - g * 128);
-    const int r = tid & 127;
-    const int q0 = slice * 16 + (tid >> 7) * 4;   // first of this thread's 4 column quads
+    const int row0 = quad * cr;             // the CTA's first row within the group
+    if (row0 >= rows) return;               // rows past the group: nothing to do
+    const int rr = tid >> 6;                // the thread's rows: row0 + rr + 4 j
+    const int c8 = tid & 63;                // eight-column group
     const int S = p.seq_lens[b];
     const int nt = ntiles_of(S, p.T, p.max_blocks);
-    const long long orow = (long long)b * Mq + g * 128 + r;
+    const long long orow0 = (long long)b * Mq + g * 128;
     // which pairs hold this row group, from seq_lens alone (as the decode
     // kernel partitions the units); one warp works it out for the CTA
-    if (tid < 32 && nt > 0) {
+    if (warp == 0 && nt > 0) {
         long long U = 0, before = 0;
         for (int b0 = 0; b0 < p.B; b0 += 32) {
             const int bb = b0 + lane;
@@ -986,9 +1135,17 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(const Param
             U += v;
             before += vb;
         }
-        if (lane == 0) {
+        const int np_g = pairs_per_set(p, G, U);
+        const bool aligned = split_is_aligned(p, U, np_g, lane);
+        if (lane == 0 && aligned) {
+            // the request's own pairs, each holding one segment of it
+            const long long pb = aligned_first_pair(before, U, np_g);
+            const long long pe = aligned_first_pair(before + nt, U, np_g);
+            sh_parts[0] = g * np_g + (int)pb;
+            sh_parts[1] = (int)(pe - pb);
+            sh_parts[2] = 0;
+        } else if (lane == 0) {
             const long long u0 = before, u1 = u0 + nt;  // within row group g's set
-            const int np_g = pairs_per_set(p, G, U);
             auto owner = [&](long long u) {  // pair of the set whose range holds unit u
                 long long pp = (u * np_g) / U;
                 while (pp + 1 < np_g && U * (pp + 1) / np_g <= u) ++pp;
@@ -1007,78 +1164,119 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(const Param
     // also write) are touched: wait for it to complete
     grid_dependency_wait();
     if (nt == 0) {
-        if (slice == 0 && g == 0 && tid == 0 && p.dev_err) {
+        if (quad == 0 && g == 0 && tid == 0 && p.dev_err) {
             if (S < 0 || (S > 0 && S < p.T)) atomicOr(p.dev_err, (int32_t)MLA_DEVERR_SEQ_SHORT);
             else if (S > p.max_blocks * 16) atomicOr(p.dev_err, (int32_t)MLA_DEVERR_SEQ_TOO_LONG);
         }
-        if (r < rows) {
-            uint2* dst = reinterpret_cast<uint2*>(p.out + orow * 512 + q0 * 4);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) dst[k] = make_uint2(0u, 0u);
-            if (slice == 0 && q0 == 0 && p.lse) p.lse[orow] = -INFINITY;
+        for (int j = 0; j < rpt; ++j) {
+            const int r = row0 + rr + 4 * j;
+            if (r < rows) {
+                reinterpret_cast<uint4*>(p.out + (orow0 + r) * 512)[c8] = make_uint4(0u, 0u, 0u, 0u);
+                if (c8 == 0 && p.lse) p.lse[orow0 + r] = -INFINITY;
+            }
         }
         return;
     }
     __syncthreads();
     const int pf = sh_parts[0], nparts = sh_parts[1], slot0_off = sh_parts[2];
-    if (nparts <= 1 || r >= rows) return;  // one pair held the whole row group and wrote it
-    float m = -INFINITY, wsum = 0.f;
-    float4 acc[4];
+    if (nparts <= 1) return;  // one pair held the whole row group and wrote it
+    auto slot_of = [&](int k) -> long long {
+        return (long long)(pf + k) * 2 + (k == 0 ? slot0_off : 0);
+    };
+    // the thread's items (row j, part k), f = j * nparts + k; rows past the
+    // group are skipped. The first batch is in flight while the weights are
+    // worked out.
+    const int nitems = rpt * nparts;
+    uint4 v[kCombineBatch];
+    {
+        int j = 0, k = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-    bool bad = false;
-    const float4* ws4 = reinterpret_cast<const float4*>(p.ws_o);
-    for (int k0 = 0; k0 < nparts; k0 += kCombineBatch) {
-        const int nk = min(kCombineBatch, nparts - k0);
-        float ls[kCombineBatch];
-        float4 v[kCombineBatch][4];
+        for (int q = 0; q < kCombineBatch; ++q) {
+            const int r = row0 + rr + 4 * j;
+            if (q < nitems && r < rows) v[q] = load_part(p, slot_of(k), r, c8);
+            if (++k == nparts) { k = 0; ++j; }
+        }
+    }
+    // the parts' LSEs of the CTA's rows, all at once
+    for (int idx = tid; idx < cr * nparts; idx += kCombineThreads) {
+        const int cw = idx / nparts, k = idx - cw * nparts;
+        const int r = row0 + cw;
+        if (r < rows) sh_w[cw][k] = p.ws_lse[slot_of(k) * 128 + r];
+    }
+    __syncthreads();
+    // weights: warp w takes the CTA's rows w, w + 8, ...; NaN marks a part that
+    // met an invalid block id (the row is voided)
+    for (int cw = warp; cw < cr; cw += 8) {
+        const int r = row0 + cw;
+        if (r >= rows) continue;
+        float m = -INFINITY;
+        int bad = 0;
+        for (int k = lane; k < nparts; k += 32) {
+            const float l = sh_w[cw][k];
+            bad |= (l != l);
+            m = fmaxf(m, l);
+        }
 #pragma unroll
-        for (int j = 0; j < kCombineBatch; ++j) {
-            if (j < nk) {
-                const long long slot = (long long)(pf + k0 + j) * 2 + (k0 + j == 0 ? slot0_off : 0);
-                ls[j] = p.ws_lse[slot * 128 + r];
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        bad = __any_sync(0xffffffffu, bad);
+        float sum = 0.f;
+        for (int k = lane; k < nparts; k += 32) {
+            const float l = sh_w[cw][k];
+            const float e = (l == -INFINITY || m == -INFINITY) ? 0.f : expf(l - m);
+            sh_w[cw][k] = e;
+            sum += e;
+        }
 #pragma unroll
-                for (int q = 0; q < 4; ++q) v[j][q] = ws4[(slot * 128 + q0 + q) * 128 + r];
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        const bool empty = bad || !(sum > 0.f);
+        const float inv = empty ? 0.f : 1.f / sum;
+        for (int k = lane; k < nparts; k += 32) sh_w[cw][k] *= inv;
+        if (lane == 0) sh_lse[cw] = empty ? -INFINITY : m + logf(sum);
+    }
+    __syncthreads();
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    int j = 0, k = 0;  // the item after the last accumulated one
+    for (int f0 = 0; f0 < nitems; f0 += kCombineBatch) {
+        if (f0 > 0) {
+            int jj = j, kk = k;
+#pragma unroll
+            for (int q = 0; q < kCombineBatch; ++q) {
+                const int r = row0 + rr + 4 * jj;
+                if (f0 + q < nitems && r < rows) v[q] = load_part(p, slot_of(kk), r, c8);
+                if (++kk == nparts) { kk = 0; ++jj; }
             }
         }
 #pragma unroll
-        for (int j = 0; j < kCombineBatch; ++j) {
-            if (j < nk) {
-                bad |= (ls[j] != ls[j]);
-                if (ls[j] > m) {  // a new maximum: rescale what has been summed
-                    const float a = (m == -INFINITY) ? 0.f : expf(m - ls[j]);
-                    wsum *= a;
+        for (int q = 0; q < kCombineBatch; ++q) {
+            if (f0 + q < nitems) {
+                const int cw = rr + 4 * j;
+                const int r = row0 + cw;
+                if (r < rows) {
+                    const float wk = sh_w[cw][k];
+                    const uint32_t u[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        acc[q].x *= a;
-                        acc[q].y *= a;
-                        acc[q].z *= a;
-                        acc[q].w *= a;
+                    for (int e = 0; e < 4; ++e) {
+                        acc[2 * e] += wk * __uint_as_float(u[e] << 16);
+                        acc[2 * e + 1] += wk * __uint_as_float(u[e] & 0xffff0000u);
                     }
-                    m = ls[j];
                 }
-                const float wk = (ls[j] == -INFINITY) ? 0.f : expf(ls[j] - m);
-                wsum += wk;
+                if (++k == nparts) {  // row done: write it
+                    if (r < rows) {
+                        reinterpret_cast<uint4*>(p.out + (orow0 + r) * 512)[c8] =
+                            make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                       pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+                        if (c8 == 0 && p.lse) p.lse[orow0 + r] = sh_lse[cw];
+                    }
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    acc[q].x += wk * v[j][q].x;
-                    acc[q].y += wk * v[j][q].y;
-                    acc[q].z += wk * v[j][q].z;
-                    acc[q].w += wk * v[j][q].w;
+                    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+                    k = 0;
+                    ++j;
                 }
             }
         }
     }
-    const bool empty = bad || !(wsum > 0.f);
-    const float inv = empty ? 0.f : 1.f / wsum;
-    uint4* dst = reinterpret_cast<uint4*>(p.out + orow * 512 + q0 * 4);
-#pragma unroll
-    for (int q = 0; q < 4; q += 2)
-        dst[q / 2] = make_uint4(pack_bf16x2(acc[q].x * inv, acc[q].y * inv),
-                                pack_bf16x2(acc[q].z * inv, acc[q].w * inv),
-                                pack_bf16x2(acc[q + 1].x * inv, acc[q + 1].y * inv),
-                                pack_bf16x2(acc[q + 1].z * inv, acc[q + 1].w * inv));
-    if (slice == 0 && q0 == 0 && p.lse) p.lse[orow] = empty ? -INFINITY : m + logf(wsum);
 }
 
 // ------------------------------------------------------------------ host
@@ -1133,7 +1331,7 @@ cudaError_t setup_kernel(int dev, int* max_pairs) {
         cudaError_t e = cudaOccupancyMaxActiveClusters(&n, decode_pair_kernel<W>, &cfg);
         if (e != cudaSuccess) return e;
         if (n <= 0) return cudaErrorNotSupported;
-        di.max_pairs = n;
+        di.max_pairs = n < kCombineMaxParts ? n : kCombineMaxParts;
     }
     *max_pairs = di.max_pairs;
     return cudaSuccess;
@@ -1163,7 +1361,7 @@ cudaError_t tc_decode_workspace(int32_t batch, int32_t max_blocks, const mla_dim
     cudaError_t e;
     const int np = max_pairs_for(d, &e);
     if (e != cudaSuccess) return e;
-    const size_t o = (size_t)2 * np * 128 * 512 * sizeof(float);
+    const size_t o = (size_t)2 * np * 128 * 512 * sizeof(__nv_bfloat16);
     const size_t l = (size_t)2 * np * 128 * sizeof(float);
     *bytes = o + l;
     return cudaSuccess;
@@ -1175,6 +1373,10 @@ cudaError_t launch_decode_tc(void* out, float* lse, const void* q_abs, const voi
                              const mla_dims& d, float scale, void* workspace,
                              int32_t* dev_err, cudaStream_t s) {
     const int W = d.kv_rank + d.d_rope;
+    if ((long long)batch * max_blocks > (1LL << 33)) {  // unit counts are 32-bit
+        set_error("batch * max_blocks = %lld exceeds 2^33", (long long)batch * max_blocks);
+        return cudaErrorInvalidValue;
+    }
     cudaError_t e;
     const int np = max_pairs_for(d, &e);
     if (e != cudaSuccess) return e;
@@ -1225,23 +1427,6 @@ cudaError_t launch_decode_tc(void* out, float* lse, const void* q_abs, const voi
             return cudaErrorInvalidValue;
         }
     }
-    CUtensorMap omap;
-    {
-        // output rows as {512 columns, t_q * n_head rows, batch}: a 128-row box of
-        // one request never spills into the next request's rows
-        const int Mq = d.t_q * d.n_head;
-        cuuint64_t odims[3] = {512, (cuuint64_t)Mq, (cuuint64_t)batch};
-        cuuint64_t ostrides[2] = {512 * 2, (cuuint64_t)Mq * 512 * 2};
-        cuuint32_t obox[3] = {64, (cuuint32_t)(Mq < 128 ? Mq : 128), 1};
-        cuuint32_t oes[3] = {1, 1, 1};
-        cr = enc(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out, odims, ostrides, obox, oes,
-                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                 CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (cr != CUDA_SUCCESS) {
-            set_error("cuTensorMapEncodeTiled (output) failed (%d)", (int)cr);
-            return cudaErrorInvalidValue;
-        }
-    }
     Params p;
     p.q_abs = (const __nv_bfloat16*)q_abs;
     p.kv = (const __nv_bfloat16*)kv_cache;
@@ -1249,8 +1434,8 @@ cudaError_t launch_decode_tc(void* out, float* lse, const void* q_abs, const voi
     p.seq_lens = seq_lens;
     p.out = (__nv_bfloat16*)out;
     p.lse = lse;
-    p.ws_o = (float*)workspace;
-    p.ws_lse = (float*)((char*)workspace + (size_t)2 * np * 128 * 512 * sizeof(float));
+    p.ws_o = (__nv_bfloat16*)workspace;
+    p.ws_lse = (float*)((char*)workspace + (size_t)2 * np * 128 * 512 * sizeof(__nv_bfloat16));
     p.dev_err = dev_err;
     p.B = batch;
     p.T = d.t_q;
@@ -1260,6 +1445,7 @@ cudaError_t launch_decode_tc(void* out, float* lse, const void* q_abs, const voi
     p.num_blocks = num_blocks;
     p.NP = np;
     p.min_units = 2;
+    p.combine_rpt = 1;
     p.scale_log2 = scale * 1.4426950408889634f;
 
     // a programmatic dependent of the kernel before it: the cache pipeline
@@ -1279,16 +1465,27 @@ cudaError_t launch_decode_tc(void* out, float* lse, const void* q_abs, const voi
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     if (W == 576)
-        e = cudaLaunchKernelEx(&cfg, decode_pair_kernel<576>, tmap, qmap, vmap, omap, p);
+        e = cudaLaunchKernelEx(&cfg, decode_pair_kernel<576>, tmap, qmap, vmap, p);
     else
-        e = cudaLaunchKernelEx(&cfg, decode_pair_kernel<512>, tmap, qmap, vmap, omap, p);
+        e = cudaLaunchKernelEx(&cfg, decode_pair_kernel<512>, tmap, qmap, vmap, p);
     if (e != cudaSuccess) return e;
     const long long G = (d.t_q * d.n_head + 127) / 128;
     cudaLaunchConfig_t ccfg = {};
     cudaLaunchAttribute cattr[1];
     cattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     cattr[0].val.programmaticStreamSerializationAllowed = 1;
-    ccfg.gridDim = dim3((unsigned)((long long)batch * G * kCombineSlices), 1, 1);
+    // rows per combine thread: one while a single wave of CTAs (two per SM,
+    // four rows each) covers every row, more for larger batches
+    {
+        const int rows = d.t_q * d.n_head < 128 ? d.t_q * d.n_head : 128;
+        const long long wave = 2LL * 2 * np;  // two CTAs per SM, two SMs per pair
+        int rpt = 1;
+        while (rpt < kCombineMaxRpt &&
+               (long long)batch * G * ((rows + 4 * rpt - 1) / (4 * rpt)) > wave)
+            rpt *= 2;
+        p.combine_rpt = rpt;
+    }
+    ccfg.gridDim = dim3((unsigned)((long long)batch * G * (128 / (4 * p.combine_rpt))), 1, 1);
     ccfg.blockDim = dim3(kCombineThreads, 1, 1);
     ccfg.dynamicSmemBytes = 0;
     ccfg.stream = s;
