@@ -7,6 +7,8 @@
  *   mla_decode_paged    all heads attend MQA-style to the shared cache rows
  *                       [c_kv | k_pe], split over the keys, merged by LSE
  *   mla_decompress_out  decompress the latent output once through W_UV
+ *   mla_attend_absorbed the three above as one call (absorb, decode, merge
+ *                       and decompress), the form a decode step uses
  *   mla_cache_append    write new tokens' latent rows into the paged cache
  *   mla_rope_norm_to_neox_perm / mla_permute_rope_cols / mla_permute_rope_rows
  *                       the host-side load-time rope permutation
@@ -25,6 +27,11 @@
  *     the LSE is always f32. Accumulation is always f32.
  *   - Results are deterministic: the same inputs on the same device give the
  *     same bits (every reduction has a fixed order).
+ *   - Kernels launch as programmatic dependents of the kernel before them on
+ *     the stream: their set-up overlaps its end, but they read no input and
+ *     write nothing before it has completed. (Inside mla_attend_absorbed the
+ *     library's own later kernels read the inputs its earlier ones do not
+ *     write, the cache and the weights, early.)
  */
 #ifndef MLA_GB300_H
 #define MLA_GB300_H
@@ -177,6 +184,41 @@ mla_status mla_decode_paged_static(void* out, float* lse, const void* q_abs,
  */
 mla_status mla_decompress_out(void* out, const void* o_lat, const void* w_uv,
                               int32_t rows, const mla_dims* dims, void* stream);
+
+/*
+ * Bytes of scratch mla_attend_absorbed needs: the absorbed queries, the
+ * latent output and the decode's split scratch.
+ */
+mla_status mla_attend_workspace_size(int32_t batch, int32_t max_blocks,
+                                     const mla_dims* dims, size_t* bytes);
+
+/*
+ * The absorbed attention of one decode step ("memra_engine/mla.rs source",
+ * fn mla_attend_absorbed): absorb, paged decode, decompress, as
+ *   q_abs = mla_absorb_q(q_nope, q_pe, w_uk)          rows = batch * t_q
+ *   o_lat, lse = mla_decode_paged(q_abs, kv_cache, ...)
+ *   out = mla_decompress_out(o_lat, w_uv)
+ * with the same results (the same bits) as those three calls. On the bf16
+ * tensor-core path the decompress also merges the decode's split rows (the
+ * combine) while it streams W_UV, and the decode starts its cache stream
+ * while the absorb finishes.
+ * out         [B][t_q][H][Dv]  out, dims->dtype
+ * lse         [B][t_q][H] f32  out; may be NULL
+ * q_nope      [B][t_q][H][Dn], q_pe [B][t_q][H][P] (NULL when P == 0)
+ * w_uk        [H][Dn][R], w_uv [H][Dv][R]
+ * kv_cache, block_table, seq_lens, batch, max_blocks, num_blocks, scale,
+ * dev_err     as for mla_decode_paged
+ * workspace   >= mla_attend_workspace_size(batch, max_blocks, dims) bytes,
+ *             256-byte aligned, not shared with a concurrent call
+ */
+mla_status mla_attend_absorbed(void* out, float* lse, const void* q_nope,
+                               const void* q_pe, const void* w_uk, const void* w_uv,
+                               const void* kv_cache, const int32_t* block_table,
+                               const int32_t* seq_lens, int32_t batch,
+                               int32_t max_blocks, int32_t num_blocks,
+                               const mla_dims* dims, float scale, void* workspace,
+                               size_t workspace_bytes, int32_t* dev_err,
+                               void* stream);
 
 /*
  * Cache append ("vllm.v1.attention.backends.mla.cpu_mla",

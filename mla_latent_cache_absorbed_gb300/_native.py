@@ -27,6 +27,7 @@ DEVERR_TIMEOUT = 8
 # Every exported symbol of include/mla.h.
 EXPORTS = ("mla_absorb_q", "mla_decode_workspace_size", "mla_decode_paged",
            "mla_decode_paged_static", "mla_decompress_out", "mla_cache_append",
+           "mla_attend_workspace_size", "mla_attend_absorbed",
            "mla_rope_norm_to_neox_perm",
            "mla_permute_rope_cols", "mla_permute_rope_rows", "mla_status_str",
            "mla_last_error")
@@ -72,6 +73,9 @@ def load(path: str = LIB_PATH):
     lib.mla_decode_paged_static.argtypes = [P, P, P, P, P, P, I32, I32, I32, D, F, P, P]
     lib.mla_decompress_out.argtypes = [P, P, P, I32, D, P]
     lib.mla_cache_append.argtypes = [P, P, P, P, I32, I32, I32, D, P, P]
+    lib.mla_attend_workspace_size.argtypes = [I32, I32, D, ctypes.POINTER(ctypes.c_size_t)]
+    lib.mla_attend_absorbed.argtypes = [P, P, P, P, P, P, P, P, P, I32, I32, I32, D, F, P,
+                                        ctypes.c_size_t, P, P]
     lib.mla_rope_norm_to_neox_perm.argtypes = [I32, P]
     lib.mla_permute_rope_cols.argtypes = [P, I32, I64, I64, I32, I32]
     lib.mla_permute_rope_rows.argtypes = [P, I32, I64, I32, I32]
@@ -80,7 +84,8 @@ def load(path: str = LIB_PATH):
     lib.mla_last_error.argtypes = []
     lib.mla_last_error.restype = ctypes.c_char_p
     for name in ("mla_absorb_q", "mla_decode_workspace_size", "mla_decode_paged",
-                 "mla_decode_paged_static", "mla_decompress_out",
+                 "mla_decode_paged_static", "mla_decompress_out", "mla_cache_append",
+                 "mla_attend_workspace_size", "mla_attend_absorbed",
                  "mla_rope_norm_to_neox_perm", "mla_permute_rope_cols",
                  "mla_permute_rope_rows"):
         getattr(lib, name).restype = ctypes.c_int
@@ -161,6 +166,26 @@ def mla_cache_append(kv_cache, kv_c, k_pe, slot_mapping, n_tokens: int, num_bloc
            load().mla_cache_append(_ptr(kv_cache), _ptr(kv_c), _ptr(k_pe), _ptr(slot_mapping),
                                    n_tokens, num_blocks, src_dtype, ctypes.byref(dims),
                                    _ptr(dev_err), _stream(stream)))
+
+
+def mla_attend_workspace_size(batch: int, max_blocks: int, dims: MlaDims) -> int:
+    n = ctypes.c_size_t(0)
+    _check("mla_attend_workspace_size",
+           load().mla_attend_workspace_size(batch, max_blocks, ctypes.byref(dims),
+                                            ctypes.byref(n)))
+    return n.value
+
+
+def mla_attend_absorbed(out, lse, q_nope, q_pe, w_uk, w_uv, kv_cache, block_table, seq_lens,
+                        batch: int, max_blocks: int, num_blocks: int, dims: MlaDims,
+                        scale: float, workspace, workspace_bytes: int, dev_err=None,
+                        stream=None):
+    _check("mla_attend_absorbed",
+           load().mla_attend_absorbed(_ptr(out), _ptr(lse), _ptr(q_nope), _ptr(q_pe), _ptr(w_uk),
+                                      _ptr(w_uv), _ptr(kv_cache), _ptr(block_table),
+                                      _ptr(seq_lens), batch, max_blocks, num_blocks,
+                                      ctypes.byref(dims), float(scale), _ptr(workspace),
+                                      workspace_bytes, _ptr(dev_err), _stream(stream)))
 
 
 def mla_rope_norm_to_neox_perm(n_dims: int) -> np.ndarray:

@@ -110,7 +110,7 @@ mla_status mla_absorb_q(void* q_abs, const void* q_nope, const void* q_pe, const
             "device buffers must be 16-byte aligned");
     cudaStream_t s = (cudaStream_t)stream;
     if (dims->dtype == MLA_BF16 && tc_gemm_supported(*dims, rows, /*absorb=*/true)) {
-        MLA_CUDA_TRY(launch_absorb_tc(q_abs, q_nope, q_pe, w_uk, rows, *dims, s),
+        MLA_CUDA_TRY(launch_absorb_tc(q_abs, q_nope, q_pe, w_uk, rows, *dims, s, /*early=*/false),
                      "absorb (tensor cores)");
         return MLA_OK;
     }
@@ -155,7 +155,7 @@ mla_status mla_decompress_out(void* out, const void* o_lat, const void* w_uv, in
             "device buffers must be 16-byte aligned");
     cudaStream_t s = (cudaStream_t)stream;
     if (dims->dtype == MLA_BF16 && tc_gemm_supported(*dims, rows, /*absorb=*/false)) {
-        MLA_CUDA_TRY(launch_decompress_tc(out, o_lat, w_uv, rows, *dims, s),
+        MLA_CUDA_TRY(launch_decompress_tc(out, o_lat, w_uv, rows, *dims, s, /*early=*/false),
                      "decompress (tensor cores)");
         return MLA_OK;
     }
@@ -204,7 +204,7 @@ mla_status mla_decode_paged(void* out, float* lse, const void* q_abs, const void
     if (dims->dtype == MLA_BF16 && tc_decode_supported(*dims)) {
         MLA_CUDA_TRY(launch_decode_tc(out, lse, q_abs, kv_cache, block_table, seq_lens, batch,
                                       max_blocks, num_blocks, *dims, scale, workspace, dev_err,
-                                      s),
+                                      s, /*early=*/false, /*combine=*/true),
                      "decode (tensor cores)");
         return MLA_OK;
     }
@@ -213,6 +213,87 @@ mla_status mla_decode_paged(void* out, float* lse, const void* q_abs, const void
                                     s),
                  "decode");
     return MLA_OK;
+}
+
+namespace {
+size_t round256(size_t n) { return (n + 255) & ~(size_t)255; }
+}  // namespace
+
+mla_status mla_attend_workspace_size(int32_t batch, int32_t max_blocks, const mla_dims* dims,
+                                     size_t* bytes) {
+    g_last_error[0] = 0;
+    if (mla_status st = check_dims(dims)) return st;
+    REQUIRE(bytes, "bytes must be non-NULL");
+    REQUIRE(batch >= 0 && max_blocks >= 1, "batch >= 0 and max_blocks >= 1 required");
+    size_t dws = 0;
+    if (mla_status st = mla_decode_workspace_size(batch, max_blocks, dims, &dws)) return st;
+    const size_t esz = dims->dtype == MLA_F32 ? 4 : 2;
+    const size_t qrows = (size_t)batch * dims->t_q * dims->n_head;
+    *bytes = round256(qrows * (dims->kv_rank + dims->d_rope) * esz) +
+             round256(qrows * dims->kv_rank * esz) + dws;
+    return MLA_OK;
+}
+
+mla_status mla_attend_absorbed(void* out, float* lse, const void* q_nope, const void* q_pe,
+                               const void* w_uk, const void* w_uv, const void* kv_cache,
+                               const int32_t* block_table, const int32_t* seq_lens,
+                               int32_t batch, int32_t max_blocks, int32_t num_blocks,
+                               const mla_dims* dims, float scale, void* workspace,
+                               size_t workspace_bytes, int32_t* dev_err, void* stream) {
+    g_last_error[0] = 0;
+    if (mla_status st = check_dims(dims)) return st;
+    REQUIRE(batch >= 0 && max_blocks >= 1 && num_blocks >= 1,
+            "batch >= 0, max_blocks >= 1 and num_blocks >= 1 required");
+    if (batch == 0) return MLA_OK;
+    REQUIRE(out && q_nope && w_uk && w_uv && kv_cache && block_table && seq_lens && workspace,
+            "out, q_nope, w_uk, w_uv, kv_cache, block_table, seq_lens and workspace must be "
+            "non-NULL");
+    REQUIRE(q_pe || dims->d_rope == 0, "q_pe may be NULL only when d_rope == 0");
+    REQUIRE(aligned16(out) && aligned16(q_nope) && (!q_pe || aligned16(q_pe)) &&
+                aligned16(w_uk) && aligned16(w_uv) && aligned16(kv_cache) &&
+                aligned16(block_table) && aligned16(seq_lens) && (!lse || aligned16(lse)),
+            "device buffers must be 16-byte aligned");
+    REQUIRE(((uintptr_t)workspace & 255u) == 0, "workspace must be 256-byte aligned");
+    REQUIRE(scale == scale, "scale is NaN");
+    size_t need = 0;
+    if (mla_status st = mla_attend_workspace_size(batch, max_blocks, dims, &need)) return st;
+    REQUIRE(workspace_bytes >= need, "workspace too small: %zu bytes given, %zu needed",
+            workspace_bytes, need);
+    const size_t esz = dims->dtype == MLA_F32 ? 4 : 2;
+    const size_t qrows = (size_t)batch * dims->t_q * dims->n_head;
+    const int32_t rows = batch * dims->t_q;
+    char* ws = static_cast<char*>(workspace);
+    void* q_abs = ws;
+    void* o_lat = ws + round256(qrows * (dims->kv_rank + dims->d_rope) * esz);
+    void* dws = static_cast<char*>(o_lat) + round256(qrows * dims->kv_rank * esz);
+    const size_t dws_bytes = workspace_bytes - (size_t)(static_cast<char*>(dws) - ws);
+    cudaStream_t s = (cudaStream_t)stream;
+    DecodeSplitInfo info = {};
+    if (dims->dtype == MLA_BF16 && tc_decode_supported(*dims) &&
+        tc_gemm_supported(*dims, rows, /*absorb=*/true) &&
+        tc_decode_split_info(*dims, dws, &info) == cudaSuccess &&
+        tc_merge_supported(*dims, rows, info.NP)) {
+        // the library's own chain: the absorb waits for the caller's previous
+        // kernel before reading anything; the decode may read the cache before
+        // the absorb completes (the absorb writes only q_abs); the decompress
+        // merges the decode's split rows and streams its weights meanwhile
+        MLA_CUDA_TRY(launch_absorb_tc(q_abs, q_nope, q_pe, w_uk, rows, *dims, s, /*early=*/false),
+                     "attend: absorb (tensor cores)");
+        MLA_CUDA_TRY(launch_decode_tc(o_lat, lse, q_abs, kv_cache, block_table, seq_lens, batch,
+                                      max_blocks, num_blocks, *dims, scale, dws, dev_err, s,
+                                      /*early=*/true, /*combine=*/false),
+                     "attend: decode (tensor cores)");
+        MLA_CUDA_TRY(launch_decompress_merge_tc(out, lse, o_lat, w_uv, seq_lens, batch, max_blocks,
+                                                *dims, info, dev_err, s),
+                     "attend: merge + decompress (tensor cores)");
+        return MLA_OK;
+    }
+    if (mla_status st = mla_absorb_q(q_abs, q_nope, q_pe, w_uk, rows, dims, stream)) return st;
+    if (mla_status st = mla_decode_paged(o_lat, lse, q_abs, kv_cache, block_table, seq_lens,
+                                         batch, max_blocks, num_blocks, dims, scale, dws,
+                                         dws_bytes, dev_err, stream))
+        return st;
+    return mla_decompress_out(out, o_lat, w_uv, rows, dims, stream);
 }
 
 mla_status mla_rope_norm_to_neox_perm(int32_t n_dims, int32_t* perm_out) {

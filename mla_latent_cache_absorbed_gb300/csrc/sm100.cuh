@@ -112,6 +112,17 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// Bounded wait that suspends between polls (up to 1 us each): for a warp that
+// waits while others of its CTA compute. Returns false after `limit_ns`.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait_hint(bar, parity, 1000)) return true;
+        if ((i & 63) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // Bounded wait: polls until the phase with `parity` completes; gives up (and
 // returns false) once `limit_ns` nanoseconds have passed.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
@@ -130,6 +141,14 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // ----------------------------------------------------------------- TMA
+// L2 prefetch of one 3-D box (the coordinates a tma_load_3d would take); no
+// shared memory or barrier is involved. L2 is the coherence point, so a
+// prefetch issued before the producer of the data has finished cannot hand a
+// later load stale bytes.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* m, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];"
+                 ::"l"(m), "r"(c0), "r"(c1), "r"(c2) : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
 }

@@ -38,11 +38,20 @@
 #include "internal.h"
 #include "sm100.cuh"
 #include "tc_decode.h"
+#include "tc_split.cuh"
 
 namespace mla {
 namespace {
 
 using namespace sm100;
+using split::ntiles_of;
+using split::ChunkScan;
+using split::scan_chunk;
+using split::aligned_tried;
+using split::aligned_first_pair;
+using split::aligned_check;
+using split::aligned_decide;
+using split::pairs_per_set;
 
 constexpr int kTok = 64;                      // cache tokens per tile
 constexpr int kNS = 3;                        // pipeline stages
@@ -119,100 +128,22 @@ struct Params {
     int32_t* dev_err;
     int B, T, H, W, max_blocks, num_blocks;
     int NP, min_units;
-    int combine_rpt;              // combine: query rows per thread (1, 2 or 4)
+    int combine_rpt;              // combine: query rows per thread (1, 2, 4 or 8)
+    int early;                    // read cache, table and seq_lens before the previous
+                                  // kernel completes (it writes none of them)
     float scale_log2;
 };
 
 // ------------------------------------------------------------------ schedule
-__device__ __forceinline__ int ntiles_of(int S, int T, int max_blocks) {
-    if (S <= 0 || S < T || S > max_blocks * 16) return 0;
-    return (S + kTok - 1) / kTok;
-}
-
-// Work split. When a request has G > 1 row groups (t_q * n_head > 128), the
-// pairs form G sets of np / G: set g handles row group g of every request, and
-// pair k of each set covers the same (request, tile) range, so the G sets read
-// the same cache tiles at about the same time (one HBM read, the rest from
-// L2). Within a set the unit sequence is request b, then tile; pair k takes
-// units [U k / np_g, U (k + 1) / np_g), U = sum over requests of their tiles.
-// Every warp of both CTAs computes the same walk.
+// The work split is the one tc_split.cuh defines (even or request-aligned).
+// With G > 1 row groups the G sets read the same cache tiles at about the
+// same time: one HBM read, the rest from L2. One warp per CTA works out the
+// pair's walk; every warp of both CTAs then follows it.
+static_assert(kTok == split::kTok, "unit size");
 struct Walk {
     int b, g, tile, ntiles, S;
     long long u, u_end;
 };
-
-// pairs per set (np_g) and the set size cap, as both kernels derive them
-__device__ __forceinline__ int pairs_per_set(const Params& p, int G, long long U) {
-    int np_g = p.NP / G;
-    const long long cap = (U + p.min_units - 1) / p.min_units;
-    if (cap < np_g) np_g = (int)(cap > 0 ? cap : 1);
-    return np_g;
-}
-
-// One chunk of 32 requests, warp-cooperative: lane l holds request b0 + l's
-// units v (0 past the batch), its seq_len S, and the inclusive prefix of v
-// within the chunk; total is the chunk's sum. Unit counts fit 32 bits (the
-// host requires batch * max_blocks <= 2^33).
-struct ChunkScan {
-    int v, S, incl, total;
-};
-__device__ __forceinline__ ChunkScan scan_chunk(const Params& p, int b0, int lane) {
-    const int b = b0 + lane;
-    ChunkScan c;
-    c.S = b < p.B ? p.seq_lens[b] : 0;
-    c.v = b < p.B ? ntiles_of(c.S, p.T, p.max_blocks) : 0;
-    c.incl = c.v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, c.incl, o);
-        if (lane >= o) c.incl += t;
-    }
-    c.total = __shfl_sync(0xffffffffu, c.incl, 31);
-    return c;
-}
-
-// Request-aligned split. Request b (tiles_b units, prefix_b units before it)
-// gets the pairs [P_b, P_{b+1}) of its set, P_b = round(np_g prefix_b / U),
-// and its units evenly among them, so no pair holds two segments. Used when
-// every non-empty request gets a pair and no pair gets more than two tiles
-// above the even split's ceil(U / np_g): a pair holding two partial segments
-// costs more than that (an extra epilogue and a query reload). It is only
-// tried while a pair's share is small (then the straddling cost dominates)
-// and the arithmetic fits 32 bits.
-constexpr int kAlignedMaxShare = 32;  // tiles per pair
-__device__ __forceinline__ bool aligned_tried(long long U, int np_g) {
-    return U <= (long long)kAlignedMaxShare * np_g && 2 * (long long)np_g * U + U < (1LL << 31);
-}
-__device__ __forceinline__ int aligned_first_pair(long long prefix, long long U, int np_g) {
-    return (int)((2u * (uint32_t)np_g * (uint32_t)prefix + (uint32_t)U) / (2u * (uint32_t)U));
-}
-// Per chunk: lanes whose request gets no pair (bad) and the largest share.
-__device__ __forceinline__ void aligned_check(const ChunkScan& c, int base, long long U, int np_g,
-                                              int& bad, int& worst) {
-    const int n = aligned_first_pair(base + c.incl, U, np_g) -
-                  aligned_first_pair(base + c.incl - c.v, U, np_g);
-    if (c.v > 0) {
-        if (n <= 0) bad = 1;
-        else worst = max(worst, (int)(((uint32_t)c.v + (uint32_t)n - 1u) / (uint32_t)n));
-    }
-}
-__device__ __forceinline__ bool aligned_decide(int bad, int worst, long long U, int np_g) {
-    bad = __any_sync(0xffffffffu, bad);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) worst = max(worst, __shfl_xor_sync(0xffffffffu, worst, o));
-    return !bad && worst <= (U + np_g - 1) / np_g + 2;
-}
-// warp-cooperative; the same answer in every lane
-__device__ bool split_is_aligned(const Params& p, long long U, int np_g, int lane) {
-    if (!aligned_tried(U, np_g)) return false;
-    int base = 0, worst = 0, bad = 0;
-    for (int b0 = 0; b0 < p.B; b0 += 32) {
-        const ChunkScan c = scan_chunk(p, b0, lane);
-        aligned_check(c, base, U, np_g, bad, worst);
-        base += c.total;
-    }
-    return aligned_decide(bad, worst, U, np_g);
-}
 
 // This pair's set and unit range; warp-cooperative, at most two passes over
 // seq_lens (one load when the batch fits a chunk). Returns false when the
@@ -461,6 +392,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 2) {
         // the pair's unit range, worked out once per CTA while the barriers and
         // TMEM are set up; every warp starts its walk from it
+        if (!p.early) grid_dependency_wait();
         Walk w0;
         const bool ok = walk_init(p, pair, w0);
         if (lane == 0) {
@@ -480,6 +412,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cluster_sync();
     tc_fence_after();
     const uint32_t tbase = c.tmem_base;
+    // a call outside the library's own chain: the previous kernel may have
+    // written any input, so nothing is read before it completes
+    if (!p.early) grid_dependency_wait();
 
     Walk w;
     const bool has_work = c.walk_ok != 0;
@@ -1084,7 +1019,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // loads in flight at a time, so a request split into a few parts costs one
 // memory round trip for all the thread's rows. The parts' LSEs of all the
 // CTA's rows are loaded together while the first loads are in flight; one
-// warp per row then works out its weights.
+// thread per row then works out its weights.
 //
 // Launched as a programmatic dependent of the decode kernel: everything up to
 // the partials' first read overlaps the decode kernel's tail.
@@ -1122,42 +1057,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const Params p
     // which pairs hold this row group, from seq_lens alone (as the decode
     // kernel partitions the units); one warp works it out for the CTA
     if (warp == 0 && nt > 0) {
-        long long U = 0, before = 0;
-        for (int b0 = 0; b0 < p.B; b0 += 32) {
-            const int bb = b0 + lane;
-            long long v = bb < p.B ? (long long)ntiles_of(p.seq_lens[bb], p.T, p.max_blocks) : 0;
-            long long vb = bb < b ? v : 0;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                v += __shfl_xor_sync(0xffffffffu, v, o);
-                vb += __shfl_xor_sync(0xffffffffu, vb, o);
-            }
-            U += v;
-            before += vb;
-        }
-        const int np_g = pairs_per_set(p, G, U);
-        const bool aligned = split_is_aligned(p, U, np_g, lane);
-        if (lane == 0 && aligned) {
-            // the request's own pairs, each holding one segment of it
-            const long long pb = aligned_first_pair(before, U, np_g);
-            const long long pe = aligned_first_pair(before + nt, U, np_g);
-            sh_parts[0] = g * np_g + (int)pb;
-            sh_parts[1] = (int)(pe - pb);
-            sh_parts[2] = 0;
-        } else if (lane == 0) {
-            const long long u0 = before, u1 = u0 + nt;  // within row group g's set
-            auto owner = [&](long long u) {  // pair of the set whose range holds unit u
-                long long pp = (u * np_g) / U;
-                while (pp + 1 < np_g && U * (pp + 1) / np_g <= u) ++pp;
-                while (pp > 0 && U * pp / np_g > u) --pp;
-                return (int)pp;
-            };
-            const int kf = owner(u0), kl = owner(u1 - 1);
-            sh_parts[0] = g * np_g + kf;  // the pairs' global indices
-            sh_parts[1] = kl - kf + 1;
-            // part 0 is pair kf's first segment when its range starts at u0, else
-            // its last one; every later part is that pair's first segment
-            sh_parts[2] = (U * kf / np_g) >= u0 ? 0 : 1;
+        const split::Parts q = split::request_parts(p, b, g, lane);
+        if (lane == 0) {
+            sh_parts[0] = q.pf;
+            sh_parts[1] = q.nparts;
+            sh_parts[2] = q.slot0_off;
         }
     }
     // from here on the decode kernel's results (and the output rows it may
@@ -1204,34 +1108,30 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const Params p
         if (r < rows) sh_w[cw][k] = p.ws_lse[slot_of(k) * 128 + r];
     }
     __syncthreads();
-    // weights: warp w takes the CTA's rows w, w + 8, ...; NaN marks a part that
-    // met an invalid block id (the row is voided)
-    for (int cw = warp; cw < cr; cw += 8) {
+    // weights: thread t takes the CTA's row t, summing its parts in order (the
+    // merging decompress of the fused path does the same, bit for bit); NaN
+    // marks a part that met an invalid block id (the row is voided)
+    for (int cw = tid; cw < cr; cw += kCombineThreads) {
         const int r = row0 + cw;
         if (r >= rows) continue;
+        float* wr = sh_w[cw];
         float m = -INFINITY;
-        int bad = 0;
-        for (int k = lane; k < nparts; k += 32) {
-            const float l = sh_w[cw][k];
-            bad |= (l != l);
-            m = fmaxf(m, l);
+        bool bad = false;
+        for (int k = 0; k < nparts; ++k) {
+            bad |= (wr[k] != wr[k]);
+            m = fmaxf(m, wr[k]);
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        bad = __any_sync(0xffffffffu, bad);
         float sum = 0.f;
-        for (int k = lane; k < nparts; k += 32) {
-            const float l = sh_w[cw][k];
+        for (int k = 0; k < nparts; ++k) {
+            const float l = wr[k];
             const float e = (l == -INFINITY || m == -INFINITY) ? 0.f : expf(l - m);
-            sh_w[cw][k] = e;
+            wr[k] = e;
             sum += e;
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
         const bool empty = bad || !(sum > 0.f);
         const float inv = empty ? 0.f : 1.f / sum;
-        for (int k = lane; k < nparts; k += 32) sh_w[cw][k] *= inv;
-        if (lane == 0) sh_lse[cw] = empty ? -INFINITY : m + logf(sum);
+        for (int k = 0; k < nparts; ++k) wr[k] *= inv;
+        sh_lse[cw] = empty ? -INFINITY : m + logf(sum);
     }
     __syncthreads();
     float acc[8];
@@ -1354,6 +1254,17 @@ bool tc_decode_supported(const mla_dims& d) {
            d.block_size == 16 && d.t_q * d.n_head <= 1 << 20;
 }
 
+cudaError_t tc_decode_split_info(const mla_dims& d, void* workspace, DecodeSplitInfo* info) {
+    cudaError_t e;
+    const int np = max_pairs_for(d, &e);
+    if (e != cudaSuccess) return e;
+    info->NP = np;
+    info->min_units = 2;
+    info->ws_o = workspace;
+    info->ws_lse = (float*)((char*)workspace + (size_t)2 * np * 128 * 512 * sizeof(__nv_bfloat16));
+    return cudaSuccess;
+}
+
 cudaError_t tc_decode_workspace(int32_t batch, int32_t max_blocks, const mla_dims& d,
                                 size_t* bytes) {
     (void)batch;
@@ -1371,7 +1282,7 @@ cudaError_t launch_decode_tc(void* out, float* lse, const void* q_abs, const voi
                              const int32_t* block_table, const int32_t* seq_lens,
                              int32_t batch, int32_t max_blocks, int32_t num_blocks,
                              const mla_dims& d, float scale, void* workspace,
-                             int32_t* dev_err, cudaStream_t s) {
+                             int32_t* dev_err, cudaStream_t s, bool early, bool combine) {
     const int W = d.kv_rank + d.d_rope;
     if ((long long)batch * max_blocks > (1LL << 33)) {  // unit counts are 32-bit
         set_error("batch * max_blocks = %lld exceeds 2^33", (long long)batch * max_blocks);
@@ -1444,8 +1355,9 @@ cudaError_t launch_decode_tc(void* out, float* lse, const void* q_abs, const voi
     p.max_blocks = max_blocks;
     p.num_blocks = num_blocks;
     p.NP = np;
-    p.min_units = 2;
+    p.min_units = 2;  // as tc_decode_split_info reports
     p.combine_rpt = 1;
+    p.early = early ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
 
     // a programmatic dependent of the kernel before it: the cache pipeline
@@ -1469,6 +1381,7 @@ cudaError_t launch_decode_tc(void* out, float* lse, const void* q_abs, const voi
     else
         e = cudaLaunchKernelEx(&cfg, decode_pair_kernel<512>, tmap, qmap, vmap, p);
     if (e != cudaSuccess) return e;
+    if (!combine) return cudaGetLastError();
     const long long G = (d.t_q * d.n_head + 127) / 128;
     cudaLaunchConfig_t ccfg = {};
     cudaLaunchAttribute cattr[1];

@@ -25,6 +25,7 @@
 #include "internal.h"
 #include "sm100.cuh"
 #include "tc_decode.h"
+#include "tc_split.cuh"
 
 namespace mla {
 namespace {
@@ -44,6 +45,7 @@ struct GemmParams {
     int out_stride;              // elements between consecutive (r, h) rows: W or Dv
     int P;                       // absorb: rope width copied from q_pe
     int a_rows;                  // rows of the A box (the M tile's real rows, multiple of 8)
+    int early;                   // weights may be read before the previous kernel completes
     int32_t* dev_err;            // optional: timeout bit
 };
 
@@ -88,8 +90,21 @@ __global__ void __launch_bounds__(kGThreads, 1)
         if (elect_one()) {
             tma_prefetch_desc(&amap);
             tma_prefetch_desc(&bmap);
-            // weight chunks first (inputs of no earlier kernel), the first ring's
-            // worth before waiting for the previous kernel; A after the wait
+            // weight chunks first: in the library's own chain (early) the first
+            // ring's worth before waiting for the previous kernel, which does
+            // not write them; otherwise only L2 prefetches of them before the
+            // wait. A after the wait.
+            if (!p.early) {
+                for (int kc = 0; kc < nk; ++kc) {
+                    if (kBMnMajor) {
+                        for (int j = 0; j < p.n_tile / 64; ++j)
+                            tma_prefetch_l2_3d(&bmap, n0 + j * 64, kc * 64, h);
+                    } else {
+                        tma_prefetch_l2_3d(&bmap, kc * 64, n0, h);
+                    }
+                }
+                grid_dependency_wait();
+            }
             auto load_b = [&](int kc) {
                 const int s = kc % kGStages;
                 unsigned char* st = smem + s * stage_bytes;
@@ -257,6 +272,378 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const GemmParams&
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Decompress that merges the split decode's partial rows itself (the fused
+// path, mla_attend_absorbed). Same GEMM as the decompress above, but the A
+// operand (the latent output rows of head h, K = 512) is built in shared
+// memory by the CTA: a row held whole by one pair is copied from o_lat, a row
+// of a request split across pairs is merged from the pairs' partial rows with
+// the combine's LSE weights (out = sum_k exp(lse_k - lse) o_k), and a row of
+// an empty or invalid request is zero. No combine kernel runs in between, and
+// the merge overlaps the weight stream.
+//
+// Roles: warp 0 streams the weight chunks (3-stage ring), warp 1 issues the
+// MMAs once A is complete, warps 2..11 build A, warps 2..5 then run the
+// epilogue. Launched as a programmatic dependent of the decode kernel: the
+// split shape and the weight stream start before it completes; the partial
+// rows, o_lat and every write wait for it.
+constexpr int kMThreads = 384;
+constexpr int kMStages = 3;
+constexpr int kMergeWarps = 10;
+constexpr int kMergeLanes = kMergeWarps * 32 / 64;  // rows a merge step covers
+constexpr int kMChunks = 8;                 // K = 512 in 64-column chunks
+
+struct MergeParams {
+    // the decode's split (fields read by tc_split.cuh)
+    const int32_t* seq_lens;
+    int B, T, H, max_blocks, NP, min_units;
+    const __nv_bfloat16* ws_o;   // partial rows [2 NP][128][512]
+    const float* ws_lse;         // [2 NP][128] (NaN: the part met an invalid block id)
+    const __nv_bfloat16* o_lat;  // [rows][H][512], rows held whole by one pair
+    __nv_bfloat16* out;          // [rows][H][Dv]
+    float* lse;                  // [rows][H] or null
+    int32_t* dev_err;
+    int rows, Dv, n_tile;
+};
+
+__device__ __forceinline__ void named_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// One merge step of a thread: piece pc (16 bytes, K chunk pc / 8) of the G
+// rows r_g = r0 + step * g (g < G, r_g < mrows), whose parts are loaded KP at
+// a time (G * KP loads in flight). Per row, np: 0 empty (zeros), 1 copied from
+// o_lat (weight 1), more: the parts' partial rows with the weights in sh_w.
+template <int G, int KP>
+__device__ __forceinline__ void merge_rows(const MergeParams& p, int h, int m0, int mrows, int r0,
+                                           int step, int pc, int np_max, const int* sh_pf,
+                                           const int* sh_np, const int* sh_s0, const int* sh_rr,
+                                           const float* sh_w, unsigned char* a_smem) {
+    // per row: its piece in part k's slot is at base + 2 k * kSlot (k > 0) and
+    // base + s0 * kSlot (k = 0); a copied row reads o_lat at base
+    constexpr long long kSlot = 128 * 64;  // uint4 per slot
+    const uint4* base[G];
+    int np[G], s0[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const int r = r0 + step * g;
+        np[g] = r < mrows ? sh_np[r] : 0;
+        s0[g] = r < mrows ? sh_s0[r] : 0;
+        base[g] = np[g] == 1
+                      ? reinterpret_cast<const uint4*>(p.o_lat + ((long long)(m0 + r) * p.H + h) * 512) + pc
+                      : reinterpret_cast<const uint4*>(p.ws_o) +
+                            (r < mrows ? (2LL * sh_pf[r] * kSlot + sh_rr[r] * 64) : 0) + pc;
+    }
+    float acc[G][8];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
+    for (int k0 = 0; k0 < np_max; k0 += KP) {
+        uint4 v[G][KP];
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int kk = 0; kk < KP; ++kk) {
+                const int k = k0 + kk;
+                if (k < np[g])
+                    v[g][kk] = base[g][np[g] == 1 ? 0 : (k == 0 ? s0[g] : 2 * k) * kSlot];
+            }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const int r = r0 + step * g;
+#pragma unroll
+            for (int kk = 0; kk < KP; ++kk) {
+                const int k = k0 + kk;
+                if (k < np[g]) {
+                    const float wk = np[g] == 1 ? 1.f : sh_w[r * p.NP + k];
+                    const uint32_t x[4] = {v[g][kk].x, v[g][kk].y, v[g][kk].z, v[g][kk].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        acc[g][2 * e] += wk * __uint_as_float(x[e] << 16);
+                        acc[g][2 * e + 1] += wk * __uint_as_float(x[e] & 0xffff0000u);
+                    }
+                }
+            }
+        }
+    }
+    const int kc = pc >> 3, u = pc & 7;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const int r = r0 + step * g;
+        if (r < mrows)
+            st_shared_v4(smem_u32(a_smem + kc * 16384 + r * 128 + ((u ^ (r & 7)) << 4)),
+                         pack_bf16x2(acc[g][0], acc[g][1]), pack_bf16x2(acc[g][2], acc[g][3]),
+                         pack_bf16x2(acc[g][4], acc[g][5]), pack_bf16x2(acc[g][6], acc[g][7]));
+    }
+}
+
+__global__ void __launch_bounds__(kMThreads, 1)
+    tc_decompress_merge_kernel(const __grid_constant__ CUtensorMap bmap, const MergeParams p) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.x;
+    const int n0 = blockIdx.y * p.n_tile;
+    const int m0 = blockIdx.z * 128;
+    const int mrows = min(128, p.rows - m0);          // the tile's valid rows
+    const int bstage = p.n_tile * 128;                 // one weight chunk [n_tile][64 K]
+    unsigned char* a_smem = smem;                      // [8 chunks][128 rows][128 B]
+    unsigned char* b_smem = smem + kMChunks * 16384;
+    // per row of the tile: its parts (first pair, count, slot offset), its row
+    // within the group's partial slots, the LSE-load prefix, the merged LSE,
+    // and the parts' weights [128][NP]
+    uint64_t* full = reinterpret_cast<uint64_t*>(b_smem + kMStages * bstage);
+    int* sh_pf = reinterpret_cast<int*>(full + 2 * kMStages + 2 + 1);
+    int* sh_np = sh_pf + 128;     // parts per row: 0 empty, 1 copied from o_lat, >1 merged
+    int* sh_s0 = sh_np + 128;
+    int* sh_rr = sh_s0 + 128;
+    int* sh_off = sh_rr + 128;    // 130 entries: the LSE-load prefix, then the largest part count
+    float* sh_lse = reinterpret_cast<float*>(sh_off + 132);
+    float* sh_w = sh_lse + 128;
+    uint64_t* empty = full + kMStages;
+    uint64_t* aready = empty + kMStages;
+    uint64_t* done = aready + 1;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(done + 1);
+    grid_dependents_launch();
+    if ((smem_u32(smem) & 1023) != 0) return;
+    if (tid == 0) {
+        for (int s = 0; s < kMStages; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        mbar_init(smem_u32(aready), 1);
+        mbar_init(smem_u32(done), 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tslot), 128);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tslot;
+    bool ok = true;
+
+    if (warp == 0) {
+        // weight chunks [n_tile rows][64 K]: inputs of no kernel of the chain
+        if (elect_one()) {
+            tma_prefetch_desc(&bmap);
+            for (int kc = 0; kc < kMChunks; ++kc) {
+                const int s = kc % kMStages;
+                if (kc >= kMStages &&
+                    !mbar_wait_sleep(smem_u32(&empty[s]), ((kc / kMStages) & 1) ^ 1, kGWaitNs)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(smem_u32(&full[s]), (uint32_t)bstage);
+                tma_load_3d(smem_u32(b_smem + s * bstage), &bmap, smem_u32(&full[s]), kc * 64, n0, h);
+            }
+        }
+    } else if (warp == 1) {
+        if (elect_one()) {
+            const uint32_t idesc = idesc_bf16_f32(128, p.n_tile, 0, 0);
+            ok = mbar_wait_sleep(smem_u32(aready), 0, kGWaitNs);
+            for (int kc = 0; kc < kMChunks && ok; ++kc) {
+                const int s = kc % kMStages;
+                if (!mbar_wait_sleep(smem_u32(&full[s]), (kc / kMStages) & 1, kGWaitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a = smem_u32(a_smem + kc * 16384);
+                const uint32_t b = smem_u32(b_smem + s * bstage);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ss(tbase, sdesc_sw128(a + kk * 32, 16, 1024), sdesc_sw128(b + kk * 32, 16, 1024),
+                           idesc, (kc | kk) != 0);
+                mma_commit(smem_u32(&empty[s]));
+            }
+            mma_commit(smem_u32(done));
+        }
+    } else {
+        const int mt = tid - 64;  // the merge threads
+        constexpr int kMT = kMergeWarps * 32;
+        // 1. the split's shape, and each row's parts (before the decode ends:
+        //    seq_lens is an input of the chain, not a result)
+        if (warp == 2) {
+            const split::SplitShape sh = split::split_shape(p, lane);
+            // lane l of a chunk is request b = b0 + l; its rows in the tile are
+            // those with grow / T == b (t = grow - b T, query row t H + h)
+            int base = 0;
+            for (int b0 = 0; b0 < p.B; b0 += 32) {
+                const split::ChunkScan c = split::scan_chunk(p, b0, lane);
+                const long long b = b0 + lane;
+                const int r_lo = (int)max(0LL, b * p.T - m0);
+                const int r_hi = (int)min((long long)mrows, (b + 1) * p.T - m0);
+                if (b < p.B) {
+                    for (int r = r_lo; r < r_hi; ++r) {
+                        const int t = (int)(m0 + r - b * p.T);
+                        const int qi = t * p.H + h;
+                        sh_rr[r] = qi & 127;
+                        if (c.v == 0) {
+                            sh_np[r] = 0;
+                            // invalid requests: reported once (head 0, first N tile, t == 0)
+                            if (t == 0 && h == 0 && blockIdx.y == 0 && p.dev_err) {
+                                if (c.S < 0 || (c.S > 0 && c.S < p.T))
+                                    atomicOr(p.dev_err, (int32_t)MLA_DEVERR_SEQ_SHORT);
+                                else if (c.S > p.max_blocks * 16)
+                                    atomicOr(p.dev_err, (int32_t)MLA_DEVERR_SEQ_TOO_LONG);
+                            }
+                        } else {
+                            const split::Parts q = split::parts_from(base + c.incl - c.v, c.v, sh.U,
+                                                                     sh.np_g, sh.aligned, qi >> 7);
+                            sh_np[r] = q.nparts;
+                            sh_pf[r] = q.pf;
+                            sh_s0[r] = q.slot0_off;
+                        }
+                    }
+                }
+                base += c.total;
+            }
+            __syncwarp();
+            // prefix of the LSE loads (rows with more than one part)
+            if (lane == 0) {
+                int o = 0, npm = 0;
+                for (int r = 0; r < mrows; ++r) {
+                    sh_off[r] = o;
+                    o += sh_np[r] > 1 ? sh_np[r] : 0;
+                    npm = max(npm, sh_np[r]);
+                }
+                sh_off[mrows] = o;
+                sh_off[mrows + 1] = npm;  // the largest part count
+            }
+        }
+        named_sync(1, kMT);
+        // the rows this CTA will read (partial rows, copied o_lat rows) into L2
+        // while the decode finishes: L2 is the coherence point, so rows the
+        // decode writes after their prefetch still read back as written
+        {
+            const int nl0 = sh_off[mrows];
+            for (int i = mt; i < nl0; i += kMT) {
+                int r = 0;
+                while (sh_off[r + 1] <= i) ++r;
+                const int k = i - sh_off[r];
+                split::Parts q;
+                q.pf = sh_pf[r];
+                q.slot0_off = sh_s0[r];
+                prefetch_l2_bulk(p.ws_o + (split::part_slot(q, k) * 128 + sh_rr[r]) * 512, 1024);
+            }
+            for (int r = mt; r < mrows; r += kMT)
+                if (sh_np[r] == 1)
+                    prefetch_l2_bulk(p.o_lat + ((long long)(m0 + r) * p.H + h) * 512, 1024);
+        }
+        // 2. the decode's results are read from here on
+        grid_dependency_wait();
+        // 3. the parts' LSEs of the merged rows, all at once, then the weights
+        const int nl = sh_off[mrows];
+        for (int i = mt; i < nl; i += kMT) {
+            int r = 0;
+            while (sh_off[r + 1] <= i) ++r;
+            const int k = i - sh_off[r];
+            split::Parts q;
+            q.pf = sh_pf[r];
+            q.slot0_off = sh_s0[r];
+            sh_w[r * p.NP + k] = p.ws_lse[split::part_slot(q, k) * 128 + sh_rr[r]];
+        }
+        named_sync(1, kMT);
+        // weights: one thread per row (the parts' LSEs are in sh_w); NaN marks a
+        // part that met an invalid block id (the row is voided)
+        for (int r = mt; r < mrows; r += kMT) {
+            const int np = sh_np[r];
+            if (np <= 1) {
+                sh_lse[r] = np == 0 ? -INFINITY : 0.f;
+                continue;
+            }
+            float* wr = sh_w + r * p.NP;
+            float m = -INFINITY;
+            bool bad = false;
+            for (int k = 0; k < np; ++k) {
+                bad |= (wr[k] != wr[k]);
+                m = fmaxf(m, wr[k]);
+            }
+            float sum = 0.f;
+            for (int k = 0; k < np; ++k) {
+                const float l = wr[k];
+                const float e = (l == -INFINITY || m == -INFINITY) ? 0.f : expf(l - m);
+                wr[k] = e;
+                sum += e;
+            }
+            const bool empty_row = bad || !(sum > 0.f);
+            const float inv = empty_row ? 0.f : 1.f / sum;
+            for (int k = 0; k < np; ++k) wr[k] *= inv;
+            sh_lse[r] = empty_row ? -INFINITY : m + logf(sum);
+        }
+        named_sync(1, kMT);
+        // 4. A: thread mt takes the 16-byte piece pc = mt % 64 of rows
+        //    mt / 64 + kMergeLanes j, G rows at a time with their parts KP at
+        //    a time (G * KP = 16 loads in flight); the CTA picks (G, KP) from
+        //    its largest part count
+        {
+            const int pc = mt & 63, rl = mt >> 6;
+            const int npm = sh_off[mrows + 1];
+            const int nsteps = (mrows - rl + kMergeLanes - 1) / kMergeLanes;  // rows of this lane
+            if (npm <= 4) {
+                for (int j = 0; j < nsteps; j += 4)
+                    merge_rows<4, 4>(p, h, m0, mrows, rl + kMergeLanes * j, kMergeLanes, pc, npm,
+                                     sh_pf, sh_np, sh_s0, sh_rr, sh_w, a_smem);
+            } else if (npm <= 8) {
+                for (int j = 0; j < nsteps; j += 2)
+                    merge_rows<2, 8>(p, h, m0, mrows, rl + kMergeLanes * j, kMergeLanes, pc, npm,
+                                     sh_pf, sh_np, sh_s0, sh_rr, sh_w, a_smem);
+            } else {
+                for (int j = 0; j < nsteps; ++j)
+                    merge_rows<1, 16>(p, h, m0, mrows, rl + kMergeLanes * j, kMergeLanes, pc, npm,
+                                      sh_pf, sh_np, sh_s0, sh_rr, sh_w, a_smem);
+            }
+        }
+        // the merged rows' LSEs (the rows held whole have theirs from the decode)
+        if (p.lse && blockIdx.y == 0)
+            for (int r = mt; r < mrows; r += kMT)
+                if (sh_np[r] != 1) p.lse[(long long)(m0 + r) * p.H + h] = sh_lse[r];
+        fence_proxy_async_smem();  // A is read by the MMA (async proxy)
+        named_sync(1, kMT);
+        if (mt == 0) mbar_arrive(smem_u32(aready));
+        // 5. epilogue (warps 2..5): one output row per thread
+        if (warp < 6) {
+            const int q = warp & 3;
+            const int r = q * 32 + lane;
+            const int row = m0 + r;
+            const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+            ok = __all_sync(0xffffffffu, mbar_wait_sleep(smem_u32(done), 0, kGWaitNs));
+            tc_fence_after();
+            if (ok) {
+                __nv_bfloat16* dst = p.out + ((long long)row * p.H + h) * p.Dv + n0;
+                for (int cc = 0; cc < p.n_tile; cc += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(tbase + lane_off + cc, v);
+                    tmem_wait_ld();
+                    if (row < p.rows) {
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            d4[j] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * j]), __uint_as_float(v[8 * j + 1])),
+                                               pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+                                               pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+                                               pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+                    }
+                }
+            }
+        }
+    }
+    if (!ok && tid % 32 == 0 && p.dev_err) atomicOr(p.dev_err, (int32_t)MLA_DEVERR_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tbase, 128);
+}
+
+size_t merge_smem_bytes(int n_tile, int np) {
+    return (size_t)kMChunks * 16384 + (size_t)kMStages * n_tile * 128 +
+           (size_t)(2 * kMStages + 3) * 8 + (size_t)(4 * 128 + 132) * 4 + 128 * 4 +
+           (size_t)128 * np * 4;
+}
+
 }  // namespace
 
 bool tc_gemm_supported(const mla_dims& d, int32_t rows, bool absorb) {
@@ -268,7 +655,7 @@ bool tc_gemm_supported(const mla_dims& d, int32_t rows, bool absorb) {
 
 cudaError_t launch_absorb_tc(void* q_abs, const void* q_nope, const void* q_pe,
                              const void* w_uk, int32_t rows, const mla_dims& d,
-                             cudaStream_t s) {
+                             cudaStream_t s, bool early) {
     const int H = d.n_head, Dn = d.d_nope, R = d.kv_rank, P = d.d_rope;
     CUtensorMap a, b;
     // A: q_nope viewed as {Dn, H, rows}; box {64, 1, a_rows}
@@ -290,12 +677,13 @@ cudaError_t launch_absorb_tc(void* q_abs, const void* q_nope, const void* q_pe,
     p.out_stride = R + P;
     p.P = P;
     p.a_rows = a_rows;
+    p.early = early ? 1 : 0;
     p.dev_err = nullptr;
     return launch<true>(a, b, p, s);
 }
 
 cudaError_t launch_decompress_tc(void* out, const void* o_lat, const void* w_uv, int32_t rows,
-                                 const mla_dims& d, cudaStream_t s) {
+                                 const mla_dims& d, cudaStream_t s, bool early) {
     const int H = d.n_head, R = d.kv_rank, Dv = d.d_v;
     const int n_tile = Dv == 128 ? 128 : (Dv >= 256 && Dv % 256 == 0 ? 128 : 128);
     CUtensorMap a, b;
@@ -319,8 +707,67 @@ cudaError_t launch_decompress_tc(void* out, const void* o_lat, const void* w_uv,
     p.out_stride = Dv;
     p.P = 0;
     p.a_rows = a_rows;
+    p.early = early ? 1 : 0;
     p.dev_err = nullptr;
     return launch<false>(a, b, p, s);
+}
+
+bool tc_merge_supported(const mla_dims& d, int32_t rows, int np) {
+    return tc_gemm_supported(d, rows, /*absorb=*/false) && d.kv_rank == 512 && d.d_v % 128 == 0 &&
+           np > 0 && merge_smem_bytes(128, np) <= 232448;
+}
+
+cudaError_t launch_decompress_merge_tc(void* out, float* lse, const void* o_lat,
+                                       const void* w_uv, const int32_t* seq_lens,
+                                       int32_t batch, int32_t max_blocks, const mla_dims& d,
+                                       const DecodeSplitInfo& info, int32_t* dev_err,
+                                       cudaStream_t s) {
+    const int H = d.n_head, R = d.kv_rank, Dv = d.d_v;
+    const int rows = batch * d.t_q;
+    const int n_tile = 128;
+    CUtensorMap b;
+    // B: w_uv viewed as {R, Dv, H} (K contiguous); box {64 K, n_tile N, 1}
+    cudaError_t e = make_map(&b, w_uv, R, Dv, H, (cuuint64_t)R * 2, (cuuint64_t)Dv * R * 2, 64,
+                             (cuuint32_t)n_tile, 1);
+    if (e != cudaSuccess) return e;
+    MergeParams p;
+    p.seq_lens = seq_lens;
+    p.B = batch;
+    p.T = d.t_q;
+    p.H = H;
+    p.max_blocks = max_blocks;
+    p.NP = info.NP;
+    p.min_units = info.min_units;
+    p.ws_o = (const __nv_bfloat16*)info.ws_o;
+    p.ws_lse = info.ws_lse;
+    p.o_lat = (const __nv_bfloat16*)o_lat;
+    p.out = (__nv_bfloat16*)out;
+    p.lse = lse;
+    p.dev_err = dev_err;
+    p.rows = rows;
+    p.Dv = Dv;
+    p.n_tile = n_tile;
+    const size_t smem = merge_smem_bytes(n_tile, info.NP) + 1024;  // + alignment slack
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(tc_decompress_merge_kernel,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(H, Dv / n_tile, (rows + 127) / 128);
+    cfg.blockDim = dim3(kMThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, tc_decompress_merge_kernel, b, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
 }
 
 }  // namespace mla

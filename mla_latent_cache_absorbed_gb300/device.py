@@ -110,7 +110,28 @@ def decompress(dc: DeviceCase, stream=None, o_lat=None, out=None):
 
 
 def full_step(dc: DeviceCase, stream=None):
-    """One pass of the hot path: absorb -> paged decode -> decompress."""
+    """One pass of the hot path: absorb -> paged decode -> decompress, as three
+    calls (o_lat and q_abs land in the case's buffers)."""
     absorb(dc, stream)
     decode(dc, stream)
     decompress(dc, stream)
+
+
+def attend_workspace(dc: DeviceCase):
+    """The fused call's scratch (allocated once per case)."""
+    ws = getattr(dc, "_attend_ws", None)
+    if ws is None:
+        torch = _torch()
+        n = N.mla_attend_workspace_size(dc.batch, dc.max_blocks, dc.dims)
+        ws = (torch.empty(max(n, 256), dtype=torch.uint8, device=dc.out.device), n)
+        dc._attend_ws = ws
+    return ws
+
+
+def attend(dc: DeviceCase, stream=None, out=None, lse=None):
+    """One pass of the hot path as one call (mla_attend_absorbed)."""
+    ws, n = attend_workspace(dc)
+    N.mla_attend_absorbed(dc.out if out is None else out, dc.lse if lse is None else lse,
+                          dc.q_nope, dc.q_pe, dc.w_uk, dc.w_uv, dc.kv_cache, dc.block_table,
+                          dc.seq_lens, dc.batch, dc.max_blocks, dc.num_blocks, dc.dims,
+                          dc.scale, ws, n, dc.dev_err, stream)
