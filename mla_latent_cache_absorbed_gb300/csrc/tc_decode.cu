@@ -1018,8 +1018,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // partial row. Its (row, part) items are walked row by row, kCombineBatch
 // loads in flight at a time, so a request split into a few parts costs one
 // memory round trip for all the thread's rows. The parts' LSEs of all the
-// CTA's rows are loaded together while the first loads are in flight; one
-// thread per row then works out its weights.
+// CTA's rows are loaded together while the first loads are in flight; eight
+// lanes per row then work out its weights.
 //
 // Launched as a programmatic dependent of the decode kernel: everything up to
 // the partials' first read overlaps the decode kernel's tail.
@@ -1032,7 +1032,7 @@ __device__ __forceinline__ uint4 load_part(const Params& p, long long slot, int 
     return reinterpret_cast<const uint4*>(p.ws_o + (slot * 128 + r) * 512)[c8];
 }
 
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const Params p) {
+__global__ void __launch_bounds__(kCombineThreads, 2) combine_kernel(const Params p) {
     __shared__ int sh_parts[3];  // first pair, part count, first part's slot offset
     __shared__ float sh_w[4 * kCombineMaxRpt][kCombineMaxParts];
     __shared__ float sh_lse[4 * kCombineMaxRpt];
@@ -1108,30 +1108,15 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const Params p
         if (r < rows) sh_w[cw][k] = p.ws_lse[slot_of(k) * 128 + r];
     }
     __syncthreads();
-    // weights: thread t takes the CTA's row t, summing its parts in order (the
-    // merging decompress of the fused path does the same, bit for bit); NaN
-    // marks a part that met an invalid block id (the row is voided)
-    for (int cw = tid; cw < cr; cw += kCombineThreads) {
-        const int r = row0 + cw;
-        if (r >= rows) continue;
-        float* wr = sh_w[cw];
-        float m = -INFINITY;
-        bool bad = false;
-        for (int k = 0; k < nparts; ++k) {
-            bad |= (wr[k] != wr[k]);
-            m = fmaxf(m, wr[k]);
-        }
-        float sum = 0.f;
-        for (int k = 0; k < nparts; ++k) {
-            const float l = wr[k];
-            const float e = (l == -INFINITY || m == -INFINITY) ? 0.f : expf(l - m);
-            wr[k] = e;
-            sum += e;
-        }
-        const bool empty = bad || !(sum > 0.f);
-        const float inv = empty ? 0.f : 1.f / sum;
-        for (int k = 0; k < nparts; ++k) wr[k] *= inv;
-        sh_lse[cw] = empty ? -INFINITY : m + logf(sum);
+    // weights: 8 lanes per row (split::row_weights; the merging decompress of
+    // the fused path computes them the same way, bit for bit)
+    {
+        // a group of 8 lanes per row (rows of a CTA <= 32 = its groups)
+        const int grp = tid / split::kWeightLanes, gl = tid % split::kWeightLanes;
+        const int r = row0 + grp;
+        const bool mine = grp < cr && r < rows;
+        const float l = split::row_weights(sh_w[mine ? grp : 0], mine ? nparts : 0, gl);
+        if (mine && gl == 0) sh_lse[grp] = l;
     }
     __syncthreads();
     float acc[8];

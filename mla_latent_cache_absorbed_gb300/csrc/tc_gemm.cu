@@ -549,30 +549,17 @@ __global__ void __launch_bounds__(kMThreads, 1)
         named_sync(1, kMT);
         // weights: one thread per row (the parts' LSEs are in sh_w); NaN marks a
         // part that met an invalid block id (the row is voided)
-        for (int r = mt; r < mrows; r += kMT) {
-            const int np = sh_np[r];
-            if (np <= 1) {
-                sh_lse[r] = np == 0 ? -INFINITY : 0.f;
-                continue;
+        {
+            // 8 lanes per row (split::row_weights, as the combine), in
+            // warp-uniform rounds of kMT / 8 rows
+            constexpr int kGroups = kMT / split::kWeightLanes;
+            const int grp = mt / split::kWeightLanes, gl = mt % split::kWeightLanes;
+            for (int r0 = 0; r0 < mrows; r0 += kGroups) {
+                const int r = r0 + grp;
+                const int np = r < mrows ? sh_np[r] : 0;
+                const float l = split::row_weights(sh_w + (r < mrows ? r : 0) * p.NP, np > 1 ? np : 0, gl);
+                if (r < mrows && gl == 0) sh_lse[r] = np > 1 ? l : (np == 0 ? -INFINITY : 0.f);
             }
-            float* wr = sh_w + r * p.NP;
-            float m = -INFINITY;
-            bool bad = false;
-            for (int k = 0; k < np; ++k) {
-                bad |= (wr[k] != wr[k]);
-                m = fmaxf(m, wr[k]);
-            }
-            float sum = 0.f;
-            for (int k = 0; k < np; ++k) {
-                const float l = wr[k];
-                const float e = (l == -INFINITY || m == -INFINITY) ? 0.f : expf(l - m);
-                wr[k] = e;
-                sum += e;
-            }
-            const bool empty_row = bad || !(sum > 0.f);
-            const float inv = empty_row ? 0.f : 1.f / sum;
-            for (int k = 0; k < np; ++k) wr[k] *= inv;
-            sh_lse[r] = empty_row ? -INFINITY : m + logf(sum);
         }
         named_sync(1, kMT);
         // 4. A: thread mt takes the 16-byte piece pc = mt % 64 of rows

@@ -26,6 +26,7 @@
 // small problem gets).
 #pragma once
 
+#include <math.h>
 #include <stdint.h>
 
 namespace mla {
@@ -186,6 +187,45 @@ __device__ Parts request_parts(const P& p, int b, int g, int lane) {
     if (q.nt == 0) return q;
     const SplitShape sh = split_shape(p, lane);
     return parts_from(before, q.nt, sh.U, sh.np_g, sh.aligned, g);
+}
+
+// The merge weights of one row, by a group of 8 adjacent lanes: w holds the
+// parts' LSEs (natural log; NaN marks a part that met an invalid block id)
+// and gets w_k = exp(lse_k - max) / sum; the row's LSE is returned in every
+// lane of the group (-inf for an empty or voided row, whose weights are 0).
+// Lane j of the group takes parts j, j + 8, ... and sums them in that order;
+// the group then adds its lanes' sums by an xor butterfly (4, 2, 1). The
+// combine and the merging decompress both call this with the same grouping,
+// so they agree bit for bit. Every lane of the warp must call it (the
+// shuffles span the warp); a group with nothing to do passes np = 0.
+constexpr int kWeightLanes = 8;
+__device__ __forceinline__ float row_weights(float* w, int np, int gl) {
+    float m = -INFINITY;
+    int bad = 0;
+    for (int k = gl; k < np; k += kWeightLanes) {
+        const float l = w[k];
+        bad |= (l != l);
+        m = fmaxf(m, l);
+    }
+#pragma unroll
+    for (int o = kWeightLanes / 2; o > 0; o >>= 1) {
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o, kWeightLanes));
+        bad |= __shfl_xor_sync(0xffffffffu, bad, o, kWeightLanes);
+    }
+    float sum = 0.f;
+    for (int k = gl; k < np; k += kWeightLanes) {
+        const float l = w[k];
+        const float e = (l == -INFINITY || m == -INFINITY) ? 0.f : expf(l - m);
+        w[k] = e;
+        sum += e;
+    }
+#pragma unroll
+    for (int o = kWeightLanes / 2; o > 0; o >>= 1)
+        sum += __shfl_xor_sync(0xffffffffu, sum, o, kWeightLanes);
+    const bool empty = bad || !(sum > 0.f);
+    const float inv = empty ? 0.f : 1.f / sum;
+    for (int k = gl; k < np; k += kWeightLanes) w[k] *= inv;
+    return empty ? -INFINITY : m + logf(sum);
 }
 
 }  // namespace split
