@@ -282,6 +282,11 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const GemmParams&
 // an empty or invalid request is zero. No combine kernel runs in between, and
 // the merge overlaps the weight stream.
 //
+// The CTAs of one head (its d_v / n_tile column tiles, 1 to 4) form a
+// cluster and share the merge: each merges every csize-th row and writes it into all of
+// their A operands (its own by st.shared, the others' by st.async, counted
+// on their A barriers).
+//
 // Roles: warp 0 streams the weight chunks (3-stage ring), warp 1 issues the
 // MMAs once A is complete, warps 2..11 build A, warps 2..5 then run the
 // epilogue. Launched as a programmatic dependent of the decode kernel: the
@@ -318,7 +323,8 @@ template <int G, int KP>
 __device__ __forceinline__ void merge_rows(const MergeParams& p, int h, int m0, int mrows, int r0,
                                            int step, int pc, int np_max, const int* sh_pf,
                                            const int* sh_np, const int* sh_s0, const int* sh_rr,
-                                           const float* sh_w, unsigned char* a_smem) {
+                                           const float* sh_w, unsigned char* a_smem, int csize,
+                                           uint32_t rank, uint32_t aready) {
     // per row: its piece in part k's slot is at base + 2 k * kSlot (k > 0) and
     // base + s0 * kSlot (k = 0); a copied row reads o_lat at base
     constexpr long long kSlot = 128 * 64;  // uint4 per slot
@@ -371,10 +377,17 @@ __device__ __forceinline__ void merge_rows(const MergeParams& p, int h, int m0, 
 #pragma unroll
     for (int g = 0; g < G; ++g) {
         const int r = r0 + step * g;
-        if (r < mrows)
-            st_shared_v4(smem_u32(a_smem + kc * 16384 + r * 128 + ((u ^ (r & 7)) << 4)),
-                         pack_bf16x2(acc[g][0], acc[g][1]), pack_bf16x2(acc[g][2], acc[g][3]),
-                         pack_bf16x2(acc[g][4], acc[g][5]), pack_bf16x2(acc[g][6], acc[g][7]));
+        if (r < mrows) {
+            const uint32_t x0 = pack_bf16x2(acc[g][0], acc[g][1]), x1 = pack_bf16x2(acc[g][2], acc[g][3]);
+            const uint32_t x2 = pack_bf16x2(acc[g][4], acc[g][5]), x3 = pack_bf16x2(acc[g][6], acc[g][7]);
+            const uint32_t at = smem_u32(a_smem + kc * 16384 + r * 128 + ((u ^ (r & 7)) << 4));
+            st_shared_v4(at, x0, x1, x2, x3);
+            // the same A row in the other CTAs of the cluster
+            for (int c = 1; c < csize; ++c) {
+                const uint32_t dst = (rank + c) % csize;
+                st_async_v4(mapa(at, dst), x0, x1, x2, x3, mapa(aready, dst));
+            }
+        }
     }
 }
 
@@ -397,8 +410,8 @@ __global__ void __launch_bounds__(kMThreads, 1)
     int* sh_np = sh_pf + 128;     // parts per row: 0 empty, 1 copied from o_lat, >1 merged
     int* sh_s0 = sh_np + 128;
     int* sh_rr = sh_s0 + 128;
-    int* sh_off = sh_rr + 128;    // 130 entries: the LSE-load prefix, then the largest part count
-    float* sh_lse = reinterpret_cast<float*>(sh_off + 132);
+    int* sh_off = sh_rr + 128;    // 131 entries: the LSE-load prefix, the largest part count, the others' rows
+    float* sh_lse = reinterpret_cast<float*>(sh_off + 132);  // 131 used
     float* sh_w = sh_lse + 128;
     uint64_t* empty = full + kMStages;
     uint64_t* aready = empty + kMStages;
@@ -419,8 +432,12 @@ __global__ void __launch_bounds__(kMThreads, 1)
         tmem_alloc(smem_u32(tslot), 128);
         tmem_relinquish();
     }
+    // the cluster's CTAs share one head: each merges every csize-th row and
+    // writes it into every CTA's A (barriers initialised cluster-wide first)
+    const int csize = (int)(gridDim.y);
+    const uint32_t rank = cluster_ctarank();
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();
     tc_fence_after();
     const uint32_t tbase = *tslot;
     bool ok = true;
@@ -504,14 +521,22 @@ __global__ void __launch_bounds__(kMThreads, 1)
             __syncwarp();
             // prefix of the LSE loads (rows with more than one part)
             if (lane == 0) {
-                int o = 0, npm = 0;
+                // over this CTA's own rows (r % csize == rank): the LSE-load
+                // prefix and the largest part count; and the rows the other
+                // CTAs write into this one's A
+                int o = 0, npm = 0, others = 0;
                 for (int r = 0; r < mrows; ++r) {
                     sh_off[r] = o;
-                    o += sh_np[r] > 1 ? sh_np[r] : 0;
-                    npm = max(npm, sh_np[r]);
+                    if (r % csize == (int)rank) {
+                        o += sh_np[r] > 1 ? sh_np[r] : 0;
+                        npm = max(npm, sh_np[r]);
+                    } else {
+                        ++others;
+                    }
                 }
                 sh_off[mrows] = o;
-                sh_off[mrows + 1] = npm;  // the largest part count
+                sh_off[mrows + 1] = npm;
+                sh_off[mrows + 2] = others;
             }
         }
         named_sync(1, kMT);
@@ -530,7 +555,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
                 prefetch_l2_bulk(p.ws_o + (split::part_slot(q, k) * 128 + sh_rr[r]) * 512, 1024);
             }
             for (int r = mt; r < mrows; r += kMT)
-                if (sh_np[r] == 1)
+                if (sh_np[r] == 1 && r % csize == (int)rank)
                     prefetch_l2_bulk(p.o_lat + ((long long)(m0 + r) * p.H + h) * 512, 1024);
         }
         // 2. the decode's results are read from here on
@@ -554,8 +579,8 @@ __global__ void __launch_bounds__(kMThreads, 1)
             // warp-uniform rounds of kMT / 8 rows
             constexpr int kGroups = kMT / split::kWeightLanes;
             const int grp = mt / split::kWeightLanes, gl = mt % split::kWeightLanes;
-            for (int r0 = 0; r0 < mrows; r0 += kGroups) {
-                const int r = r0 + grp;
+            for (int i0 = 0; i0 * csize < mrows; i0 += kGroups) {
+                const int r = (int)rank + csize * (i0 + grp);  // this CTA's rows
                 const int np = r < mrows ? sh_np[r] : 0;
                 const float l = split::row_weights(sh_w + (r < mrows ? r : 0) * p.NP, np > 1 ? np : 0, gl);
                 if (r < mrows && gl == 0) sh_lse[r] = np > 1 ? l : (np == 0 ? -INFINITY : 0.f);
@@ -567,30 +592,36 @@ __global__ void __launch_bounds__(kMThreads, 1)
         //    a time (G * KP = 16 loads in flight); the CTA picks (G, KP) from
         //    its largest part count
         {
+            // this CTA's rows rank + csize (rl + kMergeLanes j)
             const int pc = mt & 63, rl = mt >> 6;
             const int npm = sh_off[mrows + 1];
-            const int nsteps = (mrows - rl + kMergeLanes - 1) / kMergeLanes;  // rows of this lane
+            const int r0 = (int)rank + csize * rl, step = csize * kMergeLanes;
+            const int nsteps = r0 < mrows ? (mrows - r0 + step - 1) / step : 0;
+            const uint32_t ab = smem_u32(aready);
             if (npm <= 4) {
                 for (int j = 0; j < nsteps; j += 4)
-                    merge_rows<4, 4>(p, h, m0, mrows, rl + kMergeLanes * j, kMergeLanes, pc, npm,
-                                     sh_pf, sh_np, sh_s0, sh_rr, sh_w, a_smem);
+                    merge_rows<4, 4>(p, h, m0, mrows, r0 + step * j, step, pc, npm, sh_pf, sh_np,
+                                     sh_s0, sh_rr, sh_w, a_smem, csize, rank, ab);
             } else if (npm <= 8) {
                 for (int j = 0; j < nsteps; j += 2)
-                    merge_rows<2, 8>(p, h, m0, mrows, rl + kMergeLanes * j, kMergeLanes, pc, npm,
-                                     sh_pf, sh_np, sh_s0, sh_rr, sh_w, a_smem);
+                    merge_rows<2, 8>(p, h, m0, mrows, r0 + step * j, step, pc, npm, sh_pf, sh_np,
+                                     sh_s0, sh_rr, sh_w, a_smem, csize, rank, ab);
             } else {
                 for (int j = 0; j < nsteps; ++j)
-                    merge_rows<1, 16>(p, h, m0, mrows, rl + kMergeLanes * j, kMergeLanes, pc, npm,
-                                      sh_pf, sh_np, sh_s0, sh_rr, sh_w, a_smem);
+                    merge_rows<1, 16>(p, h, m0, mrows, r0 + step * j, step, pc, npm, sh_pf, sh_np,
+                                      sh_s0, sh_rr, sh_w, a_smem, csize, rank, ab);
             }
         }
         // the merged rows' LSEs (the rows held whole have theirs from the decode)
-        if (p.lse && blockIdx.y == 0)
+        if (p.lse)
             for (int r = mt; r < mrows; r += kMT)
-                if (sh_np[r] != 1) p.lse[(long long)(m0 + r) * p.H + h] = sh_lse[r];
+                if (sh_np[r] != 1 && r % csize == (int)rank)
+                    p.lse[(long long)(m0 + r) * p.H + h] = sh_lse[r];
         fence_proxy_async_smem();  // A is read by the MMA (async proxy)
         named_sync(1, kMT);
-        if (mt == 0) mbar_arrive(smem_u32(aready));
+        // A is complete once this CTA's rows are written (the arrival below)
+        // and the other CTAs' rows have landed (their st.async bytes)
+        if (mt == 0) mbar_arrive_expect_tx(smem_u32(aready), (uint32_t)sh_off[mrows + 2] * 1024u);
         // 5. epilogue (warps 2..5): one output row per thread
         if (warp < 6) {
             const int q = warp & 3;
@@ -620,7 +651,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
     }
     if (!ok && tid % 32 == 0 && p.dev_err) atomicOr(p.dev_err, (int32_t)MLA_DEVERR_TIMEOUT);
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();  // no CTA leaves while another may still write its A
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tbase, 128);
 }
@@ -699,9 +730,23 @@ cudaError_t launch_decompress_tc(void* out, const void* o_lat, const void* w_uv,
     return launch<false>(a, b, p, s);
 }
 
+// Output columns per CTA of the merging decompress. The CTAs of one head
+// (d_v / n_tile of them) form a cluster that shares the merge. A d_v of 128
+// is split in two 64-column tiles only while the grid stays one wave (one
+// CTA per SM): a second wave costs more than the shared merge saves.
+int merge_n_tile(const mla_dims& d, int32_t rows) {
+    if (d.d_v != 128) return 128;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 128;
+    const long long ctas = 2LL * d.n_head * ((rows + 127) / 128);
+    return ctas <= sms ? 64 : 128;
+}
+
 bool tc_merge_supported(const mla_dims& d, int32_t rows, int np) {
     return tc_gemm_supported(d, rows, /*absorb=*/false) && d.kv_rank == 512 && d.d_v % 128 == 0 &&
-           np > 0 && merge_smem_bytes(128, np) <= 232448;
+           d.d_v <= 512 && np > 0 && merge_smem_bytes(128, np) + 1024 <= 232448;
 }
 
 cudaError_t launch_decompress_merge_tc(void* out, float* lse, const void* o_lat,
@@ -711,7 +756,7 @@ cudaError_t launch_decompress_merge_tc(void* out, float* lse, const void* o_lat,
                                        cudaStream_t s) {
     const int H = d.n_head, R = d.kv_rank, Dv = d.d_v;
     const int rows = batch * d.t_q;
-    const int n_tile = 128;
+    const int n_tile = merge_n_tile(d, rows);
     CUtensorMap b;
     // B: w_uv viewed as {R, Dv, H} (K contiguous); box {64 K, n_tile N, 1}
     cudaError_t e = make_map(&b, w_uv, R, Dv, H, (cuuint64_t)R * 2, (cuuint64_t)Dv * R * 2, 64,
@@ -743,15 +788,19 @@ cudaError_t launch_decompress_merge_tc(void* out, float* lse, const void* o_lat,
     });
     if (attr_err != cudaSuccess) return attr_err;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;  // the CTAs of one head
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = (unsigned)(Dv / n_tile);
+    attr[1].val.clusterDim.z = 1;
     cfg.gridDim = dim3(H, Dv / n_tile, (rows + 127) / 128);
     cfg.blockDim = dim3(kMThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, tc_decompress_merge_kernel, b, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
