@@ -298,34 +298,6 @@ __device__ __forceinline__ int valid_blocks(const Walk& w) {
     return nb < 4 ? nb : 4;
 }
 
-// One epilogue step of a warp: its 32 rows x 64 columns of O (x0, x1: this
-// lane's row, f32), scaled by inv, go out as bf16 through a 4 KB scratch so
-// that each store writes whole 128-byte row pieces (lane l: 16 bytes l % 8 of
-// row 4 i + l / 8; rows from row_lim on are not written).
-__device__ __forceinline__ void epilogue_emit64(uint32_t scr, int lane, const uint32_t (&x0)[32],
-                                                const uint32_t (&x1)[32], float inv,
-                                                __nv_bfloat16* dst0, int col, int row_lim) {
-    const uint32_t rowa = scr + lane * 128;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-        const uint32_t* x = u < 4 ? &x0[8 * u] : &x1[8 * (u - 4)];
-        st_shared_v4(rowa + ((u ^ (lane & 7)) << 4),
-                     pack_bf16x2(__uint_as_float(x[0]) * inv, __uint_as_float(x[1]) * inv),
-                     pack_bf16x2(__uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv),
-                     pack_bf16x2(__uint_as_float(x[4]) * inv, __uint_as_float(x[5]) * inv),
-                     pack_bf16x2(__uint_as_float(x[6]) * inv, __uint_as_float(x[7]) * inv));
-    }
-    __syncwarp();
-    const int pc = lane & 7;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int rw = 4 * i + (lane >> 3);
-        const uint4 val = ld_shared_v4(scr + rw * 128 + ((pc ^ (rw & 7)) << 4));
-        if (rw < row_lim) *reinterpret_cast<uint4*>(dst0 + (long long)rw * 512 + col + pc * 8) = val;
-    }
-    __syncwarp();
-}
-
 // ------------------------------------------------------------------ kernel
 // Role map (13 warps per CTA):
 //   S-CTA  warps 0-3  K loaders: warp k expects block k of each tile; warps 0-1
@@ -344,7 +316,8 @@ __device__ __forceinline__ void epilogue_emit64(uint32_t scr, int lane, const ui
 template <int W>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_pair_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap qmap,
-                       const __grid_constant__ CUtensorMap vmap, const Params p) {
+                       const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
+                       const __grid_constant__ CUtensorMap wmap, const Params p) {
     constexpr int NKC = W / 64;  // 64-column chunks in a cache row (9 or 8)
     extern __shared__ __align__(1024) unsigned char smem[];
     Ctrl& c = *reinterpret_cast<Ctrl*>(smem + kCtrlOff);
@@ -957,27 +930,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const float inv = empty ? 0.f : 1.f / lsum;
                 const float lse_v = empty ? -INFINITY : (m + log2f(lsum)) * 0.69314718055994531f;
                 // bf16 rows: each warp takes its 32 rows and its half of the
-                // columns, 64 at a time, through a private 4 KB scratch in the
-                // freed V stage, and writes whole 128-byte row pieces (lane l
-                // stores piece l % 8 of row 4 i + l / 8). A full segment writes
-                // the output rows, a partial one its workspace slot, which the
-                // combine merges.
+                // columns, 64 at a time, into one of two private 4 KB scratch
+                // buffers in the freed V stage, and one lane stores the
+                // [32 rows x 64 columns] box by TMA; the next block's TMEM load
+                // runs while that store reads its buffer. A full segment writes
+                // the output rows (rows past the request's fall outside the
+                // output map), a partial one its workspace slot, which the
+                // combine or the merging decompress reads.
                 const int slot = pair * 2 + (seg == 0 ? 0 : 1);
-                {
-                    const uint32_t scr = smem_u32(smem + stage * kStage) + (uint32_t)(warp - 5) * 4096;
-                    __nv_bfloat16* dst0 = full_seg ? p.out + ((long long)w.b * Mq + w.g * 128 + q * 32) * 512
-                                                   : p.ws_o + ((long long)slot * 128 + q * 32) * 512;
-                    const int row_lim = min(32, min(128, Mq - w.g * 128) - q * 32);  // valid rows
+                const int row_lim = min(128, Mq - w.g * 128) - q * 32;  // this warp's valid rows
+                if (row_lim > 0) {
+                    const uint32_t scr0 = smem_u32(smem + stage * kStage) + (uint32_t)(warp - 5) * 8192;
 #pragma unroll 1
-                    for (int cb = c_lo; cb < c_lo + 256; cb += 64) {
+                    for (int cb = c_lo, nb = 0; cb < c_lo + 256; cb += 64, ++nb) {
+                        const uint32_t scr = scr0 + (uint32_t)(nb & 1) * 4096;
+                        if (nb >= 2) {
+                            if (lane == 0) bulk_wait_read_1();  // the store of block nb - 2 has read it
+                            __syncwarp();
+                        }
                         uint32_t v0[32], v1[32];
                         tmem_ld32(tbase + lane_off + cb, v0);
                         tmem_ld32(tbase + lane_off + cb + 32, v1);
                         tmem_wait_ld();
-                        epilogue_emit64(scr, lane, v0, v1, inv, dst0, cb, row_lim);
+                        const uint32_t rowa = scr + lane * 128;
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const uint32_t* x = u < 4 ? &v0[8 * u] : &v1[8 * (u - 4)];
+                            st_shared_v4(rowa + ((u ^ (lane & 7)) << 4),
+                                         pack_bf16x2(__uint_as_float(x[0]) * inv, __uint_as_float(x[1]) * inv),
+                                         pack_bf16x2(__uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv),
+                                         pack_bf16x2(__uint_as_float(x[4]) * inv, __uint_as_float(x[5]) * inv),
+                                         pack_bf16x2(__uint_as_float(x[6]) * inv, __uint_as_float(x[7]) * inv));
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (full_seg)
+                                tma_store_3d(&omap, scr, cb, w.g * 128 + q * 32, w.b);
+                            else
+                                tma_store_3d(&wmap, scr, cb, q * 32, slot);
+                            bulk_commit();
+                        }
                     }
-                    // the scratch is in a stage the async proxy refills next
-                    fence_proxy_async_smem();
+                    if (lane == 0) bulk_wait_read_all();  // the stage may be refilled after this
+                    __syncwarp();
                 }
                 if (lead && row_ok) {
                     if (full_seg) {
@@ -997,6 +993,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     seg_tile0 = w.tile;
                 }
             }
+            if (lane == 0) bulk_wait_all();  // the epilogue's stores are complete
             __syncwarp();
         }
     }
@@ -1323,6 +1320,30 @@ cudaError_t launch_decode_tc(void* out, float* lse, const void* q_abs, const voi
             return cudaErrorInvalidValue;
         }
     }
+    // epilogue stores: [32 rows x 64 columns] boxes of output rows
+    // {512, t_q * n_head, batch} (rows past a request's fall outside) and of
+    // the workspace's partial rows {512, 128, 2 * pairs}
+    CUtensorMap omap, wmap;
+    {
+        const int Mq = d.t_q * d.n_head;
+        cuuint64_t odims[3] = {512, (cuuint64_t)Mq, (cuuint64_t)batch};
+        cuuint64_t ostrides[2] = {512 * 2, (cuuint64_t)Mq * 512 * 2};
+        cuuint64_t wdims[3] = {512, 128, (cuuint64_t)2 * np};
+        cuuint64_t wstrides[2] = {512 * 2, 128 * 512 * 2};
+        cuuint32_t box[3] = {64, 32, 1};
+        cuuint32_t es3[3] = {1, 1, 1};
+        cr = enc(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out, odims, ostrides, box, es3,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr == CUDA_SUCCESS)
+            cr = enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, workspace, wdims, wstrides, box,
+                     es3, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr != CUDA_SUCCESS) {
+            set_error("cuTensorMapEncodeTiled (epilogue stores) failed (%d)", (int)cr);
+            return cudaErrorInvalidValue;
+        }
+    }
     Params p;
     p.q_abs = (const __nv_bfloat16*)q_abs;
     p.kv = (const __nv_bfloat16*)kv_cache;
@@ -1362,9 +1383,9 @@ cudaError_t launch_decode_tc(void* out, float* lse, const void* q_abs, const voi
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     if (W == 576)
-        e = cudaLaunchKernelEx(&cfg, decode_pair_kernel<576>, tmap, qmap, vmap, p);
+        e = cudaLaunchKernelEx(&cfg, decode_pair_kernel<576>, tmap, qmap, vmap, omap, wmap, p);
     else
-        e = cudaLaunchKernelEx(&cfg, decode_pair_kernel<512>, tmap, qmap, vmap, p);
+        e = cudaLaunchKernelEx(&cfg, decode_pair_kernel<512>, tmap, qmap, vmap, omap, wmap, p);
     if (e != cudaSuccess) return e;
     if (!combine) return cudaGetLastError();
     const long long G = (d.t_q * d.n_head + 127) / 128;
