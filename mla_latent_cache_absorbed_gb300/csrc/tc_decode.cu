@@ -362,6 +362,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_u32(&c.tmem_base), 512);
         tmem_relinquish();
     }
+    if (rank == 1 && warp != 2) {
+        // O-CTA: clear the V stages once, so a block past a request's end that
+        // the P*V MMA reads (under P = 0) never holds a NaN
+        for (int i = tid - (warp > 2 ? 32 : 0); i < kNS * kStage / 16; i += kThreads - 32)
+            reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+    }
     if (warp == 2) {
         // the pair's unit range, worked out once per CTA while the barriers and
         // TMEM are set up; every warp starts its walk from it
@@ -732,21 +739,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                   kWaitLimit);
             }
         } else if (warp == 1) {
-            // ---------------- V landing: rows past the request are zeroed (P there
-            // is 0, but 0 * NaN would still poison the accumulator)
+            // ---------------- V landing: the rows of the tile's last cache block
+            // past the request are zeroed (P there is 0, but 0 * NaN would still
+            // poison the accumulator). Blocks past the request are not loaded;
+            // their rows are zeros (the stages are cleared at start) or rows of
+            // an earlier tile, all finite.
             long long i = 0;
             for (; w.u < w.u_end; walk_next(p, w), ++i) {
                 const int s = (int)(i % kNS);
                 if (!wt.wait_warp(smem_u32(&c.full[s]), (uint32_t)((i / kNS) & 1))) break;
                 const int nvalid = min(kTok, w.S - w.tile * kTok);
-                if (nvalid < kTok) {
-                    const int rows = kTok - nvalid;
-                    for (int e = lane; e < rows * 8 * 8; e += 32) {
-                        const int ch = e / (rows * 8);
-                        const int rr = nvalid + (e / 8) % rows;
-                        const int u = e % 8;
-                        *reinterpret_cast<uint4*>(smem + s * kStage + (rr >> 4) * kVBlock +
-                                                  ch * 2048 + (rr & 15) * 128 + u * 16) =
+                const int r0 = nvalid & 15;  // first row past the request in its block
+                if (r0 != 0) {
+                    // [8 chunks][16 - r0 rows][8 pieces of 16 bytes] of block nvalid / 16
+                    const int nr = 16 - r0;
+                    unsigned char* blk = smem + s * kStage + (nvalid >> 4) * kVBlock + r0 * 128;
+                    for (int e = lane; e < 8 * 8 * nr; e += 32) {
+                        const int ch = e >> 3 & 7, u = e & 7, rr = e >> 6;
+                        *reinterpret_cast<uint4*>(blk + ch * 2048 + rr * 128 + u * 16) =
                             make_uint4(0, 0, 0, 0);
                     }
                     fence_proxy_async_smem();
@@ -847,7 +857,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const uint32_t pa = smem_u32(smem + kSideOff + slot * kPBytes);
                     const uint32_t va = smem_u32(smem + s * kStage);
                     // V: K-step kk is cache block kk of the tile; its latent columns
-                    // sit in 8 chunks of [16 rows][128 B] at a 2 KB stride
+                    // sit in 8 chunks of [16 rows][128 B] at a 2 KB stride. A block
+                    // past the request holds zeros or an earlier tile's rows (finite),
+                    // under P columns that are 0.
 #pragma unroll
                     for (int half = 0; half < 2; ++half)
 #pragma unroll

@@ -410,8 +410,8 @@ __global__ void __launch_bounds__(kMThreads, 1)
     int* sh_np = sh_pf + 128;     // parts per row: 0 empty, 1 copied from o_lat, >1 merged
     int* sh_s0 = sh_np + 128;
     int* sh_rr = sh_s0 + 128;
-    int* sh_off = sh_rr + 128;    // 131 entries: the LSE-load prefix, the largest part count, the others' rows
-    float* sh_lse = reinterpret_cast<float*>(sh_off + 132);  // 131 used
+    int* sh_off = sh_rr + 128;    // 132 entries: the LSE-load prefix, the largest part count, the others' rows, prefetch
+    float* sh_lse = reinterpret_cast<float*>(sh_off + 132);
     float* sh_w = sh_lse + 128;
     uint64_t* empty = full + kMStages;
     uint64_t* aready = empty + kMStages;
@@ -537,13 +537,18 @@ __global__ void __launch_bounds__(kMThreads, 1)
                 sh_off[mrows] = o;
                 sh_off[mrows + 1] = npm;
                 sh_off[mrows + 2] = others;
+                // a long decode (pairs past 32 tiles) wrote its first partial rows
+                // long before it ends: they are prefetched back into L2 below
+                sh_off[mrows + 3] = sh.U > split::kAlignedMaxShare * sh.np_g ? 1 : 0;
             }
         }
         named_sync(1, kMT);
         // the rows this CTA will read (partial rows, copied o_lat rows) into L2
         // while the decode finishes: L2 is the coherence point, so rows the
-        // decode writes after their prefetch still read back as written
-        {
+        // decode writes after their prefetch still read back as written. Only
+        // after a long decode: a short one's rows are still in L2, and the
+        // prefetches would only delay the merge.
+        if (sh_off[mrows + 3]) {
             const int nl0 = sh_off[mrows];
             for (int i = mt; i < nl0; i += kMT) {
                 int r = 0;
