@@ -44,23 +44,36 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def kernel_fingerprint():
+    """sha1 of the pair decode kernel's code: tc_decode.cu and the headers it
+    includes, with comments, blank lines and indentation dropped (a comment
+    edit does not change the kernel)."""
+    import hashlib
+    h = hashlib.sha1()
+    for name in ("tc_decode.cu", "tc_split.cuh", "sm100.cuh"):
+        path = os.path.join(ROOT, "mla_latent_cache_absorbed_gb300", "csrc", name)
+        if not os.path.exists(path):
+            return None
+        for line in open(path):
+            code = line.split("//", 1)[0].strip()
+            if code:
+                h.update(code.encode() + b"\n")
+    return h.hexdigest()
+
+
 def profiled_traffic(config_name):
     """DRAM bytes (read + write) per launch of the pair decode kernel from the
     committed ncu summary of this workload, or None when there is none or the
-    kernel source has changed since it was captured (the summary records the
-    sha1 of tc_decode.cu it was taken on)."""
-    import hashlib
+    kernel has changed since it was captured (the summary records the
+    kernel_fingerprint() it was taken on)."""
     prof = os.path.join(ROOT, "profiles", f"decode_pair_{config_name}.md")
-    src = os.path.join(ROOT, "mla_latent_cache_absorbed_gb300", "csrc", "tc_decode.cu")
-    if not (os.path.exists(prof) and os.path.exists(src)):
+    if not os.path.exists(prof):
         return None
     text = open(prof).read()
     m_t = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
-    m_h = re.search(r"kernel_source_sha1:\s*([0-9a-f]+)", text)
-    if not (m_t and m_h):
-        return None
-    sha = hashlib.sha1(open(src, "rb").read()).hexdigest()
-    if not sha.startswith(m_h.group(1)):
+    m_h = re.search(r"kernel_fingerprint:\s*([0-9a-f]+)", text)
+    fp = kernel_fingerprint()
+    if not (m_t and m_h and fp) or not fp.startswith(m_h.group(1)):
         return None
     return int(m_t.group(1))
 

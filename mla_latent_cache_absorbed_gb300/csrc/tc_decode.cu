@@ -11,15 +11,17 @@
 // form row groups of 128 (the MMA M dimension); all rows share the same
 // cache rows, so heads are the M dimension and cache tokens the N (scores)
 // or K (P*V) dimension. A unit of work is (request, row group, 64-token
-// tile). A persistent grid of CTA pairs splits the unit sequence evenly.
-// In each pair:
+// tile). A persistent grid of CTA pairs splits the unit sequence as
+// tc_split.cuh describes (evenly, or aligned to requests when pairs get few
+// tiles). In each pair:
 //   CTA 0 ("S-CTA") holds the 128 query rows in TMEM (A operand) and computes
 //     S = Q K^T for each tile (M=128, N=64, K=576 or 512) into TMEM, runs the
-//     online softmax (one thread per query row, lazy rescaling), and writes
+//     online softmax (two threads per query row, lazy rescaling), and writes
 //     the bf16 probabilities P [128 x 64] into CTA 1's shared memory.
 //   CTA 1 ("O-CTA") holds O [128 x 512] f32 in all 512 TMEM columns and
 //     computes O += P V (M=128, N=2x256, K=64) with V the leading 512 columns
-//     of the same tile, delivered to both CTAs by one multicast TMA load.
+//     of the same tile, which it loads itself (L2 hits: its prefetcher warp
+//     pulls the tiles ahead of both CTAs).
 // The O accumulator alone fills a TMEM, so splitting the roles keeps both the
 // QK^T and the P*V contractions at M=128 with no repeated work; the only
 // exchange is P (16 KB per 64-token tile) plus per-row rescale factors.
@@ -306,13 +308,16 @@ __device__ __forceinline__ int valid_blocks(const Walk& w) {
 //          warps 5-12 softmax, two threads per query row (32 score columns
 //                     each); P goes to the O-CTA by st.async
 //   O-CTA  warp 0     V loader: one 4-D box per cache block
-//          warp 1     V landing: zeroes rows past the request, releases the stage
+//          warp 1     V landing: zeroes the rows of a partial last block past
+//                     the request, releases the stage
 //          warp 2     L2 prefetcher of upcoming cache blocks
 //          warp 4     O += P V MMA issuer; owns the TMEM allocation
 //          warps 5-12 rescale and epilogue: warp w takes the TMEM lanes of
 //                     its quadrant (w % 4) and half the 512 columns
 //          warp 3     K helper: loads blocks 2-3 of each S-CTA tile (multicast
 //                     to the S-CTA only), so both TMA units share the boxes
+// In both CTAs warp 2 first works out the pair's unit range (walk_init) while
+// the barriers and TMEM are set up; every warp then follows that walk.
 template <int W>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_pair_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap qmap,
