@@ -60,6 +60,9 @@ CASES = [
     ("deepseek_decode", [8192, 1, 100, 16, 0, 2049, 3000, 5000]),
     ("glm53_flash_nope", [2048, 7, 0, 129, 31, 32768]),         # NoPE rows, one long request
     ("glm52_causal_t4", [4, 5, 100, 1000, 0, 4096]),            # t_q = 4: two row groups
+    ("glm52_decode", [32768]),       # one request on every pair: 76 parts a row
+    ("glm52_decode", [5000]),        # batch of one: the cluster's second CTA owns no row
+    ("deepseek_decode", [20000]),    # batch of one, 128 heads, one merge CTA per head
 ]
 
 
