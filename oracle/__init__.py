@@ -60,6 +60,7 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int
 _F = ctypes.c_float
 _I64 = ctypes.c_int64
+_D = ctypes.c_double
 
 
 def _declare(lib):
@@ -80,10 +81,14 @@ def _declare(lib):
     lib.oracle_rope_neox.argtypes = [_P, _I, _F, _F]
     lib.oracle_norm_to_neox_perm.argtypes = [_I, _P]
     lib.oracle_cache_append.argtypes = [_P, _I, _P, _P, _I, _P, _I, _I64, _I, _I]
+    lib.oracle_kv_prolog_row.argtypes = [_P, _P, _P, _P, _I, _I64, _I64, _I, _I, _D, _F]
+    lib.oracle_cache_append_rmsnorm_rope.argtypes = [_P, _I, _P, _P, _P, _I, _P, _P, _I, _I64,
+                                                     _I, _I, _D, _F]
     for name in ("oracle_absorb_q", "oracle_decode_range", "oracle_decode_rows",
                  "oracle_decode_paged", "oracle_combine", "oracle_decompress",
                  "oracle_attend_naive", "oracle_attend_absorbed",
-                 "oracle_norm_to_neox_perm", "oracle_cache_append"):
+                 "oracle_norm_to_neox_perm", "oracle_cache_append", "oracle_kv_prolog_row",
+                 "oracle_cache_append_rmsnorm_rope"):
         getattr(lib, name).restype = _I
     lib.oracle_rope_interleaved.restype = None
     lib.oracle_rope_neox.restype = None
@@ -320,5 +325,56 @@ def cache_append(kv_cache, kv_c, k_pe, slot_mapping, allow_errors=False, lib=Non
     num_slots = int(np.prod(cache.shape[:-1]))
     st = lib.oracle_cache_append(_ptr(cache), cdt, _ptr(kv_c_a), _ptr(k_pe_a), sdt, _ptr(slots), n,
                                  num_slots, R, P)
+    _check(st, allow_errors)
+    return cache
+
+
+def _prolog_inputs(kv_c, k_pe, gamma, positions):
+    kv_c_a, sdt = _elem(np.asarray(kv_c))
+    n, R = kv_c_a.shape
+    if k_pe is None:
+        k_pe_a, sdt2, P = np.zeros((n, 0), kv_c_a.dtype), sdt, 0
+    else:
+        k_pe_a, sdt2 = _elem(np.asarray(k_pe))
+        P = k_pe_a.shape[1]
+    g_a, sdt3 = _elem(np.asarray(gamma))
+    if not (sdt == sdt2 == sdt3):
+        raise TypeError("kv_c, k_pe and gamma must share an element type")
+    if g_a.shape != (R,):
+        raise ValueError("gamma must have kv_rank elements")
+    pos = np.ascontiguousarray(np.zeros(n) if positions is None else positions, dtype=np.int64)
+    return kv_c_a, k_pe_a, g_a, pos, sdt, n, R, P
+
+
+def kv_prolog_rows(kv_c, k_pe, gamma, positions, eps, rope_base, lib=None) -> np.ndarray:
+    """The cache rows [RmsNorm(kv_c[n]) | rope_neox(k_pe[n], positions[n])]
+    before any cast, as float64 [n, R + P] (the norm in f64, the rope in the
+    mla.rs page's f32); the "aclnnMlaProlog" page's key formulas."""
+    lib = lib or load()
+    kv_c_a, k_pe_a, g_a, pos, sdt, n, R, P = _prolog_inputs(kv_c, k_pe, gamma, positions)
+    rows = np.empty((n, R + P), np.float64)
+    for t in range(n):
+        _check(lib.oracle_kv_prolog_row(_ptr(rows[t]), _ptr(kv_c_a), _ptr(k_pe_a), _ptr(g_a), sdt,
+                                        t, int(pos[t]), R, P, float(eps), float(rope_base)), False)
+    return rows
+
+
+def cache_append_rmsnorm_rope(kv_cache, kv_c, k_pe, gamma, positions, slot_mapping, eps,
+                              rope_base, allow_errors=False, lib=None):
+    """cache_append of the rows kv_prolog_rows gives (rounded to f32, then
+    cast to the cache's type), on a copy of kv_cache that is returned."""
+    lib = lib or load()
+    cache = np.array(kv_cache, copy=True, order="C")
+    if cache.dtype not in (np.float32, np.uint16):
+        raise TypeError("cache must be float32 or bf16 bits (uint16)")
+    cdt = BF16 if cache.dtype == np.uint16 else F32
+    kv_c_a, k_pe_a, g_a, pos, sdt, n, R, P = _prolog_inputs(kv_c, k_pe, gamma, positions)
+    if cache.shape[-1] != R + P:
+        raise ValueError("cache row width must be kv_rank + d_rope")
+    slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    num_slots = int(np.prod(cache.shape[:-1]))
+    st = lib.oracle_cache_append_rmsnorm_rope(_ptr(cache), cdt, _ptr(kv_c_a), _ptr(k_pe_a),
+                                              _ptr(g_a), sdt, _ptr(pos), _ptr(slots), n,
+                                              num_slots, R, P, float(eps), float(rope_base))
     _check(st, allow_errors)
     return cache

@@ -39,6 +39,12 @@
  *   oracle_cache_append    the vLLM CPU MLA page, CPUMLAImpl.do_kv_cache_update
  *                          (scatter of [kv_c | k_pe] rows by slot mapping,
  *                          padding slots -1 skipped, cast to the cache type).
+ *   oracle_kv_prolog_row / oracle_cache_append_rmsnorm_rope
+ *                          the "aclnnMlaProlog" page, computation formulas of
+ *                          the key (RmsNorm of the latent, rope of k^R, both
+ *                          stored in the cache), with the mla.rs NEOX rope and
+ *                          the scatter of do_kv_cache_update. The RmsNorm is
+ *                          taken in f64 (the page fixes no precision).
  */
 #include <math.h>
 #include <stdint.h>
@@ -464,4 +470,78 @@ int oracle_norm_to_neox_perm(int n_dims, int32_t* perm) {
         perm[2 * j + 1] = j + half;
     }
     return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* KV half of the MLA prolog ("aclnnMlaProlog" page, computation formulas of  */
+/* the key: c^KV = RmsNorm(x W^DKV) to the cache, k^R = Cache(ROPE(x W^KR))),  */
+/* written by slot mapping as the vLLM CPU MLA page's do_kv_cache_update does  */
+/* ------------------------------------------------------------------------- */
+/* One token's cache row before the cast, in f64:
+ *   row[i]     = gamma_i * x_i / RMS(x),  RMS(x) = sqrt(sum_k x_k^2 / R + eps)
+ *                over the R = kv_rank latent elements x = kv_c[n] (the page's
+ *                RmsNorm formula; it fixes no precision, so this is f64);
+ *   row[R + j] = the mla.rs NEOX rope of k_pe[n] at the token's position, in
+ *                f32 as that page computes it (the rope features are in NEOX
+ *                order: the load-time permutation was applied to W^KR).
+ * gamma has kv_rank elements of src_dtype. */
+int oracle_kv_prolog_row(double* row, const void* kv_c, const void* k_pe, const void* gamma,
+                         int src_dtype, int64_t n, int64_t position, int kv_rank, int d_rope,
+                         double eps, float rope_base) {
+    if (kv_rank <= 0 || d_rope < 0 || (d_rope & 1) || d_rope > 4096 || !(eps >= 0.0))
+        return ORACLE_BAD_ARG;
+    double ss = 0.0;
+    for (int k = 0; k < kv_rank; ++k) {
+        const double x = load_elem(kv_c, src_dtype, n * kv_rank + k);
+        ss += x * x;
+    }
+    const double rms = sqrt(ss / (double)kv_rank + eps);
+    for (int i = 0; i < kv_rank; ++i) {
+        const double x = load_elem(kv_c, src_dtype, n * kv_rank + i);
+        const double g = load_elem(gamma, src_dtype, i);
+        row[i] = g * x / rms;
+    }
+    if (d_rope > 0) {
+        float pe[4096];
+        for (int j = 0; j < d_rope; ++j) pe[j] = load_elem(k_pe, src_dtype, n * d_rope + j);
+        oracle_rope_neox(pe, d_rope, (float)position, rope_base);
+        for (int j = 0; j < d_rope; ++j) row[kv_rank + j] = pe[j];
+    }
+    return ORACLE_OK;
+}
+
+/* For every token n with slot s = slots[n] >= 0: flat cache row s = the row
+ * above, rounded to f32 and then cast to the cache type (the kernel rounds
+ * from f32 too, so both sides take the bf16 rounding from the same f32
+ * value). Padding slots (< 0) are skipped; a slot at or past num_slots is
+ * skipped and reported (status BAD_BLOCK), as in oracle_cache_append. */
+int oracle_cache_append_rmsnorm_rope(void* cache, int cache_dtype, const void* kv_c,
+                                     const void* k_pe, const void* gamma, int src_dtype,
+                                     const int64_t* positions, const int64_t* slots, int n_tokens,
+                                     int64_t num_slots, int kv_rank, int d_rope, double eps,
+                                     float rope_base) {
+    if (n_tokens < 0 || kv_rank <= 0 || d_rope < 0 || kv_rank + d_rope > 8192) return ORACLE_BAD_ARG;
+    const int W = kv_rank + d_rope;
+    double row[8192];
+    int status = ORACLE_OK;
+    for (int n = 0; n < n_tokens; ++n) {
+        const int64_t s = slots[n];
+        if (s < 0) continue;
+        if (s >= num_slots) {
+            status = ORACLE_BAD_BLOCK;
+            continue;
+        }
+        const int st = oracle_kv_prolog_row(row, kv_c, k_pe, gamma, src_dtype, n,
+                                            d_rope > 0 ? positions[n] : 0, kv_rank, d_rope, eps,
+                                            rope_base);
+        if (st != ORACLE_OK) return st;
+        for (int j = 0; j < W; ++j) {
+            const float v = (float)row[j];
+            if (cache_dtype == ORACLE_BF16)
+                ((uint16_t*)cache)[s * W + j] = f32_to_bf16_rne(v);
+            else
+                ((float*)cache)[s * W + j] = v;
+        }
+    }
+    return status;
 }

@@ -18,7 +18,10 @@ AssertionError when the oracle disagrees with:
   * the cache append of the vLLM CPU MLA page (do_kv_cache_update): rows land
     at their slots unchanged (f32) or as torch's bf16 cast of them, padding
     slots are skipped, other rows keep their bits, a slot past the cache is
-    reported.
+    reported;
+  * the KV half of the MLA prolog of the "aclnnMlaProlog" page (RmsNorm of
+    the latent, rope of k^R at each token's position, then the same scatter):
+    closed forms of the norm and an f64 rotation for the rope.
 """
 from __future__ import annotations
 
@@ -485,9 +488,97 @@ def check_cache_append(lib):
         pass
 
 
+def _rotation_f64(k_pe_row, pos, base):
+    """NEOX rope written as the rotation it is: pair (j, j + n/2) turned by
+    theta_j = pos * base^(-2j/n), in f64."""
+    n = k_pe_row.size
+    half = n // 2
+    th = float(pos) * float(base) ** (-2.0 * np.arange(half) / n)
+    a = k_pe_row[:half].astype(np.float64)
+    b = k_pe_row[half:].astype(np.float64)
+    return np.concatenate([a * np.cos(th) - b * np.sin(th), a * np.sin(th) + b * np.cos(th)])
+
+
+def check_kv_prolog(lib):
+    """KV half of the MLA prolog ("aclnnMlaProlog" page, key formulas): the
+    RmsNorm of the latent against closed forms (a constant row c gives
+    gamma sign(c) with eps = 0 and gamma c / sqrt(c^2 + eps) otherwise; unit
+    mean square; scale invariance; a zero row stays zero), the rope of k^R
+    against an f64 rotation at each token's own position (identity at 0,
+    pair norms kept at large positions), and the scatter of
+    do_kv_cache_update (padding skipped, other rows untouched, f32 rows
+    exact, bf16 rows torch's cast of them, a slot past the cache reported)."""
+    import oracle as O
+    import torch
+    rng = np.random.default_rng(13)
+    R, P, base = 32, 8, 10000.0
+    gamma = rng.uniform(0.5, 1.5, R).astype(np.float32)
+    kv = np.array([[3.0] * R, [-0.5] * R], np.float32)
+    kp = np.zeros((2, P), np.float32)
+    rows = O.kv_prolog_rows(kv, kp, gamma, [0, 0], 0.0, base, lib=lib)
+    assert maxdiff(rows[0, :R], gamma) <= 1e-12 and maxdiff(rows[1, :R], -gamma) <= 1e-12
+    for c, eps in ((3.0, 27.0), (-0.5, 0.75)):   # eps = 3 c^2: gamma sign(c) / 2
+        row = O.kv_prolog_rows(np.full((1, R), c, np.float32), kp[:1], gamma, [0], eps, base,
+                               lib=lib)[0]
+        assert maxdiff(row[:R], gamma * math.copysign(0.5, c)) <= 1e-12, (c, eps)
+    x = rng.standard_normal((3, R)).astype(np.float32)
+    ones = np.ones(R, np.float32)
+    y = O.kv_prolog_rows(x, np.zeros((3, P), np.float32), ones, [0, 0, 0], 0.0, base, lib=lib)
+    assert np.all(np.abs((y[:, :R] ** 2).mean(1) - 1.0) <= 1e-12)
+    y4 = O.kv_prolog_rows(4 * x, np.zeros((3, P), np.float32), ones, [0] * 3, 0.0, base, lib=lib)
+    assert maxdiff(y4[:, :R], y[:, :R]) <= 1e-14
+    yg = O.kv_prolog_rows(x, np.zeros((3, P), np.float32), gamma, [0] * 3, 0.0, base, lib=lib)
+    assert maxdiff(yg[:, :R], y[:, :R] * gamma) <= 1e-12
+    z = O.kv_prolog_rows(np.zeros((1, R), np.float32), kp[:1], gamma, [0], 1e-6, base, lib=lib)
+    assert np.all(z == 0.0)
+    # rope: each token at its own position
+    kpe = rng.standard_normal((5, P)).astype(np.float32)
+    pos = np.array([0, 1, 3, 40, 17], np.int64)
+    rows = O.kv_prolog_rows(x[np.arange(5) % 3], kpe, gamma, pos, 1e-6, base, lib=lib)
+    assert np.array_equal(rows[0, R:], kpe[0].astype(np.float64))
+    for t in range(1, 5):
+        assert maxdiff(rows[t, R:], _rotation_f64(kpe[t], pos[t], base)) <= 2e-5, t
+    far = O.kv_prolog_rows(x[:1], kpe[:1], gamma, [100000], 1e-6, base, lib=lib)[0, R:]
+    h = P // 2
+    n0 = np.hypot(kpe[0, :h].astype(np.float64), kpe[0, h:])
+    n1 = np.hypot(far[:h], far[h:])
+    assert np.all(np.abs(n1 - n0) <= 1e-5 * n0)
+    # scatter by slot mapping
+    nb, bs = 4, 16
+    slots = np.array([7, -1, 63, 2, 20], np.int64)   # row 0 is nobody's
+    kvs = x[np.arange(5) % 3]
+    poison = np.full((nb, bs, R + P), -7.25, np.float32)
+    out = O.cache_append_rmsnorm_rope(poison, kvs, kpe, gamma, pos, slots, 1e-6, base,
+                                      lib=lib).reshape(-1, R + P)
+    rows32 = rows.astype(np.float32)
+    for t, s_ in enumerate(slots):
+        if s_ >= 0:
+            assert np.array_equal(out[s_], rows32[t]), t
+            assert maxdiff(out[s_, R:], _rotation_f64(kpe[t], pos[t], base)) <= 2e-5, t
+    untouched = np.setdiff1d(np.arange(nb * bs), slots[slots >= 0])
+    assert np.all(out[untouched] == -7.25)
+    pb = np.full((nb, bs, R + P), 0x1234, np.uint16)
+    outb = O.cache_append_rmsnorm_rope(pb, kvs, kpe, gamma, pos, slots, 1e-6, base,
+                                       lib=lib).reshape(-1, R + P)
+    ref = torch.from_numpy(rows32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    for t, s_ in enumerate(slots):
+        if s_ >= 0:
+            assert np.array_equal(outb[s_], ref[t]), t
+    assert np.all(outb.reshape(-1, R + P)[untouched] == 0x1234)
+    bad = O.cache_append_rmsnorm_rope(poison, kvs[:1], kpe[:1], gamma, [5], [nb * bs], 1e-6, base,
+                                      allow_errors=True, lib=lib)
+    assert np.all(bad == -7.25)
+    try:
+        O.cache_append_rmsnorm_rope(poison, kvs[:1], kpe[:1], gamma, [5], [nb * bs], 1e-6, base,
+                                    lib=lib)
+        raise AssertionError("a slot past the cache must be reported")
+    except O.OracleError:
+        pass
+
+
 QUICK_CHECKS = [check_naive_equals_absorbed, check_paged_chain_equals_naive,
                 check_bruteforce_f64, check_sdpa_reduction, check_closed_forms,
                 check_split_combine, check_paged_equals_contiguous,
                 check_decode_rows_consistent, check_invalid_requests,
                 check_absorb_decompress_unit_weights, check_rope_permutation,
-                check_rope_against_rotation, check_cache_append]
+                check_rope_against_rotation, check_cache_append, check_kv_prolog]

@@ -59,6 +59,16 @@ MUTANTS = [
      "const int64_t s = slots[n] < 0 ? 0 : slots[n];", 0),
     ("append_rope_from_kv", "(int64_t)n * d_rope + (j - kv_rank));",
      "(int64_t)n * kv_rank + (j - kv_rank));", 0),
+    ("prolog_norm_sum_not_mean", "sqrt(ss / (double)kv_rank + eps)", "sqrt(ss + eps)", 0),
+    ("prolog_norm_drops_eps", "sqrt(ss / (double)kv_rank + eps)", "sqrt(ss / (double)kv_rank)", 0),
+    ("prolog_norm_no_gamma", "row[i] = g * x / rms;", "row[i] = x / rms;", 0),
+    ("prolog_norm_no_sqrt", "const double rms = sqrt(ss / (double)kv_rank + eps);",
+     "const double rms = ss / (double)kv_rank + eps;", 0),
+    ("prolog_rope_interleaved", "oracle_rope_neox(pe, d_rope,", "oracle_rope_interleaved(pe, d_rope,", 0),
+    ("prolog_rope_skipped", "oracle_rope_neox(pe, d_rope, (float)position, rope_base);", ";", 0),
+    ("prolog_position_of_token0", "d_rope > 0 ? positions[n] : 0", "d_rope > 0 ? positions[0] : 0", 0),
+    ("prolog_writes_padding", "const int64_t s = slots[n];\n        if (s < 0) continue;",
+     "const int64_t s = slots[n] < 0 ? 0 : slots[n];", 1),
 ]
 
 
