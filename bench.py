@@ -461,7 +461,11 @@ def measure_cache_append(wl, dc, stream, hbm_peak):
     cache: one new token per query row (the decode step's append) and a
     32768-token chunk (a prefill chunk), bf16 rows into the bf16 cache, unique
     random slots. CUDA-graph replays timed with events; algorithmic bytes =
-    tokens x (W x 2 read + W x 2 written + 8 slot bytes)."""
+    tokens x (W x 2 read + W x 2 written + 8 slot bytes). The same two
+    launches of mla_cache_append_rmsnorm_rope (RmsNorm of the latent and rope
+    of k_pe fused in, "aclnnMlaProlog" key formulas) add 8 position bytes a
+    token and the R x 2 bytes of gamma once; their positions are the decode
+    rows' own (seq_len - t_q + t) and 0 .. n-1 for the chunk."""
     import torch
     from mla_latent_cache_absorbed_gb300 import _native as N
     g = wl.geom
@@ -474,16 +478,31 @@ def measure_cache_append(wl, dc, stream, hbm_peak):
     rng = np.random.default_rng(99)
     # a scratch cache of the same geometry: the measured caches stay intact
     cache = torch.empty((dc.num_blocks, 16, W), dtype=torch.bfloat16, device=dev)
-    for label, n in (("decode_step", wl.rows), ("chunk_32k", 32768)):
+    gamma = (torch.rand(R, device=dev) + 0.5).to(torch.bfloat16)
+    cases = [(lab + sfx, n, fused) for fused, sfx in ((False, ""), (True, "_rmsnorm_rope"))
+             for lab, n in (("decode_step", wl.rows), ("chunk_32k", 32768))]
+    for label, n, fused in cases:
         n = min(n, num_slots)
         kv_c = torch.randn(n, R, device=dev).to(torch.bfloat16)
         k_pe = torch.randn(n, max(P, 1), device=dev).to(torch.bfloat16)
         slots = torch.from_numpy(rng.choice(num_slots, size=n, replace=False).astype(np.int64)).to(dev)
+        if n == wl.rows:   # the decode step: each query row's own position in its request
+            T = g.t_q
+            pos = np.repeat(np.asarray(wl.seq_lens, np.int64), T) - T + np.tile(np.arange(T), wl.batch)
+        else:              # a prefill chunk: consecutive positions
+            pos = np.arange(n)
+        positions = torch.from_numpy(np.maximum(pos, 0).astype(np.int64)).to(dev)
         reps = 200 if n < 4096 else 20
 
         def call():
-            N.mla_cache_append(cache, kv_c, k_pe if P else None, slots, n, dc.num_blocks, 1,
-                               dc.dims, None, stream)
+            if fused:
+                N.mla_cache_append_rmsnorm_rope(cache, kv_c, k_pe if P else None, gamma,
+                                                positions if P else None, slots, n,
+                                                dc.num_blocks, 1, 1e-6, 10000.0, dc.dims, None,
+                                                stream)
+            else:
+                N.mla_cache_append(cache, kv_c, k_pe if P else None, slots, n, dc.num_blocks, 1,
+                                   dc.dims, None, stream)
 
         call()
         torch.cuda.synchronize()
@@ -499,7 +518,7 @@ def measure_cache_append(wl, dc, stream, hbm_peak):
         e1.record(stream)
         torch.cuda.synchronize()
         us = e0.elapsed_time(e1) * 1e3 / reps
-        nbytes = n * (W * 2 * 2 + 8)
+        nbytes = n * (W * 2 * 2 + 8) + ((n * 8 if P else 0) + R * 2 if fused else 0)
         res[label] = {"tokens": n, "us": us, "bytes": nbytes,
                       "achieved_GBps": nbytes / (us * 1e-6) / 1e9,
                       "frac_of_hbm": nbytes / (us * 1e-6) / 1e9 / hbm_peak}

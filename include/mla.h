@@ -10,6 +10,8 @@
  *   mla_attend_absorbed the three above as one call (absorb, decode, merge
  *                       and decompress), the form a decode step uses
  *   mla_cache_append    write new tokens' latent rows into the paged cache
+ *   mla_cache_append_rmsnorm_rope  the same, with the RmsNorm of the latent
+ *                       and the rope of k_pe computed on the way in
  *   mla_rope_norm_to_neox_perm / mla_permute_rope_cols / mla_permute_rope_rows
  *                       the host-side load-time rope permutation
  *
@@ -243,6 +245,36 @@ mla_status mla_cache_append(void* kv_cache, const void* kv_c, const void* k_pe,
                             const int64_t* slot_mapping, int32_t n_tokens, int32_t num_blocks,
                             int32_t src_dtype, const mla_dims* dims, int32_t* dev_err,
                             void* stream);
+
+/*
+ * Cache append with the key half of the MLA prolog fused in ("aclnnMlaProlog",
+ * computation formulas of the key: c^KV = RmsNorm(x W^DKV) and
+ * k^R = ROPE(x W^KR), both stored in the cache). Takes the projections x W^DKV
+ * and x W^KR and writes, for every token n whose slot_mapping[n] >= 0,
+ *   flat[slot_mapping[n]] = [ gamma * kv_c[n] / RMS(kv_c[n]) |
+ *                             rope_neox(k_pe[n], positions[n]) ]   cast to dims->dtype
+ * with RMS(x) = sqrt(mean_i x_i^2 + eps) over the R latent elements, and the
+ * NEOX rope of the "memra_engine/mla.rs source" (fn rope_neox): pair
+ * (j, j + P/2) rotated by theta_j = pos * s^j, s = rope_base^(-2/P), theta
+ * stepped from pos by s in f32. The rope features are in NEOX order: the
+ * load-time permutation (below) has been applied to W^KR's rope rows.
+ * kv_cache, slot_mapping, num_blocks, dev_err: as mla_cache_append.
+ * kv_c      [n_tokens][R]   in, src_dtype; the latent before the norm
+ * k_pe      [n_tokens][P]   in, src_dtype; before the rope. NULL only if P == 0
+ * gamma     [R]             in, src_dtype; the norm's weight
+ * positions [n_tokens] int64 in; each token's position (theta uses it as an
+ *                           f32, exact below 2^24). NULL only if P == 0
+ * eps       >= 0, finite; rope_base > 0, finite (unused when P == 0)
+ * Arithmetic in f32 (sum of squares, scale, rotation); the cast to bf16
+ * rounds to nearest even. kv_c, gamma, kv_cache 16-byte aligned; slot_mapping
+ * and positions 8-byte aligned. n_tokens == 0 is a no-op. Stream-ordered.
+ */
+mla_status mla_cache_append_rmsnorm_rope(void* kv_cache, const void* kv_c, const void* k_pe,
+                                         const void* gamma, const int64_t* positions,
+                                         const int64_t* slot_mapping, int32_t n_tokens,
+                                         int32_t num_blocks, int32_t src_dtype, float eps,
+                                         float rope_base, const mla_dims* dims, int32_t* dev_err,
+                                         void* stream);
 
 /*
  * Load-time rope permutation ("memra_engine/mla.rs source", fn

@@ -27,7 +27,7 @@ DEVERR_TIMEOUT = 8
 # Every exported symbol of include/mla.h.
 EXPORTS = ("mla_absorb_q", "mla_decode_workspace_size", "mla_decode_paged",
            "mla_decode_paged_static", "mla_decompress_out", "mla_cache_append",
-           "mla_attend_workspace_size", "mla_attend_absorbed",
+           "mla_cache_append_rmsnorm_rope", "mla_attend_workspace_size", "mla_attend_absorbed",
            "mla_rope_norm_to_neox_perm",
            "mla_permute_rope_cols", "mla_permute_rope_rows", "mla_status_str",
            "mla_last_error")
@@ -73,6 +73,7 @@ def load(path: str = LIB_PATH):
     lib.mla_decode_paged_static.argtypes = [P, P, P, P, P, P, I32, I32, I32, D, F, P, P]
     lib.mla_decompress_out.argtypes = [P, P, P, I32, D, P]
     lib.mla_cache_append.argtypes = [P, P, P, P, I32, I32, I32, D, P, P]
+    lib.mla_cache_append_rmsnorm_rope.argtypes = [P, P, P, P, P, P, I32, I32, I32, F, F, D, P, P]
     lib.mla_attend_workspace_size.argtypes = [I32, I32, D, ctypes.POINTER(ctypes.c_size_t)]
     lib.mla_attend_absorbed.argtypes = [P, P, P, P, P, P, P, P, P, I32, I32, I32, D, F, P,
                                         ctypes.c_size_t, P, P]
@@ -85,7 +86,8 @@ def load(path: str = LIB_PATH):
     lib.mla_last_error.restype = ctypes.c_char_p
     for name in ("mla_absorb_q", "mla_decode_workspace_size", "mla_decode_paged",
                  "mla_decode_paged_static", "mla_decompress_out", "mla_cache_append",
-                 "mla_attend_workspace_size", "mla_attend_absorbed",
+                 "mla_cache_append_rmsnorm_rope", "mla_attend_workspace_size",
+                 "mla_attend_absorbed",
                  "mla_rope_norm_to_neox_perm", "mla_permute_rope_cols",
                  "mla_permute_rope_rows"):
         getattr(lib, name).restype = ctypes.c_int
@@ -166,6 +168,17 @@ def mla_cache_append(kv_cache, kv_c, k_pe, slot_mapping, n_tokens: int, num_bloc
            load().mla_cache_append(_ptr(kv_cache), _ptr(kv_c), _ptr(k_pe), _ptr(slot_mapping),
                                    n_tokens, num_blocks, src_dtype, ctypes.byref(dims),
                                    _ptr(dev_err), _stream(stream)))
+
+
+def mla_cache_append_rmsnorm_rope(kv_cache, kv_c, k_pe, gamma, positions, slot_mapping,
+                                  n_tokens: int, num_blocks: int, src_dtype: int, eps: float,
+                                  rope_base: float, dims: MlaDims, dev_err=None, stream=None):
+    _check("mla_cache_append_rmsnorm_rope",
+           load().mla_cache_append_rmsnorm_rope(_ptr(kv_cache), _ptr(kv_c), _ptr(k_pe),
+                                                _ptr(gamma), _ptr(positions), _ptr(slot_mapping),
+                                                n_tokens, num_blocks, src_dtype, eps, rope_base,
+                                                ctypes.byref(dims), _ptr(dev_err),
+                                                _stream(stream)))
 
 
 def mla_attend_workspace_size(batch: int, max_blocks: int, dims: MlaDims) -> int:

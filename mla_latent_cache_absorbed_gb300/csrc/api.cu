@@ -1,11 +1,13 @@
 // C ABI of libmla_gb300 (declared in include/mla.h): argument validation,
 // status codes, workspace sizing and dispatch to the kernels.
+#include <math.h>
 #include <cuda_runtime.h>
 #include <stdarg.h>
 #include <stdint.h>
 #include <stdio.h>
 #include <string.h>
 
+#include <cmath>
 #include <vector>
 
 #include "internal.h"
@@ -141,6 +143,44 @@ mla_status mla_cache_append(void* kv_cache, const void* kv_c, const void* k_pe,
     MLA_CUDA_TRY(launch_cache_append(kv_cache, kv_c, k_pe, slot_mapping, n_tokens, num_blocks,
                                      src_dtype, *dims, dev_err, s),
                  "cache append");
+    return MLA_OK;
+}
+
+mla_status mla_cache_append_rmsnorm_rope(void* kv_cache, const void* kv_c, const void* k_pe,
+                                         const void* gamma, const int64_t* positions,
+                                         const int64_t* slot_mapping, int32_t n_tokens,
+                                         int32_t num_blocks, int32_t src_dtype, float eps,
+                                         float rope_base, const mla_dims* dims, int32_t* dev_err,
+                                         void* stream) {
+    g_last_error[0] = 0;
+    if (mla_status st = check_dims(dims)) return st;
+    REQUIRE(n_tokens >= 0 && num_blocks >= 0, "n_tokens and num_blocks must be >= 0");
+    REQUIRE(src_dtype == MLA_F32 || src_dtype == MLA_BF16, "src_dtype must be MLA_F32 or MLA_BF16");
+    REQUIRE(std::isfinite(eps) && eps >= 0.f, "eps must be finite and >= 0");
+    const int P = dims->d_rope;
+    REQUIRE(P == 0 || (std::isfinite(rope_base) && rope_base > 0.f),
+            "rope_base must be finite and > 0");
+    if (n_tokens == 0) return MLA_OK;
+    REQUIRE(kv_cache && kv_c && gamma && slot_mapping,
+            "kv_cache, kv_c, gamma and slot_mapping must be non-NULL");
+    REQUIRE(P == 0 || (k_pe && positions), "k_pe and positions may be NULL only when d_rope == 0");
+    REQUIRE(aligned16(kv_cache) && aligned16(kv_c) && aligned16(gamma) &&
+                ((uintptr_t)slot_mapping & 7u) == 0 && ((uintptr_t)positions & 7u) == 0 &&
+                ((uintptr_t)k_pe & (src_dtype == MLA_BF16 ? 1u : 3u)) == 0,
+            "kv_cache, kv_c and gamma must be 16-byte aligned, slot_mapping and positions "
+            "8-byte aligned, k_pe element aligned");
+    const int piece = dims->dtype == MLA_BF16 ? 8 : 4;
+    if (dims->kv_rank % piece || P % piece) {
+        set_error("cache append: kv_rank and d_rope must be multiples of %d", piece);
+        return MLA_ERR_UNSUPPORTED;
+    }
+    // the rope's per-pair frequency ratio, once, in f32 as the rope is computed
+    const float theta_scale = P > 0 ? powf(rope_base, -2.0f / (float)P) : 1.f;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    MLA_CUDA_TRY(launch_cache_append_rmsnorm_rope(kv_cache, kv_c, k_pe, gamma, positions,
+                                                  slot_mapping, n_tokens, num_blocks, src_dtype,
+                                                  eps, theta_scale, *dims, dev_err, s),
+                 "cache append (rmsnorm, rope)");
     return MLA_OK;
 }
 

@@ -34,6 +34,12 @@ cudaError_t launch_cache_append(void* cache, const void* kv_c, const void* k_pe,
                                 const int64_t* slots, int32_t n_tokens, int32_t num_blocks,
                                 int32_t src_dtype, const mla_dims& d, int32_t* dev_err,
                                 cudaStream_t s);
+cudaError_t launch_cache_append_rmsnorm_rope(void* cache, const void* kv_c, const void* k_pe,
+                                             const void* gamma, const int64_t* positions,
+                                             const int64_t* slots, int32_t n_tokens,
+                                             int32_t num_blocks, int32_t src_dtype, float eps,
+                                             float theta_scale, const mla_dims& d,
+                                             int32_t* dev_err, cudaStream_t s);
 cudaError_t launch_absorb_simt(void* q_abs, const void* q_nope, const void* q_pe,
                                const void* w_uk, int32_t rows, const mla_dims& d,
                                cudaStream_t s);

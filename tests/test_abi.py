@@ -115,3 +115,32 @@ def test_decode_workspace_and_validation(lib):
         N.mla_decode_paged(256, 0, 256, 256, 256, 256, 2, 4, 8, d, float("nan"), 256, n,
                            None, 0)
     N.mla_decode_paged(0, 0, 0, 0, 0, 0, 0, 4, 8, d, 0.2, 0, 0, None, 0)  # empty batch
+
+
+def test_cache_append_rmsnorm_rope_validation(lib):
+    """Argument checks of the fused append, all before any launch."""
+    d = N.MlaDims(4, 16, 8, 16, 32, 1, 16, N.MLA_BF16)
+    f = N.mla_cache_append_rmsnorm_rope
+    ok = dict(eps=1e-6, rope_base=10000.0)
+    # (cache, kv_c, k_pe, gamma, positions, slots): fake aligned addresses, never read
+    a = (256, 512, 768, 1024, 1280, 1536)
+    with pytest.raises(N.MlaError):
+        f(*a, 4, 2, N.MLA_F32, -1.0, 10000.0, d, None, 0)             # eps < 0
+    with pytest.raises(N.MlaError):
+        f(*a, 4, 2, N.MLA_F32, float("nan"), 10000.0, d, None, 0)     # eps NaN
+    with pytest.raises(N.MlaError):
+        f(*a, 4, 2, N.MLA_F32, 1e-6, 0.0, d, None, 0)                 # rope_base <= 0
+    with pytest.raises(N.MlaError):
+        f(256, 512, 768, 0, 1280, 1536, 4, 2, N.MLA_F32, ok["eps"], ok["rope_base"], d, None, 0)  # gamma
+    with pytest.raises(N.MlaError):
+        f(256, 512, 768, 1024, 0, 1536, 4, 2, N.MLA_F32, ok["eps"], ok["rope_base"], d, None, 0)  # positions
+    with pytest.raises(N.MlaError):
+        f(256, 512, 768, 1032, 1280, 1536, 4, 2, N.MLA_F32, ok["eps"], ok["rope_base"], d, None, 0)  # gamma misaligned
+    with pytest.raises(N.MlaError):
+        f(256, 512, 768, 1024, 1284, 1536, 4, 2, N.MLA_F32, ok["eps"], ok["rope_base"], d, None, 0)  # positions misaligned
+    odd = N.MlaDims(4, 16, 4, 16, 32, 1, 16, N.MLA_BF16)     # 4 rope elements: not a 16-byte row
+    with pytest.raises(N.MlaError):
+        f(*a, 4, 2, N.MLA_F32, ok["eps"], ok["rope_base"], odd, None, 0)
+    f(0, 0, 0, 0, 0, 0, 0, 2, N.MLA_F32, ok["eps"], ok["rope_base"], d, None, 0)  # no tokens: no-op
+    nope = N.MlaDims(4, 16, 0, 16, 32, 1, 16, N.MLA_BF16)
+    f(0, 0, 0, 0, 0, 0, 0, 2, N.MLA_F32, ok["eps"], 0.0, nope, None, 0)  # rope_base unused without rope
