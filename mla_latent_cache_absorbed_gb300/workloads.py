@@ -23,6 +23,15 @@ measured on:
                      interleaved (NORM) rope base 10000 whose columns the
                      library's load-time permutation maps to NEOX, seed 4
 
+A sixth workload is the chunked causal prefill in absorbed form, the same
+attention with a block of queries per request:
+
+  glm52_prefill_chunk  GLM-5.2 dims, bf16, t_q=128 (a prompt chunk of 128
+                     tokens, the last 128 positions of each request), B=4,
+                     seq_lens U[129, 8192] with seq_lens[0] = 128 (a first
+                     chunk: t_q == t_kv, query t sees keys 0..t), NEOX rope
+                     base 10000, seed 5
+
 Value recipe (all workloads): q_nope, q_pe, k_pe ~ N(0, 1); c_kv rows ~ N(0, 1)
 then x / sqrt(mean(x^2) + 1e-6) computed in f64; w_uk, w_uv ~ N(0, sd =
 1/sqrt(kv_rank)). Rope angles theta_j = pos * base^(-2j/n) are computed
@@ -100,7 +109,7 @@ class Workload:
 
 
 NAMES = ("tiny_f32", "glm52_decode", "deepseek_decode", "glm53_flash_nope",
-         "glm52_causal_t4")
+         "glm52_causal_t4", "glm52_prefill_chunk")
 
 _GEOMS = {
     "tiny_f32": Geometry(4, 16, 8, 16, 32, 1, "f32"),
@@ -108,10 +117,12 @@ _GEOMS = {
     "deepseek_decode": Geometry(128, 128, 64, 128, 512, 1, "bf16"),
     "glm53_flash_nope": Geometry(64, 256, 0, 256, 512, 1, "bf16"),
     "glm52_causal_t4": Geometry(64, 192, 64, 256, 512, 4, "bf16"),
+    "glm52_prefill_chunk": Geometry(64, 192, 64, 256, 512, 128, "bf16"),
 }
 _SEEDS = {n: i for i, n in enumerate(NAMES)}
 _ROPE = {"tiny_f32": "none", "glm52_decode": "neox", "deepseek_decode": "none",
-         "glm53_flash_nope": "none", "glm52_causal_t4": "norm"}
+         "glm53_flash_nope": "none", "glm52_causal_t4": "norm",
+         "glm52_prefill_chunk": "neox"}
 
 
 def geometry(name: str) -> Geometry:
@@ -131,6 +142,9 @@ def default_seq_lens(name: str, rng: np.random.Generator) -> np.ndarray:
         s = np.clip(s, 1, 32768)
     elif name == "glm52_causal_t4":
         s = rng.integers(8192, 65537, size=32)
+    elif name == "glm52_prefill_chunk":
+        s = rng.integers(129, 8193, size=4)
+        s[0] = 128
     else:
         raise KeyError(name)
     return s.astype(np.int32)

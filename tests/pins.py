@@ -21,7 +21,10 @@ AssertionError when the oracle disagrees with:
     reported;
   * the KV half of the MLA prolog of the "aclnnMlaProlog" page (RmsNorm of
     the latent, rope of k^R at each token's position, then the same scatter):
-    closed forms of the norm and an f64 rotation for the rope.
+    closed forms of the norm and an f64 rotation for the rope;
+  * chunked causal prefill: a block of queries per request is causal
+    attention (torch's SDPA with a causal mask), and each of its queries the
+    one-query decode of the request cut at that query's position.
 """
 from __future__ import annotations
 
@@ -576,9 +579,58 @@ def check_kv_prolog(lib):
         pass
 
 
+def check_causal_prefill(lib):
+    """A chunk of t_q queries per request (chunked prefill in absorbed form,
+    the queries being the request's last t_q positions):
+      * a first chunk (t_q == t_kv) is ordinary causal self-attention over the
+        whole rows: torch's SDPA with is_causal (f64) on the gathered rows
+        gives the output, and logsumexp of the causally masked scaled scores
+        the LSE;
+      * a later chunk (t_q < t_kv): the same with the mask aligned to the
+        chunk's end (query t sees keys 0 .. t_kv - t_q + t), built from
+        torch.tril with a diagonal offset;
+      * query t of a chunk is the one-query decode of the same request cut to
+        its first t_kv - t_q + t + 1 rows, bit for bit."""
+    import torch
+    rng = np.random.default_rng(21)
+    H, R, P = 2, 32, 8
+    W = R + P
+    scale = 1.0 / math.sqrt(24)
+    for T, lens in [(24, [24, 24]), (20, [45, 20, 33])]:
+        rows = [rng.standard_normal((s, W)).astype(np.float32) for s in lens]
+        cache, bt = page(rows, lens, rng)
+        sl = np.array(lens, np.int32)
+        q = rng.standard_normal((len(lens), T, H, W)).astype(np.float32)
+        o, lse = oracle.decode_paged(q, cache, bt, sl, T, R, scale, lib=lib)
+        for b, S in enumerate(lens):
+            qt = torch.from_numpy(q[b].astype(np.float64)).permute(1, 0, 2)[None]   # [1,H,T,W]
+            kt = torch.from_numpy(rows[b].astype(np.float64))[None, None].expand(1, H, S, W)
+            vt = kt[..., :R]
+            if S == T:
+                ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=scale,
+                                                                       is_causal=True)
+            mask = torch.tril(torch.ones(T, S, dtype=torch.bool), diagonal=S - T)
+            if S != T:
+                ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=scale,
+                                                                       attn_mask=mask)
+            sc = (qt @ kt.transpose(-1, -2)) * scale
+            ref_lse = torch.logsumexp(sc.masked_fill(~mask, float("-inf")), -1)
+            ref = ref[0].permute(1, 0, 2).numpy()          # [T,H,R]
+            ref_lse = ref_lse[0].permute(1, 0).numpy()     # [T,H]
+            assert maxdiff(ref, o[b]) <= 3e-6, (T, S, maxdiff(ref, o[b]))
+            assert maxdiff(ref_lse, lse[b]) <= 3e-6, (T, S, maxdiff(ref_lse, lse[b]))
+            for t in (0, T // 2, T - 1):
+                cut = np.array([S - T + t + 1], np.int32)
+                o1, l1 = oracle.decode_paged(q[b:b + 1, t:t + 1], cache, bt[b:b + 1], cut, 1, R,
+                                             scale, lib=lib)
+                assert np.array_equal(o1[0, 0], o[b, t]) and np.array_equal(l1[0, 0], lse[b, t]), \
+                    (T, S, t)
+
+
 QUICK_CHECKS = [check_naive_equals_absorbed, check_paged_chain_equals_naive,
                 check_bruteforce_f64, check_sdpa_reduction, check_closed_forms,
                 check_split_combine, check_paged_equals_contiguous,
                 check_decode_rows_consistent, check_invalid_requests,
                 check_absorb_decompress_unit_weights, check_rope_permutation,
-                check_rope_against_rotation, check_cache_append, check_kv_prolog]
+                check_rope_against_rotation, check_cache_append, check_kv_prolog,
+                check_causal_prefill]

@@ -32,6 +32,8 @@ MUTANTS = [
      "p * load_elem(kv_cache, kv_dtype, entry + W - 1 - d);", 0),
     ("decode_horizon_off_by_one", "horizon = seq_len - t_q + t + 1;",
      "horizon = seq_len - t_q + t;", 0),
+    ("decode_horizon_from_chunk_start", "horizon = seq_len - t_q + t + 1;",
+     "horizon = t + 1;", 0),
     ("decode_row_in_block_reversed", "(j % block_size)) * W;",
      "(block_size - 1 - j % block_size)) * W;", 0),
     ("decode_lse_no_log", "*lse_out = l > 0.0f ? m + logf(l) : -INFINITY;",

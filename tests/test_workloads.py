@@ -44,7 +44,7 @@ def test_bf16_values_are_exact_bf16():
     assert wl.block_table[1, 0] == -1
 
 
-@pytest.mark.parametrize("name", ["glm52_decode", "glm52_causal_t4"])
+@pytest.mark.parametrize("name", ["glm52_decode", "glm52_causal_t4", "glm52_prefill_chunk"])
 def test_rope_positions(name):
     """Roped query/key dot products depend only on the position difference."""
     wl = W.make_workload(name, seq_lens=[20, 33], poison="none")
@@ -96,3 +96,5 @@ def test_default_seq_len_recipes():
     assert 1000 < np.median(s) < 4000
     s = W.default_seq_lens("glm52_causal_t4", np.random.default_rng(4))
     assert s.min() >= 8192 and s.max() <= 65536
+    s = W.default_seq_lens("glm52_prefill_chunk", np.random.default_rng(5))
+    assert s.shape == (4,) and s[0] == 128 and s[1:].min() >= 129 and s.max() <= 8192
