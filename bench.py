@@ -527,9 +527,11 @@ def measure_cache_append(wl, dc, stream, hbm_peak):
 
 def LAUNCHES_PER_STEP(wl):
     """Kernels of this library launched per fused step: absorb, decode and the
-    decompress that merges the split rows (bf16); the f32 path runs its
-    combine as a fourth kernel."""
-    return 3 if wl.geom.dtype == "bf16" else 4
+    decompress that merges the split rows (bf16, up to 256 query rows per
+    request); the f32 path and larger query blocks (prefill chunks) run the
+    decode's combine as a fourth kernel."""
+    g = wl.geom
+    return 3 if g.dtype == "bf16" and g.t_q * g.n_head <= 256 else 4
 
 
 def run_e2e(args, wl, layers, stream, nl, steps):

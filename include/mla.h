@@ -201,9 +201,10 @@ mla_status mla_attend_workspace_size(int32_t batch, int32_t max_blocks,
  *   o_lat, lse = mla_decode_paged(q_abs, kv_cache, ...)
  *   out = mla_decompress_out(o_lat, w_uv)
  * with the same results (the same bits) as those three calls. On the bf16
- * tensor-core path the decompress also merges the decode's split rows (the
- * combine) while it streams W_UV, and the decode starts its cache stream
- * while the absorb finishes.
+ * tensor-core path, for up to 256 query rows per request (t_q * n_head), the
+ * decompress also merges the decode's split rows (the combine) while it
+ * streams W_UV, and the decode starts its cache stream while the absorb
+ * finishes; larger query blocks (prefill chunks) run the three calls.
  * out         [B][t_q][H][Dv]  out, dims->dtype
  * lse         [B][t_q][H] f32  out; may be NULL
  * q_nope      [B][t_q][H][Dn], q_pe [B][t_q][H][P] (NULL when P == 0)

@@ -203,13 +203,29 @@ mla_status mla_decompress_out(void* out, const void* o_lat, const void* w_uv, in
     return MLA_OK;
 }
 
+namespace {
+// The bf16 tensor-core decode gives each row group of a request (128 of its
+// t_q * n_head query rows) a set of CTA pairs of its own, so it serves a
+// geometry only while the row groups number no more than the pairs of its
+// grid on this device (76 pairs on 152 SMs: up to 9728 query rows per
+// request). Larger query blocks, such as long prefill chunks, take the SIMT
+// decode.
+bool use_tc_decode(const mla_dims& d) {
+    if (d.dtype != MLA_BF16 || !tc_decode_supported(d)) return false;
+    size_t bytes = 0;
+    if (tc_decode_workspace(1, 1, d, &bytes) != cudaSuccess) return false;
+    const long long pairs = (long long)(bytes / kTcDecodeBytesPerPair);
+    return ((long long)d.t_q * d.n_head + 127) / 128 <= pairs;
+}
+}  // namespace
+
 mla_status mla_decode_workspace_size(int32_t batch, int32_t max_blocks, const mla_dims* dims,
                                      size_t* bytes) {
     g_last_error[0] = 0;
     if (mla_status st = check_dims(dims)) return st;
     REQUIRE(bytes, "bytes must be non-NULL");
     REQUIRE(batch >= 0 && max_blocks >= 1, "batch >= 0 and max_blocks >= 1 required");
-    if (dims->dtype == MLA_BF16 && tc_decode_supported(*dims)) {
+    if (use_tc_decode(*dims)) {
         size_t b = 0;
         MLA_CUDA_TRY(tc_decode_workspace(batch, max_blocks, *dims, &b), "decode workspace");
         *bytes = b;
@@ -241,7 +257,7 @@ mla_status mla_decode_paged(void* out, float* lse, const void* q_abs, const void
     REQUIRE(workspace_bytes >= need, "workspace too small: %zu bytes given, %zu needed",
             workspace_bytes, need);
     cudaStream_t s = (cudaStream_t)stream;
-    if (dims->dtype == MLA_BF16 && tc_decode_supported(*dims)) {
+    if (use_tc_decode(*dims)) {
         MLA_CUDA_TRY(launch_decode_tc(out, lse, q_abs, kv_cache, block_table, seq_lens, batch,
                                       max_blocks, num_blocks, *dims, scale, workspace, dev_err,
                                       s, /*early=*/false, /*combine=*/true),
@@ -309,7 +325,15 @@ mla_status mla_attend_absorbed(void* out, float* lse, const void* q_nope, const 
     const size_t dws_bytes = workspace_bytes - (size_t)(static_cast<char*>(dws) - ws);
     cudaStream_t s = (cudaStream_t)stream;
     DecodeSplitInfo info = {};
-    if (dims->dtype == MLA_BF16 && tc_decode_supported(*dims) &&
+    // The merging decompress finds each of its rows' split parts through the
+    // row group the row belongs to; the 128 rows of one of its CTAs (128
+    // query positions of one head) fall in up to 128 row groups of the
+    // decode, and with many row groups per request those lookups outweigh
+    // the combine they replace (a 128-query chunk of 64 heads: 619 us fused
+    // against 374 us for the three stages). Up to two row groups of queries
+    // per request take the fused chain, larger query blocks the three calls.
+    const bool few_row_groups = (long long)dims->t_q * dims->n_head <= 256;
+    if (few_row_groups && use_tc_decode(*dims) &&
         tc_gemm_supported(*dims, rows, /*absorb=*/true) &&
         tc_decode_split_info(*dims, dws, &info) == cudaSuccess &&
         tc_merge_supported(*dims, rows, info.NP)) {

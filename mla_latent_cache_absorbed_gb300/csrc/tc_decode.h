@@ -31,6 +31,10 @@ struct DecodeSplitInfo {
     float* ws_lse;  // [2 NP][128]
 };
 cudaError_t tc_decode_split_info(const mla_dims& d, void* workspace, DecodeSplitInfo* info);
+// Workspace bytes per CTA pair of the decode's grid: two partial slots of
+// 128 rows x 512 bf16 and their 128 f32 LSEs (tc_decode_workspace is the
+// pairs times this).
+constexpr size_t kTcDecodeBytesPerPair = 2 * (128 * 512 * 2 + 128 * 4);
 
 // True when the bf16 tensor-core absorb (absorb = true) or decompress GEMM
 // serves this geometry and row count.
