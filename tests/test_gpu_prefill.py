@@ -119,7 +119,9 @@ def test_prefill_chunk_workload_sampled():
                                            ("glm52_prefill_chunk", 128, None)])
 def test_fused_chunk_equals_three_calls(name, t_q, lens):
     """mla_attend_absorbed on a chunk gives the bits of absorb -> decode ->
-    decompress (the merging decompress handles every row group's parts)."""
+    decompress. With more than 256 query rows per request the fused call runs
+    those three calls itself (the merging decompress would look up the split
+    parts of up to 128 row groups per CTA), so this pins that dispatch."""
     wl = (W.make_workload(name) if lens is None else chunk_workload(name, t_q, lens))
     _, ref, got = attend.three_then_fused(wl)
     assert ref[2] == 0
