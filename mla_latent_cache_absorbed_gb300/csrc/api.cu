@@ -124,6 +124,7 @@ mla_status mla_cache_append(void* kv_cache, const void* kv_c, const void* k_pe,
                             const int64_t* slot_mapping, int32_t n_tokens, int32_t num_blocks,
                             int32_t src_dtype, const mla_dims* dims, int32_t* dev_err,
                             void* stream) {
+    g_last_error[0] = 0;
     if (mla_status st = check_dims(dims)) return st;
     REQUIRE(n_tokens >= 0 && num_blocks >= 0, "n_tokens and num_blocks must be >= 0");
     REQUIRE(src_dtype == MLA_F32 || src_dtype == MLA_BF16, "src_dtype must be MLA_F32 or MLA_BF16");
@@ -204,6 +205,18 @@ mla_status mla_decompress_out(void* out, const void* o_lat, const void* w_uv, in
 }
 
 namespace {
+// Index limits of the decode kernels: query rows (batch * t_q * n_head) and
+// cache positions (max_blocks * 16) are 32-bit counts.
+mla_status check_decode_shape(int32_t batch, int32_t max_blocks, const mla_dims& d) {
+    if ((long long)batch * d.t_q * d.n_head > INT32_MAX || max_blocks >= (1 << 27)) {
+        set_error("decode: batch * t_q * n_head = %lld query rows (at most 2^31 - 1) and "
+                  "max_blocks = %d (below 2^27) are supported",
+                  (long long)batch * d.t_q * d.n_head, max_blocks);
+        return MLA_ERR_UNSUPPORTED;
+    }
+    return MLA_OK;
+}
+
 // The bf16 tensor-core decode gives each row group of a request (128 of its
 // t_q * n_head query rows) a set of CTA pairs of its own, so it serves a
 // geometry only while the row groups number no more than the pairs of its
@@ -225,6 +238,7 @@ mla_status mla_decode_workspace_size(int32_t batch, int32_t max_blocks, const ml
     if (mla_status st = check_dims(dims)) return st;
     REQUIRE(bytes, "bytes must be non-NULL");
     REQUIRE(batch >= 0 && max_blocks >= 1, "batch >= 0 and max_blocks >= 1 required");
+    if (mla_status st = check_decode_shape(batch, max_blocks, *dims)) return st;
     if (use_tc_decode(*dims)) {
         size_t b = 0;
         MLA_CUDA_TRY(tc_decode_workspace(batch, max_blocks, *dims, &b), "decode workspace");

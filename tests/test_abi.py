@@ -115,6 +115,18 @@ def test_decode_workspace_and_validation(lib):
         N.mla_decode_paged(256, 0, 256, 256, 256, 256, 2, 4, 8, d, float("nan"), 256, n,
                            None, 0)
     N.mla_decode_paged(0, 0, 0, 0, 0, 0, 0, 4, 8, d, 0.2, 0, 0, None, 0)  # empty batch
+    # 32-bit index limits: query rows and cache positions
+    big = N.MlaDims(4, 16, 8, 16, 32, 1 << 20, 16, N.MLA_F32)
+    with pytest.raises(N.MlaError) as e:
+        N.mla_decode_workspace_size(1024, 4, big)    # 2^32 query rows
+    assert e.value.status == 2 and "query rows" in N.mla_last_error()
+    with pytest.raises(N.MlaError) as e:
+        N.mla_attend_workspace_size(1024, 4, big)
+    assert e.value.status == 2
+    with pytest.raises(N.MlaError) as e:
+        N.mla_decode_workspace_size(2, 1 << 27, d)
+    assert e.value.status == 2
+    assert N.mla_decode_workspace_size(2, (1 << 27) - 1, d) > 0
 
 
 def test_cache_append_rmsnorm_rope_validation(lib):
