@@ -1,0 +1,83 @@
+"""The bench's roofline numerators and launch counts, on CPU.
+
+The roofline fraction divides algorithmic work by a measured time, so the
+work must be what the method needs and no more: every cache row once per
+request, the queries, the latent output and the LSE; and QK plus PV flops
+over the keys each query row can see (the causal horizon seq_len - t_q + t + 1
+of query t). These tests count both by brute force on small workloads.
+"""
+import numpy as np
+import pytest
+
+import bench
+from mla_latent_cache_absorbed_gb300 import workloads as W
+
+
+def brute_force(wl):
+    g = wl.geom
+    e = 2 if g.dtype == "bf16" else 4
+    H, R, Wd, T = g.n_head, g.kv_rank, g.width, g.t_q
+    cache = sum(int(s) for s in wl.seq_lens) * Wd * e
+    visible = 0
+    for s in wl.seq_lens:
+        for t in range(T):
+            if s > 0:
+                visible += int(s) - T + t + 1            # keys 0 .. s - T + t
+    rows = wl.batch * T
+    dec_bytes = cache + rows * H * (Wd * e + R * e + 4)
+    dec_flops = 2 * H * visible * (Wd + R)              # QK over Wd, PV over R
+    return dec_bytes, dec_flops
+
+
+@pytest.mark.parametrize("name,t_q,lens", [
+    ("tiny_f32", 1, [37, 64]),
+    ("glm52_decode", 1, [5, 0, 40]),
+    ("glm52_decode", 4, [4, 9, 100]),
+    ("glm52_decode", 16, [16, 17, 0]),
+    ("glm53_flash_nope", 2, [2, 33]),
+])
+def test_decode_work_matches_brute_force(name, t_q, lens):
+    g = W.geometry(name)
+    geom = W.Geometry(g.n_head, g.d_nope, g.d_rope, g.d_v, g.kv_rank, t_q, g.dtype)
+    wl = W.make_workload(name, seq_lens=lens, geom=geom)
+    alg = bench.algorithmic(wl)
+    assert alg["decode"] == brute_force(wl)
+    e = 2 if g.dtype == "bf16" else 4
+    rows = wl.batch * t_q
+    H, R, Dn, Dv, P = g.n_head, g.kv_rank, g.d_nope, g.d_v, g.d_rope
+    assert alg["absorb"] == (H * Dn * R * e + rows * H * (Dn + P) * e + rows * H * (R + P) * e,
+                             2 * rows * H * Dn * R)
+    assert alg["decompress"] == (H * Dv * R * e + rows * H * R * e + rows * H * Dv * e,
+                                 2 * rows * H * R * Dv)
+
+
+def test_first_chunk_flops_are_triangular():
+    """A first prefill chunk (t_q == seq_len = n) sees 1 + 2 + ... + n keys."""
+    n = 48
+    g = W.geometry("glm52_decode")
+    geom = W.Geometry(g.n_head, g.d_nope, g.d_rope, g.d_v, g.kv_rank, n, g.dtype)
+    wl = W.make_workload("glm52_decode", seq_lens=[n], geom=geom)
+    _, flops = bench.algorithmic(wl)["decode"]
+    assert flops == 2 * g.n_head * (n * (n + 1) // 2) * (g.width + g.kv_rank)
+
+
+def test_launches_per_step():
+    """Three kernels per fused bf16 step (absorb, decode, merging decompress)
+    up to 256 query rows per request; the combine is a fourth otherwise, and
+    on the f32 path."""
+    assert bench.LAUNCHES_PER_STEP(W.make_workload("glm52_decode", seq_lens=[5])) == 3
+    assert bench.LAUNCHES_PER_STEP(W.make_workload("glm52_causal_t4", seq_lens=[5])) == 3
+    assert bench.LAUNCHES_PER_STEP(W.make_workload("glm52_prefill_chunk")) == 4
+    assert bench.LAUNCHES_PER_STEP(W.make_workload("tiny_f32")) == 4
+
+
+def test_named_workload_work():
+    """The bench's numbers for every named workload are the brute-force
+    counts: the small ones at full size, the large ones on their first three
+    requests (the recipe's lengths, seeded)."""
+    large = ("deepseek_decode", "glm52_causal_t4", "glm53_flash_nope")
+    for name in W.NAMES:
+        lens = None if name not in large else \
+            W.default_seq_lens(name, np.random.default_rng(0))[:3]
+        wl = W.make_workload(name, seq_lens=lens)
+        assert bench.algorithmic(wl)["decode"] == brute_force(wl), name
