@@ -1,6 +1,6 @@
 """Parity of the CUDA path (through the C ABI) with the CPU oracle.
 
-Tolerances (spec gates, written here):
+Tolerances (the parity gates, written here):
   f32 inputs   every output and LSE: max abs diff <= 1e-4
   bf16 inputs  outputs: |gpu - ref| <= 1e-2 + 2^-8 |ref| (the second term is
                the storage quantum of a bf16 output, which a flat 1e-2 cannot
