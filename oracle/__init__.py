@@ -65,6 +65,7 @@ _D = ctypes.c_double
 
 def _declare(lib):
     lib.oracle_absorb_q.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I]
+    lib.oracle_absorb_q_rope.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F]
     lib.oracle_decode_range.argtypes = [_P, _P, _P, _I, _P, _I, _P, _I, _I, _I,
                                         _I, _I, _I, _I, _I, _F, _I, _I, _P, _P]
     lib.oracle_decode_rows.argtypes = [_P, _P, _P, _I, _P, _I, _P, _P, _I, _I, _I,
@@ -140,6 +141,26 @@ def absorb_q(q_nope, q_pe, w_uk, lib=None) -> np.ndarray:
     out = np.empty((rows, H, R + P), np.float32)
     _check(lib.oracle_absorb_q(_ptr(out), _ptr(q_nope), _ptr(q_pe), _ptr(w_uk),
                                rows, H, Dn, P, R), False)
+    return out
+
+
+def absorb_q_rope(q_nope, q_pe, w_uk, positions, rope_base, lib=None) -> np.ndarray:
+    """The query half of the "aclnnMlaProlog" page as the decode consumes it:
+    q_abs[r,h] = [w_uk[h]^T q_nope[r,h] | NEOX rope of q_pe[r,h] at
+    positions[r]] (mla.rs rope_neox, f32).
+
+    q_nope [rows, H, Dn], q_pe [rows, H, P] (before the rope), w_uk [H, Dn, R],
+    positions [rows] int -> [rows, H, R+P].
+    """
+    lib = lib or load()
+    q_nope, q_pe, w_uk = _f32(q_nope), _f32(q_pe), _f32(w_uk)
+    rows, H, Dn = q_nope.shape
+    P = q_pe.shape[2]
+    R = w_uk.shape[2]
+    pos = np.ascontiguousarray(np.asarray(positions, np.int64).reshape(rows))
+    out = np.empty((rows, H, R + P), np.float32)
+    _check(lib.oracle_absorb_q_rope(_ptr(out), _ptr(q_nope), _ptr(q_pe), _ptr(w_uk), _ptr(pos),
+                                    rows, H, Dn, P, R, float(rope_base)), False)
     return out
 
 

@@ -39,6 +39,10 @@
  *   oracle_cache_append    the vLLM CPU MLA page, CPUMLAImpl.do_kv_cache_update
  *                          (scatter of [kv_c | k_pe] rows by slot mapping,
  *                          padding slots -1 skipped, cast to the cache type).
+ *   oracle_absorb_q_rope   the "aclnnMlaProlog" page, computation formulas of
+ *                          the query (q^N = q^C W^UK; q^R = ROPE(c^Q W^QR)):
+ *                          the absorb above with the mla.rs NEOX rope of the
+ *                          query's rope part at the row's position.
  *   oracle_kv_prolog_row / oracle_cache_append_rmsnorm_rope
  *                          the "aclnnMlaProlog" page, computation formulas of
  *                          the key (RmsNorm of the latent, rope of k^R, both
@@ -469,6 +473,32 @@ int oracle_norm_to_neox_perm(int n_dims, int32_t* perm) {
         perm[2 * j] = j;
         perm[2 * j + 1] = j + half;
     }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Query half of the MLA prolog, as the decode consumes it ("aclnnMlaProlog"  */
+/* page, computation formulas of the query)                                   */
+/* ------------------------------------------------------------------------- */
+/* q_abs[r][h] = [q^N | q^R] for query row r and head h:
+ *   q^N = q_nope[r][h] W^UK[h]  (q_nope is q^C = c^Q W^UQ, one head's slice;
+ *                                the absorb of oracle_absorb_q)
+ *   q^R = the mla.rs NEOX rope of q_pe[r][h] (= c^Q W^QR before the rope,
+ *         whose columns carry the load-time permutation) at positions[r], in
+ *         f32 as that page computes it: the same rope as the key half's, so
+ *         that q^R . k^R depends only on the distance of the two positions. */
+int oracle_absorb_q_rope(float* q_abs, const float* q_nope, const float* q_pe,
+                         const float* w_uk, const int64_t* positions, int rows, int n_head,
+                         int d_nope, int d_rope, int kv_rank, float rope_base) {
+    if ((d_rope & 1) || (d_rope > 0 && !(rope_base > 0.0f))) return ORACLE_BAD_ARG;
+    const int st = oracle_absorb_q(q_abs, q_nope, q_pe, w_uk, rows, n_head, d_nope, d_rope,
+                                   kv_rank);
+    if (st != ORACLE_OK || d_rope == 0) return st;
+    const int W = kv_rank + d_rope;
+    for (int r = 0; r < rows; ++r)
+        for (int h = 0; h < n_head; ++h)
+            oracle_rope_neox(q_abs + ((int64_t)r * n_head + h) * W + kv_rank, d_rope,
+                             (float)positions[r], rope_base);
     return ORACLE_OK;
 }
 

@@ -22,6 +22,8 @@ AssertionError when the oracle disagrees with:
   * the KV half of the MLA prolog of the "aclnnMlaProlog" page (RmsNorm of
     the latent, rope of k^R at each token's position, then the same scatter):
     closed forms of the norm and an f64 rotation for the rope;
+  * the query half of the MLA prolog: the absorb with the query's rope at
+    each row's position, the same rotation as the key half's;
   * chunked causal prefill: a block of queries per request is causal
     attention (torch's SDPA with a causal mask), and each of its queries the
     one-query decode of the request cut at that query's position.
@@ -627,10 +629,64 @@ def check_causal_prefill(lib):
                     (T, S, t)
 
 
+def check_q_prolog(lib):
+    """Query half of the MLA prolog ("aclnnMlaProlog" page, query formulas)
+    as the decode consumes it, q_abs = [q^C W^UK | ROPE(c^Q W^QR)]:
+      * the latent part is the absorb of q^C, bit for bit, and a head whose
+        W^UK is the identity on its first d_nope columns returns q^C there;
+      * the rope part is the f64 rotation of each row at its own position
+        (identity at position 0), per head;
+      * q^R . k^R with the key half's rope (oracle_kv_prolog_row) depends
+        only on the distance of the two positions: the query and the key
+        are turned by the same convention;
+      * with no rope columns it is the absorb."""
+    import oracle as O
+    rng = np.random.default_rng(31)
+    rows, H, Dn, P, R = 5, 3, 8, 16, 24
+    base = 10000.0
+    qn = rng.standard_normal((rows, H, Dn)).astype(np.float32)
+    qp = rng.standard_normal((rows, H, P)).astype(np.float32)
+    w = (rng.standard_normal((H, Dn, R)) / math.sqrt(R)).astype(np.float32)
+    w[1] = 0.0
+    w[1][np.arange(Dn), np.arange(Dn)] = 1.0                  # head 1: W^UK = [I | 0]
+    pos = np.array([0, 1, 17, 4095, 70000], np.int64)
+    out = O.absorb_q_rope(qn, qp, w, pos, base, lib=lib)
+    plain = O.absorb_q(qn, qp, w, lib=lib)
+    assert np.array_equal(out[:, :, :R], plain[:, :, :R])
+    assert np.array_equal(out[:, 1, :Dn], qn[:, 1]) and np.all(out[:, 1, Dn:R] == 0)
+    assert np.array_equal(out[0, :, R:], qp[0])                # position 0: no turn
+    # the rope takes theta_j = pos * base^(-2j/P) by j f32 multiplications of
+    # the f32 ratio: |theta error| <= theta_j (j + 2) 2^-23; with sin/cos and
+    # the rotation's own f32 rounding, a pair (a, b) is off by at most
+    # (|a| + |b|) (theta error + 1e-6)
+    h2 = P // 2
+    j = np.arange(h2)
+    for r in range(rows):
+        th = float(pos[r]) * base ** (-2.0 * j / P)
+        dth = th * (j + 2) * 2.0 ** -23
+        for h in range(H):
+            ref = _rotation_f64(qp[r, h], pos[r], base)
+            ab = np.abs(qp[r, h, :h2]).astype(np.float64) + np.abs(qp[r, h, h2:])
+            bound = np.tile(ab * (dth + 1e-6), 2)
+            assert np.all(np.abs(out[r, h, R:] - ref) <= bound), (r, h)
+    # relative positions: (query at p + d) . (key at p) is the same for every p
+    k = rng.standard_normal((1, P)).astype(np.float32)
+    ones = np.ones(R, np.float32)
+    kv = np.ones((1, R), np.float32)
+    dots = []
+    for p0 in (0, 5, 300):
+        q_at = O.absorb_q_rope(qn[:1, :1], qp[:1, :1], w[:1], [p0 + 7], base, lib=lib)[0, 0, R:]
+        k_at = O.kv_prolog_rows(kv, k, ones, [p0], 0.0, base, lib=lib)[0, R:]
+        dots.append(float(np.dot(q_at.astype(np.float64), k_at)))
+    assert max(dots) - min(dots) <= 1e-4 * max(1.0, abs(dots[0])), dots
+    nope = O.absorb_q_rope(qn, qp[:, :, :0], w, pos, base, lib=lib)
+    assert np.array_equal(nope, O.absorb_q(qn, qp[:, :, :0], w, lib=lib))
+
+
 QUICK_CHECKS = [check_naive_equals_absorbed, check_paged_chain_equals_naive,
                 check_bruteforce_f64, check_sdpa_reduction, check_closed_forms,
                 check_split_combine, check_paged_equals_contiguous,
                 check_decode_rows_consistent, check_invalid_requests,
                 check_absorb_decompress_unit_weights, check_rope_permutation,
                 check_rope_against_rotation, check_cache_append, check_kv_prolog,
-                check_causal_prefill]
+                check_causal_prefill, check_q_prolog]

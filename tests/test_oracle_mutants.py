@@ -61,6 +61,11 @@ MUTANTS = [
      "const int64_t s = slots[n] < 0 ? 0 : slots[n];", 0),
     ("append_rope_from_kv", "(int64_t)n * d_rope + (j - kv_rank));",
      "(int64_t)n * kv_rank + (j - kv_rank));", 0),
+    ("q_prolog_rope_skipped", "(float)positions[r], rope_base);", "(float)0, rope_base);", 0),
+    ("q_prolog_row0_position", "(float)positions[r], rope_base);",
+     "(float)positions[0], rope_base);", 0),
+    ("q_prolog_head0_rope", "oracle_rope_neox(q_abs + ((int64_t)r * n_head + h) * W + kv_rank,",
+     "oracle_rope_neox(q_abs + ((int64_t)r * n_head) * W + kv_rank,", 0),
     ("prolog_norm_sum_not_mean", "sqrt(ss / (double)kv_rank + eps)", "sqrt(ss + eps)", 0),
     ("prolog_norm_drops_eps", "sqrt(ss / (double)kv_rank + eps)", "sqrt(ss / (double)kv_rank)", 0),
     ("prolog_norm_no_gamma", "row[i] = g * x / rms;", "row[i] = x / rms;", 0),
