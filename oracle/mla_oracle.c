@@ -7,10 +7,11 @@
  * leg do. It shares no code, header or constant with the CUDA library.
  *
  * Precision: f32 storage and f32 accumulation, one sequential summation per
- * dot product, exactly as the pages fix it ("memra_engine/mla.rs" source,
- * module docs: plain CPU f32; "vllm.cpp cpu_mla_attn.cpp", header comment:
- * accumulation is f32 throughout). Built with -ffp-contract=off so that no
- * multiply-add is fused and x86 and Arm builds sum identically.
+ * dot product, as the pages fix it (the "memra_engine/mla.rs" module docs
+ * describe their oracle as f32 code on the CPU; the header comment of
+ * "vllm.cpp cpu_mla_attn.cpp" has every sum in f32). Built with
+ * -ffp-contract=off so that no multiply-add is fused and x86 and Arm builds
+ * sum identically.
  *
  * Every function is a direct restatement of one passage:
  *   oracle_absorb_q        mla.rs, fn mla_attend_absorbed, absorb step
