@@ -75,6 +75,23 @@ static float load_elem(const void* base, int dtype, int64_t i) {
     return f;
 }
 
+/* sum_k x[k sx] y[k sy] for k = 0 .. n-1, added in index order onto `start`,
+ * each product rounded before it is added. Every f32 dot product of this
+ * file is this one summation. */
+static float dot_from(float start, const float* x, int64_t sx, const float* y, int64_t sy,
+                      int n) {
+    float s = start;
+    for (int k = 0; k < n; ++k) s += x[k * sx] * y[k * sy];
+    return s;
+}
+
+/* the same over a row of a typed buffer: sum_d q[d] * base[off + d] */
+static float dot_elem(const float* q, const void* base, int dtype, int64_t off, int n) {
+    float s = 0.0f;
+    for (int d = 0; d < n; ++d) s += q[d] * load_elem(base, dtype, off + d);
+    return s;
+}
+
 /* ------------------------------------------------------------------------- */
 /* absorb: q_abs[r][h][0:R] = w_uk[h]^T q_nope[r][h]; q_abs[r][h][R:R+P] = q_pe */
 /* ------------------------------------------------------------------------- */
@@ -84,20 +101,16 @@ int oracle_absorb_q(float* q_abs, const float* q_nope, const float* q_pe,
     if (rows < 0 || n_head <= 0 || d_nope <= 0 || d_rope < 0 || kv_rank <= 0)
         return ORACLE_BAD_ARG;
     const int W = kv_rank + d_rope;
-    for (int r = 0; r < rows; ++r) {
-        for (int h = 0; h < n_head; ++h) {
-            const float* qn = q_nope + ((int64_t)r * n_head + h) * d_nope;
-            const float* wuk = w_uk + (int64_t)h * d_nope * kv_rank;
-            float* dst = q_abs + ((int64_t)r * n_head + h) * W;
-            for (int l = 0; l < kv_rank; ++l) dst[l] = 0.0f;
-            for (int p = 0; p < d_nope; ++p) {
-                const float qv = qn[p];
-                const float* wrow = wuk + (int64_t)p * kv_rank;
-                for (int l = 0; l < kv_rank; ++l) dst[l] += qv * wrow[l];
-            }
-            const float* qp = q_pe + ((int64_t)r * n_head + h) * d_rope;
-            for (int j = 0; j < d_rope; ++j) dst[kv_rank + j] = qp[j];
-        }
+    /* one (row, head) pair at a time, row-major like the buffers */
+    for (int64_t rh = 0; rh < (int64_t)rows * n_head; ++rh) {
+        const int h = (int)(rh % n_head);
+        const float* w_h = w_uk + (int64_t)h * d_nope * kv_rank; /* [d_nope][kv_rank] */
+        const float* q = q_nope + rh * d_nope;
+        float* dst = q_abs + rh * W;
+        /* q_lat[l]: the query against column l of w_uk[h] */
+        for (int l = 0; l < kv_rank; ++l) dst[l] = dot_from(0.0f, q, 1, w_h + l, kv_rank, d_nope);
+        /* the rope part rides along as it is */
+        memcpy(dst + kv_rank, q_pe + rh * d_rope, (size_t)d_rope * sizeof(float));
     }
     return ORACLE_OK;
 }
@@ -116,6 +129,49 @@ int oracle_absorb_q(float* q_abs, const float* q_nope, const float* q_pe,
  * o_out     : kv_rank values = acc / l (zeros when nothing was visible)
  * lse_out   : m + ln l, or -inf when nothing was visible
  */
+/* Single-pass softmax state (cpu_mla_attn.cpp, MlaDecodeAttentionKernel):
+ * the largest scaled score taken so far, the sum of exp(score - largest), and
+ * the matching weighted sum of value rows. */
+typedef struct {
+    float top;   /* running maximum; -inf before the first key */
+    float mass;  /* sum of exp(score - top) */
+    float* acc;  /* sum of exp(score - top) * value row, n entries */
+    int n;
+} run_softmax;
+
+/* Take one key: its scaled score s and its value row, n entries of `base`
+ * from element `off`. When the maximum grows, everything summed so far is
+ * scaled by exp(old top - new top); while nothing has been summed (old top
+ * -inf) that factor is 0, never exp(-inf + inf). */
+static void run_softmax_take(run_softmax* st, float s, const void* base, int dtype,
+                             int64_t off) {
+    const float top = st->top > s ? st->top : s;
+    const float carry = isinf(st->top) ? 0.0f : expf(st->top - top);
+    const float w = expf(s - top);
+    for (int d = 0; d < st->n; ++d)
+        st->acc[d] = st->acc[d] * carry + w * load_elem(base, dtype, off + d);
+    st->mass = st->mass * carry + w;
+    st->top = top;
+}
+
+/* o = acc / mass and lse = top + ln mass; zeros and -inf when no key was
+ * taken */
+static void run_softmax_result(const run_softmax* st, float* o, float* lse) {
+    const int any = st->mass > 0.0f;
+    const float inv = any ? 1.0f / st->mass : 0.0f;
+    for (int d = 0; d < st->n; ++d) o[d] = any ? st->acc[d] * inv : 0.0f;
+    *lse = any ? st->top + logf(st->mass) : -INFINITY;
+}
+
+/* Element offset of key j's row in the paged cache: the block the request's
+ * table names for j / block_size, row j % block_size in it; -1 when that
+ * block is outside the pool. */
+static int64_t paged_row(const int32_t* bt_row, int j, int block_size, int num_blocks, int W) {
+    const int32_t blk = bt_row[j / block_size];
+    if (blk < 0 || blk >= num_blocks) return -1;
+    return ((int64_t)blk * block_size + j % block_size) * W;
+}
+
 int oracle_decode_range(float* o_out, float* lse_out, const void* q_row,
                         int q_dtype, const void* kv_cache, int kv_dtype,
                         const int32_t* bt_row, int seq_len, int t_q, int t,
@@ -126,53 +182,40 @@ int oracle_decode_range(float* o_out, float* lse_out, const void* q_row,
     const int W = kv_rank + d_rope;
     if (seq_len < 0 || t_q <= 0 || t < 0 || t >= t_q || block_size <= 0)
         return ORACLE_BAD_ARG;
+    /* keys the query sees: the t_q queries are the request's last positions
+       (mla.rs, struct MlaInputs), so query t sees keys 0 .. seq_len - t_q + t */
     int status = ORACLE_OK;
-    int horizon = 0; /* number of keys this query may see */
+    int horizon = 0;
     if (seq_len > 0) {
-        if (seq_len < t_q) {
+        if (seq_len < t_q)
             status = ORACLE_SEQ_SHORTER_THAN_TQ;
-        } else if (seq_len > max_blocks * block_size) {
+        else if (seq_len > max_blocks * block_size)
             status = ORACLE_SEQ_TOO_LONG;
-        } else {
+        else
             horizon = seq_len - t_q + t + 1;
-        }
     }
-    if (j_begin < 0) j_begin = 0;
-    if (j_end > horizon) j_end = horizon;
+    const int j0 = j_begin > 0 ? j_begin : 0;
+    const int j1 = j_end < horizon ? j_end : horizon;
 
     for (int d = 0; d < W; ++d) q_f[d] = load_elem(q_row, q_dtype, d);
-
-    float m = -INFINITY;
-    float l = 0.0f;
     for (int d = 0; d < kv_rank; ++d) acc[d] = 0.0f;
-
-    for (int j = j_begin; j < j_end && status == ORACLE_OK; ++j) {
-        const int slot = j / block_size;
-        const int32_t blk = bt_row[slot];
-        if (blk < 0 || blk >= num_blocks) {
+    run_softmax st = {-INFINITY, 0.0f, acc, kv_rank};
+    for (int j = j0; j < j1 && status == ORACLE_OK; ++j) {
+        const int64_t off = paged_row(bt_row, j, block_size, num_blocks, W);
+        if (off < 0) {
             status = ORACLE_BAD_BLOCK;
             break;
         }
-        const int64_t entry = ((int64_t)blk * block_size + (j % block_size)) * W;
-        float qk = 0.0f;
-        for (int d = 0; d < W; ++d)
-            qk += q_f[d] * load_elem(kv_cache, kv_dtype, entry + d);
-        qk *= scale;
-        const float m_new = m > qk ? m : qk;
-        const float rescale = isinf(m) ? 0.0f : expf(m - m_new);
-        const float p = expf(qk - m_new);
-        for (int d = 0; d < kv_rank; ++d)
-            acc[d] = acc[d] * rescale + p * load_elem(kv_cache, kv_dtype, entry + d);
-        l = l * rescale + p;
-        m = m_new;
+        /* the score spans the whole row [c_kv | k_pe]; the value is its
+           leading kv_rank entries */
+        const float s = dot_elem(q_f, kv_cache, kv_dtype, off, W) * scale;
+        run_softmax_take(&st, s, kv_cache, kv_dtype, off);
     }
     if (status != ORACLE_OK) { /* an invalid request yields the empty result */
-        m = -INFINITY;
-        l = 0.0f;
+        st.top = -INFINITY;
+        st.mass = 0.0f;
     }
-    const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-    for (int d = 0; d < kv_rank; ++d) o_out[d] = l > 0.0f ? acc[d] * inv : 0.0f;
-    *lse_out = l > 0.0f ? m + logf(l) : -INFINITY;
+    run_softmax_result(&st, o_out, lse_out);
     return status;
 }
 
@@ -269,18 +312,11 @@ int oracle_combine(float* o_out, float* lse_out, const float* o_parts,
 int oracle_decompress(float* out, const float* o_lat, const float* w_uv,
                       int rows, int n_head, int d_v, int kv_rank) {
     if (rows < 0 || n_head <= 0 || d_v <= 0 || kv_rank <= 0) return ORACLE_BAD_ARG;
-    for (int r = 0; r < rows; ++r) {
-        for (int h = 0; h < n_head; ++h) {
-            const float* o = o_lat + ((int64_t)r * n_head + h) * kv_rank;
-            const float* wuv = w_uv + (int64_t)h * d_v * kv_rank;
-            float* dst = out + ((int64_t)r * n_head + h) * d_v;
-            for (int j = 0; j < d_v; ++j) {
-                const float* wrow = wuv + (int64_t)j * kv_rank;
-                float acc = 0.0f;
-                for (int l = 0; l < kv_rank; ++l) acc += wrow[l] * o[l];
-                dst[j] = acc;
-            }
-        }
+    for (int64_t rh = 0; rh < (int64_t)rows * n_head; ++rh) {
+        const float* w_h = w_uv + (rh % n_head) * d_v * kv_rank; /* [d_v][kv_rank] */
+        const float* o = o_lat + rh * kv_rank;
+        for (int j = 0; j < d_v; ++j)
+            out[rh * d_v + j] = dot_from(0.0f, w_h + (int64_t)j * kv_rank, 1, o, 1, kv_rank);
     }
     return ORACLE_OK;
 }
@@ -288,17 +324,28 @@ int oracle_decompress(float* out, const float* o_lat, const float* w_uv,
 /* ------------------------------------------------------------------------- */
 /* the two forms over a contiguous cache (mla.rs)                              */
 /* ------------------------------------------------------------------------- */
-/* max-subtracted softmax over s[0..n) in place */
-static void softmax_inplace(float* s, int n) {
-    float m = -INFINITY;
-    for (int i = 0; i < n; ++i) m = s[i] > m ? s[i] : m;
-    float sum = 0.0f;
-    for (int i = 0; i < n; ++i) {
-        s[i] = expf(s[i] - m);
-        sum += s[i];
+/* softmax over s[0..n) in place: exp(s - max) / sum, two passes */
+static void to_probabilities(float* s, int n) {
+    float top = -INFINITY;
+    for (int k = 0; k < n; ++k)
+        if (s[k] > top) top = s[k];
+    float total = 0.0f;
+    for (int k = 0; k < n; ++k) total += (s[k] = expf(s[k] - top));
+    const float inv = 1.0f / total;
+    for (int k = 0; k < n; ++k) s[k] = s[k] * inv;
+}
+
+/* One head's keys and values, decompressed from every latent row:
+ * k_nope[t][p] = w_uk[h][p] . c_kv[t] and v[t][j] = w_uv[h][j] . c_kv[t]. */
+static void expand_head(float* k_nope, float* v, const float* c_kv, const float* wk,
+                        const float* wv, int t_kv, int dn, int dv, int r) {
+    for (int t = 0; t < t_kv; ++t) {
+        const float* c = c_kv + (int64_t)t * r;
+        for (int p = 0; p < dn; ++p)
+            k_nope[(int64_t)t * dn + p] = dot_from(0.0f, wk + (int64_t)p * r, 1, c, 1, r);
+        for (int j = 0; j < dv; ++j)
+            v[(int64_t)t * dv + j] = dot_from(0.0f, wv + (int64_t)j * r, 1, c, 1, r);
     }
-    const float inv = 1.0f / sum;
-    for (int i = 0; i < n; ++i) s[i] *= inv;
 }
 
 /*
@@ -312,38 +359,24 @@ int oracle_attend_naive(float* out, const float* q_nope, const float* q_pe,
                         int d_nope, int d_rope, int d_v, int kv_rank,
                         float scale, float* k_nope, float* v, float* scores) {
     if (t_q <= 0 || t_q > t_kv) return ORACLE_BAD_ARG;
-    const int nh = n_head, dn = d_nope, dr = d_rope, dv = d_v, r = kv_rank;
-    for (int64_t i = 0; i < (int64_t)t_q * nh * dv; ++i) out[i] = 0.0f;
-    for (int h = 0; h < nh; ++h) {
-        const float* wuk = w_uk + (int64_t)h * dn * r;
-        const float* wuv = w_uv + (int64_t)h * dv * r;
-        for (int t = 0; t < t_kv; ++t) {
-            const float* c = c_kv + (int64_t)t * r;
-            for (int p = 0; p < dn; ++p) {
-                float acc = 0.0f;
-                for (int l = 0; l < r; ++l) acc += wuk[(int64_t)p * r + l] * c[l];
-                k_nope[(int64_t)t * dn + p] = acc;
-            }
-            for (int j = 0; j < dv; ++j) {
-                float acc = 0.0f;
-                for (int l = 0; l < r; ++l) acc += wuv[(int64_t)j * r + l] * c[l];
-                v[(int64_t)t * dv + j] = acc;
-            }
-        }
+    const int dn = d_nope, dr = d_rope, dv = d_v, r = kv_rank;
+    for (int h = 0; h < n_head; ++h) {
+        /* every key and value of this head, in full */
+        expand_head(k_nope, v, c_kv, w_uk + (int64_t)h * dn * r, w_uv + (int64_t)h * dv * r,
+                    t_kv, dn, dv, r);
         for (int i = 0; i < t_q; ++i) {
-            const int visible = t_kv - t_q + i + 1;
-            const float* qn = q_nope + ((int64_t)i * nh + h) * dn;
-            const float* qp = q_pe + ((int64_t)i * nh + h) * dr;
-            for (int t = 0; t < visible; ++t) {
-                float s = 0.0f;
-                for (int p = 0; p < dn; ++p) s += qn[p] * k_nope[(int64_t)t * dn + p];
-                for (int p = 0; p < dr; ++p) s += qp[p] * k_pe[(int64_t)t * dr + p];
-                scores[t] = s * scale;
+            const int64_t qrow = (int64_t)i * n_head + h;
+            const int n_vis = t_kv - t_q + i + 1; /* causal: keys 0 .. t_kv - t_q + i */
+            /* ordinary attention with a d_nope + d_rope wide query and key */
+            for (int t = 0; t < n_vis; ++t) {
+                const float nope = dot_from(0.0f, q_nope + qrow * dn, 1,
+                                            k_nope + (int64_t)t * dn, 1, dn);
+                scores[t] = dot_from(nope, q_pe + qrow * dr, 1, k_pe + (int64_t)t * dr, 1, dr) *
+                            scale;
             }
-            softmax_inplace(scores, visible);
-            float* o = out + ((int64_t)i * nh + h) * dv;
-            for (int t = 0; t < visible; ++t)
-                for (int j = 0; j < dv; ++j) o[j] += scores[t] * v[(int64_t)t * dv + j];
+            to_probabilities(scores, n_vis);
+            for (int j = 0; j < dv; ++j)
+                out[qrow * dv + j] = dot_from(0.0f, scores, 1, v + j, dv, n_vis);
         }
     }
     return ORACLE_OK;
@@ -357,34 +390,26 @@ int oracle_attend_absorbed(float* out, const float* q_nope, const float* q_pe,
                            int d_v, int kv_rank, float scale, float* q_lat,
                            float* o_lat, float* scores) {
     if (t_q <= 0 || t_q > t_kv) return ORACLE_BAD_ARG;
-    const int nh = n_head, dn = d_nope, dr = d_rope, dv = d_v, r = kv_rank;
-    for (int h = 0; h < nh; ++h) {
-        const float* wuk = w_uk + (int64_t)h * dn * r;
-        const float* wuv = w_uv + (int64_t)h * dv * r;
+    const int dn = d_nope, dr = d_rope, dv = d_v, r = kv_rank;
+    for (int h = 0; h < n_head; ++h) {
+        const float* wk = w_uk + (int64_t)h * dn * r;
+        const float* wv = w_uv + (int64_t)h * dv * r;
         for (int i = 0; i < t_q; ++i) {
-            const int visible = t_kv - t_q + i + 1;
-            const float* qn = q_nope + ((int64_t)i * nh + h) * dn;
-            const float* qp = q_pe + ((int64_t)i * nh + h) * dr;
-            for (int l = 0; l < r; ++l) q_lat[l] = 0.0f;
-            for (int p = 0; p < dn; ++p)
-                for (int l = 0; l < r; ++l) q_lat[l] += qn[p] * wuk[(int64_t)p * r + l];
-            for (int t = 0; t < visible; ++t) {
-                const float* c = c_kv + (int64_t)t * r;
-                float s = 0.0f;
-                for (int l = 0; l < r; ++l) s += q_lat[l] * c[l];
-                for (int p = 0; p < dr; ++p) s += qp[p] * k_pe[(int64_t)t * dr + p];
-                scores[t] = s * scale;
+            const int64_t qrow = (int64_t)i * n_head + h;
+            const int n_vis = t_kv - t_q + i + 1;
+            /* fold the query into rank space: q_lat[l] = q_nope . column l of w_uk[h] */
+            for (int l = 0; l < r; ++l) q_lat[l] = dot_from(0.0f, q_nope + qrow * dn, 1, wk + l, r, dn);
+            /* MQA scores against the raw rows [c_kv | k_pe] */
+            for (int t = 0; t < n_vis; ++t) {
+                const float lat = dot_from(0.0f, q_lat, 1, c_kv + (int64_t)t * r, 1, r);
+                scores[t] = dot_from(lat, q_pe + qrow * dr, 1, k_pe + (int64_t)t * dr, 1, dr) *
+                            scale;
             }
-            softmax_inplace(scores, visible);
-            for (int l = 0; l < r; ++l) o_lat[l] = 0.0f;
-            for (int t = 0; t < visible; ++t)
-                for (int l = 0; l < r; ++l) o_lat[l] += scores[t] * c_kv[(int64_t)t * r + l];
-            float* o = out + ((int64_t)i * nh + h) * dv;
-            for (int j = 0; j < dv; ++j) {
-                float acc = 0.0f;
-                for (int l = 0; l < r; ++l) acc += wuv[(int64_t)j * r + l] * o_lat[l];
-                o[j] = acc;
-            }
+            to_probabilities(scores, n_vis);
+            /* the output in latent space, then decompressed once */
+            for (int l = 0; l < r; ++l) o_lat[l] = dot_from(0.0f, scores, 1, c_kv + l, r, n_vis);
+            for (int j = 0; j < dv; ++j)
+                out[qrow * dv + j] = dot_from(0.0f, wv + (int64_t)j * r, 1, o_lat, 1, r);
         }
     }
     return ORACLE_OK;
@@ -393,33 +418,45 @@ int oracle_attend_absorbed(float* out, const float* q_nope, const float* q_pe,
 /* ------------------------------------------------------------------------- */
 /* rope pairings and the load-time permutation (mla.rs, rope section)          */
 /* ------------------------------------------------------------------------- */
-/* pair (x[2j], x[2j+1]) rotated by theta_j = pos * base^(-2j/n), theta stepped
- * by the factor base^(-2/n) as the page does */
-void oracle_rope_interleaved(float* x, int n_dims, float pos, float base) {
-    const int half = n_dims / 2;
-    const float theta_scale = powf(base, -2.0f / (float)n_dims);
-    float theta = pos;
-    for (int j = 0; j < half; ++j) {
-        const float s = sinf(theta), c = cosf(theta);
-        const float a = x[2 * j], b = x[2 * j + 1];
-        x[2 * j] = a * c - b * s;
-        x[2 * j + 1] = a * s + b * c;
-        theta *= theta_scale;
-    }
+/* Turn the plane of entries u and v of x by the angle a:
+ * x[u] <- x[u] cos a - x[v] sin a,  x[v] <- x[u] sin a + x[v] cos a,
+ * each product rounded before the sum. */
+static void turn_plane(float* x, int u, int v, float a) {
+    const float sn = sinf(a), cs = cosf(a);
+    const float xu = x[u], xv = x[v];
+    x[u] = xu * cs - xv * sn;
+    x[v] = xu * sn + xv * cs;
 }
 
-/* pair (x[j], x[j+n/2]) rotated by the same theta_j sequence */
+/* The rope of the mla.rs rope functions turns n_dims / 2 planes of x. Plane k
+ * turns by pos * base^(-2k/n_dims), reached as those functions reach it: the
+ * angle of plane 0 is pos, and each next plane's is the previous one times
+ * base^(-2/n_dims), rounded to f32 at every step. The two layouts differ only
+ * in which entries form plane k. */
+
+/* interleaved ("NORM") layout: plane k is entries 2k and 2k + 1 */
+void oracle_rope_interleaved(float* x, int n_dims, float pos, float base) {
+    const float step = powf(base, -2.0f / (float)n_dims);
+    float angle = pos;
+    for (int k = 0; k < n_dims / 2; ++k, angle *= step) turn_plane(x, 2 * k, 2 * k + 1, angle);
+}
+
+/* NEOX layout: plane k is entries k and k + n_dims / 2 */
 void oracle_rope_neox(float* x, int n_dims, float pos, float base) {
+    const float step = powf(base, -2.0f / (float)n_dims);
     const int half = n_dims / 2;
-    const float theta_scale = powf(base, -2.0f / (float)n_dims);
-    float theta = pos;
-    for (int j = 0; j < half; ++j) {
-        const float s = sinf(theta), c = cosf(theta);
-        const float a = x[j], b = x[j + half];
-        x[j] = a * c - b * s;
-        x[j + half] = a * s + b * c;
-        theta *= theta_scale;
-    }
+    float angle = pos;
+    for (int k = 0; k < half; ++k, angle *= step) turn_plane(x, k, k + half, angle);
+}
+
+/* The load-time permutation (mla.rs, norm_to_neox_perm), as an index map
+ * from the interleaved layout to the NEOX one: entry i is plane i / 2, its
+ * first member when i is even (-> i / 2) and its second when odd
+ * (-> i / 2 + n_dims / 2). */
+int oracle_norm_to_neox_perm(int n_dims, int32_t* perm) {
+    if (n_dims < 0 || (n_dims & 1)) return ORACLE_BAD_ARG;
+    for (int i = 0; i < n_dims; ++i) perm[i] = (i & 1) ? (i >> 1) + n_dims / 2 : (i >> 1);
+    return ORACLE_OK;
 }
 
 /* ------------------------------------------------------------------------- */
@@ -464,17 +501,6 @@ int oracle_cache_append(void* cache, int cache_dtype, const void* kv_c, const vo
         }
     }
     return status;
-}
-
-/* source (interleaved) index -> NEOX index: pi(2j) = j, pi(2j+1) = j + n/2 */
-int oracle_norm_to_neox_perm(int n_dims, int32_t* perm) {
-    if (n_dims < 0 || (n_dims & 1)) return ORACLE_BAD_ARG;
-    const int half = n_dims / 2;
-    for (int j = 0; j < half; ++j) {
-        perm[2 * j] = j;
-        perm[2 * j + 1] = j + half;
-    }
-    return ORACLE_OK;
 }
 
 /* ------------------------------------------------------------------------- */

@@ -17,42 +17,41 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "mla_oracle.c")
 
 # (id, original text, replacement, occurrence index)
 MUTANTS = [
-    ("absorb_drops_q_pe", "dst[kv_rank + j] = qp[j];", "dst[kv_rank + j] = 0.0f;", 0),
-    ("absorb_head0_weights", "const float* wuk = w_uk + (int64_t)h * d_nope * kv_rank;",
-     "const float* wuk = w_uk;", 0),
-    ("absorb_head0_query", "const float* qn = q_nope + ((int64_t)r * n_head + h) * d_nope;",
-     "const float* qn = q_nope + ((int64_t)r * n_head) * d_nope;", 0),
-    ("decode_drops_rope_term", "for (int d = 0; d < W; ++d)\n            qk +=",
-     "for (int d = 0; d < kv_rank; ++d)\n            qk +=", 0),
-    ("decode_no_scale", "qk *= scale;", "qk *= 1.0f;", 0),
-    ("decode_rescale_sign", "expf(m - m_new)", "expf(m_new - m)", 0),
-    ("decode_acc_not_rescaled", "acc[d] = acc[d] * rescale + p *", "acc[d] = acc[d] + p *", 0),
-    ("decode_l_not_rescaled", "l = l * rescale + p;", "l = l + p;", 0),
-    ("decode_v_reversed", "p * load_elem(kv_cache, kv_dtype, entry + d);",
-     "p * load_elem(kv_cache, kv_dtype, entry + W - 1 - d);", 0),
+    ("absorb_drops_q_pe", "memcpy(dst + kv_rank, q_pe + rh * d_rope,",
+     "memset(dst + kv_rank, 0,", 0),
+    ("absorb_head0_weights", "const float* w_h = w_uk + (int64_t)h * d_nope * kv_rank;",
+     "const float* w_h = w_uk;", 0),
+    ("absorb_head0_query", "const float* q = q_nope + rh * d_nope;",
+     "const float* q = q_nope + (rh - h) * d_nope;", 0),
+    ("decode_drops_rope_term", "dot_elem(q_f, kv_cache, kv_dtype, off, W)",
+     "dot_elem(q_f, kv_cache, kv_dtype, off, kv_rank)", 0),
+    ("decode_no_scale", "off, W) * scale;", "off, W) * 1.0f;", 0),
+    ("decode_rescale_sign", "expf(st->top - top)", "expf(top - st->top)", 0),
+    ("decode_acc_not_rescaled", "st->acc[d] * carry + w *", "st->acc[d] + w *", 0),
+    ("decode_l_not_rescaled", "st->mass = st->mass * carry + w;", "st->mass = st->mass + w;", 0),
+    ("decode_v_reversed", "w * load_elem(base, dtype, off + d)",
+     "w * load_elem(base, dtype, off + st->n - 1 - d)", 0),
     ("decode_horizon_off_by_one", "horizon = seq_len - t_q + t + 1;",
      "horizon = seq_len - t_q + t;", 0),
     ("decode_horizon_from_chunk_start", "horizon = seq_len - t_q + t + 1;",
      "horizon = t + 1;", 0),
-    ("decode_row_in_block_reversed", "(j % block_size)) * W;",
-     "(block_size - 1 - j % block_size)) * W;", 0),
-    ("decode_lse_no_log", "*lse_out = l > 0.0f ? m + logf(l) : -INFINITY;",
-     "*lse_out = l > 0.0f ? m + l : -INFINITY;", 0),
+    ("decode_row_in_block_reversed", "+ j % block_size) * W;",
+     "+ (block_size - 1 - j % block_size)) * W;", 0),
+    ("decode_lse_no_log", "st->top + logf(st->mass)", "st->top + st->mass", 0),
     ("decode_wrong_table_row", "block_table + (int64_t)b * max_blocks", "block_table", 0),
     ("bf16_wrong_shift", "[i] << 16;", "[i] << 15;", 0),
     ("combine_weight_sign", "expf(lse_parts[s] - M)", "expf(M - lse_parts[s])", 0),
     ("combine_lse_no_log", "*lse_out = M + logf(wsum);", "*lse_out = M;", 0),
-    ("decompress_reversed", "acc += wrow[l] * o[l];", "acc += wrow[l] * o[kv_rank - 1 - l];", 0),
-    ("naive_drops_rope_term", "for (int p = 0; p < dr; ++p) s += qp[p] * k_pe[(int64_t)t * dr + p];",
-     "for (int p = 0; p < dr; ++p) s += 0.0f;", 0),
-    ("absorbed_form_drops_rope_term",
-     "for (int p = 0; p < dr; ++p) s += qp[p] * k_pe[(int64_t)t * dr + p];",
-     "for (int p = 0; p < dr; ++p) s += 0.0f;", 1),
-    ("naive_v_uses_w_uk", "acc += wuv[(int64_t)j * r + l] * c[l];",
-     "acc += wuk[(int64_t)(j % dn) * r + l] * c[l];", 0),
-    ("rope_neox_sign", "x[j + half] = a * s + b * c;", "x[j + half] = a * s - b * c;", 0),
-    ("rope_interleaved_pair", "x[2 * j + 1] = a * s + b * c;", "x[2 * j + 1] = b * c;", 0),
-    ("perm_wrong", "perm[2 * j + 1] = j + half;", "perm[2 * j + 1] = n_dims - 1 - j;", 0),
+    ("decompress_reversed", "1, o, 1, kv_rank);", "1, o + kv_rank - 1, -1, kv_rank);", 0),
+    ("naive_drops_rope_term", "k_pe + (int64_t)t * dr, 1, dr)", "k_pe + (int64_t)t * dr, 1, 0)", 0),
+    ("absorbed_form_drops_rope_term", "k_pe + (int64_t)t * dr, 1, dr)",
+     "k_pe + (int64_t)t * dr, 1, 0)", 1),
+    ("naive_v_uses_w_uk", "dot_from(0.0f, wv + (int64_t)j * r, 1, c, 1, r)",
+     "dot_from(0.0f, wk + (int64_t)(j % dn) * r, 1, c, 1, r)", 0),
+    ("rope_neox_sign", "x[v] = xu * sn + xv * cs;", "x[v] = xu * sn - xv * cs;", 0),
+    ("rope_interleaved_pair", "turn_plane(x, 2 * k, 2 * k + 1, angle)",
+     "turn_plane(x, 2 * k, (2 * k + 2) % n_dims, angle)", 0),
+    ("perm_wrong", "(i >> 1) + n_dims / 2 :", "n_dims - 1 - (i >> 1) :", 0),
     ("append_ties_away", "return (uint16_t)((u + 0x7fffu + lsb) >> 16);",
      "return (uint16_t)((u + 0x8000u) >> 16);", 0),
     ("append_truncates", "return (uint16_t)((u + 0x7fffu + lsb) >> 16);",

@@ -14,8 +14,8 @@ def test_naive_equals_absorbed_full_dims():
     pins.check_naive_equals_absorbed_full_dims(oracle.load())
 
 
-def test_nope_scale_is_qk_head_dim():
-    """mla.rs nope_scale_is_qk_head_dim: the NoPE geometry's scale is
+def test_nope_geometry_scale():
+    """MlaDims::scale of mla.rs with no rope columns: the NoPE geometry's scale is
     1/sqrt(d_nope + d_rope) = 1/16, the same as GLM-5.2's, never 1/sqrt(512)."""
     from mla_latent_cache_absorbed_gb300 import workloads
     import math
