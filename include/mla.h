@@ -100,6 +100,27 @@ mla_status mla_absorb_q(void* q_abs, const void* q_nope, const void* q_pe,
                         void* stream);
 
 /*
+ * The absorb with the query's rope ("aclnnMlaProlog", computation formulas
+ * of the query: q^N = q^C W^UK and q^R = ROPE(c^Q W^QR)), for callers that
+ * hold the query's rope part before its rotation:
+ *   q_abs[r][h] = [ sum_p q_nope[r][h][p] * w_uk[h][p][:]  |  rope(q_pe[r][h]) ]
+ * where rope turns the NEOX pair (j, j + P/2) by theta_j = positions[r] *
+ * base^(-2j/P), the ratio base^(-2/P) applied j times in f32 ("memra_engine/
+ * mla.rs source", fn rope_neox; the rope columns of W^QR carry the load-time
+ * permutation, so q_pe arrives in NEOX order). This is the rotation
+ * mla_cache_append_rmsnorm_rope gives the keys, so q^R . k^R depends only on
+ * the distance of the two positions.
+ * q_abs      [rows][H][R+P]  out, dims->dtype
+ * q_nope     [rows][H][Dn], q_pe [rows][H][P] (before the rope), w_uk [H][Dn][R]
+ * positions  [rows] int64, device, 8-byte aligned: each query row's position
+ *            (for the decode, query t of request b sits at seq_len - t_q + t)
+ * rope_base  rotary base (> 0); unused when P == 0, where this is mla_absorb_q
+ */
+mla_status mla_absorb_q_rope(void* q_abs, const void* q_nope, const void* q_pe,
+                             const void* w_uk, const int64_t* positions, int32_t rows,
+                             float rope_base, const mla_dims* dims, void* stream);
+
+/*
  * Scratch bytes mla_decode_paged needs for this batch shape on the current
  * device (split-KV partial outputs and LSEs). The contents need no
  * initialisation and are dead after the call's work completes on the stream.

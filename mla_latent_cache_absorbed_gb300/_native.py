@@ -25,7 +25,7 @@ DEVERR_SEQ_SHORT = 4
 DEVERR_TIMEOUT = 8
 
 # Every exported symbol of include/mla.h.
-EXPORTS = ("mla_absorb_q", "mla_decode_workspace_size", "mla_decode_paged",
+EXPORTS = ("mla_absorb_q", "mla_absorb_q_rope", "mla_decode_workspace_size", "mla_decode_paged",
            "mla_decode_paged_static", "mla_decompress_out", "mla_cache_append",
            "mla_cache_append_rmsnorm_rope", "mla_attend_workspace_size", "mla_attend_absorbed",
            "mla_rope_norm_to_neox_perm",
@@ -67,6 +67,7 @@ def load(path: str = LIB_PATH):
     P, I32, I64, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
     D = ctypes.POINTER(MlaDims)
     lib.mla_absorb_q.argtypes = [P, P, P, P, I32, D, P]
+    lib.mla_absorb_q_rope.argtypes = [P, P, P, P, P, I32, F, D, P]
     lib.mla_decode_workspace_size.argtypes = [I32, I32, D, ctypes.POINTER(ctypes.c_size_t)]
     lib.mla_decode_paged.argtypes = [P, P, P, P, P, P, I32, I32, I32, D, F, P,
                                      ctypes.c_size_t, P, P]
@@ -84,7 +85,8 @@ def load(path: str = LIB_PATH):
     lib.mla_status_str.restype = ctypes.c_char_p
     lib.mla_last_error.argtypes = []
     lib.mla_last_error.restype = ctypes.c_char_p
-    for name in ("mla_absorb_q", "mla_decode_workspace_size", "mla_decode_paged",
+    for name in ("mla_absorb_q", "mla_absorb_q_rope", "mla_decode_workspace_size",
+                 "mla_decode_paged",
                  "mla_decode_paged_static", "mla_decompress_out", "mla_cache_append",
                  "mla_cache_append_rmsnorm_rope", "mla_attend_workspace_size",
                  "mla_attend_absorbed",
@@ -124,6 +126,15 @@ def mla_absorb_q(q_abs, q_nope, q_pe, w_uk, rows: int, dims: MlaDims, stream=Non
     _check("mla_absorb_q", load().mla_absorb_q(_ptr(q_abs), _ptr(q_nope), _ptr(q_pe),
                                                _ptr(w_uk), rows, ctypes.byref(dims),
                                                _stream(stream)))
+
+
+def mla_absorb_q_rope(q_abs, q_nope, q_pe, w_uk, positions, rows: int, rope_base: float,
+                      dims: MlaDims, stream=None):
+    """mla_absorb_q with the query's NEOX rope at each row's position."""
+    _check("mla_absorb_q_rope",
+           load().mla_absorb_q_rope(_ptr(q_abs), _ptr(q_nope), _ptr(q_pe), _ptr(w_uk),
+                                    _ptr(positions), rows, float(rope_base), ctypes.byref(dims),
+                                    _stream(stream)))
 
 
 def mla_decode_workspace_size(batch: int, max_blocks: int, dims: MlaDims) -> int:

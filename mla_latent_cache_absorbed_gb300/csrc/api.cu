@@ -120,6 +120,38 @@ mla_status mla_absorb_q(void* q_abs, const void* q_nope, const void* q_pe, const
     return MLA_OK;
 }
 
+mla_status mla_absorb_q_rope(void* q_abs, const void* q_nope, const void* q_pe,
+                             const void* w_uk, const int64_t* positions, int32_t rows,
+                             float rope_base, const mla_dims* dims, void* stream) {
+    g_last_error[0] = 0;
+    if (mla_status st = check_dims(dims)) return st;
+    REQUIRE(rows >= 0, "rows must be >= 0 (got %d)", rows);
+    const int P = dims->d_rope;
+    REQUIRE(P == 0 || (std::isfinite(rope_base) && rope_base > 0.f),
+            "rope_base must be finite and > 0");
+    if (rows == 0) return MLA_OK;
+    REQUIRE(q_abs && q_nope && w_uk, "q_abs, q_nope and w_uk must be non-NULL");
+    REQUIRE(P == 0 || (q_pe && positions), "q_pe and positions may be NULL only when d_rope == 0");
+    REQUIRE(aligned16(q_abs) && aligned16(q_nope) && aligned16(w_uk) &&
+                (!q_pe || aligned16(q_pe)) && ((uintptr_t)positions & 7u) == 0,
+            "device buffers must be 16-byte aligned, positions 8-byte aligned");
+    if (P == 0) return mla_absorb_q(q_abs, q_nope, q_pe, w_uk, rows, dims, stream);
+    // the rope's per-pair frequency ratio, once, in f32 as the rope is computed
+    // (the same ratio the fused cache append uses for the keys)
+    const float theta_scale = powf(rope_base, -2.0f / (float)P);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (dims->dtype == MLA_BF16 && tc_gemm_supported(*dims, rows, /*absorb=*/true)) {
+        MLA_CUDA_TRY(launch_absorb_tc(q_abs, q_nope, q_pe, w_uk, rows, *dims, s, /*early=*/false,
+                                      positions, theta_scale),
+                     "absorb with rope (tensor cores)");
+        return MLA_OK;
+    }
+    MLA_CUDA_TRY(launch_absorb_simt(q_abs, q_nope, q_pe, w_uk, rows, *dims, s, positions,
+                                    theta_scale),
+                 "absorb with rope");
+    return MLA_OK;
+}
+
 mla_status mla_cache_append(void* kv_cache, const void* kv_c, const void* k_pe,
                             const int64_t* slot_mapping, int32_t n_tokens, int32_t num_blocks,
                             int32_t src_dtype, const mla_dims* dims, int32_t* dev_err,

@@ -40,9 +40,12 @@ cudaError_t launch_cache_append_rmsnorm_rope(void* cache, const void* kv_c, cons
                                              int32_t num_blocks, int32_t src_dtype, float eps,
                                              float theta_scale, const mla_dims& d,
                                              int32_t* dev_err, cudaStream_t s);
+// positions: null copies q_pe into the rope tail; otherwise the tail is the
+// NEOX rope of q_pe at positions[r] (theta_j = pos * theta_scale^j)
 cudaError_t launch_absorb_simt(void* q_abs, const void* q_nope, const void* q_pe,
                                const void* w_uk, int32_t rows, const mla_dims& d,
-                               cudaStream_t s);
+                               cudaStream_t s, const int64_t* positions = nullptr,
+                               float theta_scale = 1.f);
 cudaError_t launch_decompress_simt(void* out, const void* o_lat, const void* w_uv,
                                    int32_t rows, const mla_dims& d, cudaStream_t s);
 cudaError_t launch_decode_simt(void* out, float* lse, const void* q_abs,

@@ -56,7 +56,9 @@ __global__ void __launch_bounds__(256) absorb_simt(T* __restrict__ q_abs,
                                                    const T* __restrict__ q_nope,
                                                    const T* __restrict__ q_pe,
                                                    const T* __restrict__ w_uk, int rows,
-                                                   int H, int Dn, int P, int R) {
+                                                   int H, int Dn, int P, int R,
+                                                   const int64_t* __restrict__ positions,
+                                                   float theta_scale) {
     extern __shared__ float sq[];  // [kRowTile][Dn]
     const int h = blockIdx.x;
     const int r0 = blockIdx.z * kRowTile;
@@ -80,11 +82,26 @@ __global__ void __launch_bounds__(256) absorb_simt(T* __restrict__ q_abs,
         }
         for (int r = 0; r < nr; ++r) st(q_abs, ((int64_t)(r0 + r) * H + h) * W + l, acc[r]);
     }
-    if (blockIdx.y == 0) {
+    if (blockIdx.y == 0 && !positions) {
         for (int i = threadIdx.x; i < nr * P; i += blockDim.x) {
             const int r = i / P, j = i % P;
             const int64_t row = (int64_t)(r0 + r) * H + h;
             st(q_abs, row * W + R + j, ld(q_pe, row * P + j));
+        }
+    } else if (blockIdx.y == 0) {
+        // the query's rope at its row's position: NEOX pair (j, j + P/2)
+        // turned by theta_j = pos * theta_scale^j, the ratio applied j times
+        const int half = P / 2;
+        for (int i = threadIdx.x; i < nr * half; i += blockDim.x) {
+            const int r = i / half, j = i % half;
+            const int64_t row = (int64_t)(r0 + r) * H + h;
+            float theta = (float)positions[r0 + r];
+            for (int k = 0; k < j; ++k) theta = __fmul_rn(theta, theta_scale);
+            float sn, cs;
+            sincosf(theta, &sn, &cs);
+            const float a = ld(q_pe, row * P + j), b = ld(q_pe, row * P + j + half);
+            st(q_abs, row * W + R + j, __fsub_rn(__fmul_rn(a, cs), __fmul_rn(b, sn)));
+            st(q_abs, row * W + R + j + half, __fadd_rn(__fmul_rn(a, sn), __fmul_rn(b, cs)));
         }
     }
 }
@@ -304,18 +321,19 @@ SimtDecodePlan simt_decode_plan(int32_t batch, int32_t max_blocks, const mla_dim
 
 cudaError_t launch_absorb_simt(void* q_abs, const void* q_nope, const void* q_pe,
                                const void* w_uk, int32_t rows, const mla_dims& d,
-                               cudaStream_t s) {
+                               cudaStream_t s, const int64_t* positions, float theta_scale) {
     if (rows == 0) return cudaSuccess;
     dim3 grid(d.n_head, (d.kv_rank + 255) / 256, (rows + kRowTile - 1) / kRowTile);
     const size_t smem = (size_t)kRowTile * d.d_nope * sizeof(float);
     if (d.dtype == MLA_F32) {
         absorb_simt<float><<<grid, 256, smem, s>>>(
             (float*)q_abs, (const float*)q_nope, (const float*)q_pe, (const float*)w_uk, rows,
-            d.n_head, d.d_nope, d.d_rope, d.kv_rank);
+            d.n_head, d.d_nope, d.d_rope, d.kv_rank, positions, theta_scale);
     } else {
         absorb_simt<__nv_bfloat16><<<grid, 256, smem, s>>>(
             (__nv_bfloat16*)q_abs, (const __nv_bfloat16*)q_nope, (const __nv_bfloat16*)q_pe,
-            (const __nv_bfloat16*)w_uk, rows, d.n_head, d.d_nope, d.d_rope, d.kv_rank);
+            (const __nv_bfloat16*)w_uk, rows, d.n_head, d.d_nope, d.d_rope, d.kv_rank, positions,
+            theta_scale);
     }
     return cudaGetLastError();
 }

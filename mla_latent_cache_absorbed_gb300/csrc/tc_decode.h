@@ -41,9 +41,11 @@ constexpr size_t kTcDecodeBytesPerPair = 2 * (128 * 512 * 2 + 128 * 4);
 bool tc_gemm_supported(const mla_dims& d, int32_t rows, bool absorb);
 // early: the weights may be read before the previous kernel completes (it
 // does not write them).
+// positions: as for launch_absorb_simt (null: q_pe copied unchanged).
 cudaError_t launch_absorb_tc(void* q_abs, const void* q_nope, const void* q_pe,
                              const void* w_uk, int32_t rows, const mla_dims& d,
-                             cudaStream_t s, bool early);
+                             cudaStream_t s, bool early, const int64_t* positions = nullptr,
+                             float theta_scale = 1.f);
 cudaError_t launch_decompress_tc(void* out, const void* o_lat, const void* w_uv, int32_t rows,
                                  const mla_dims& d, cudaStream_t s, bool early);
 

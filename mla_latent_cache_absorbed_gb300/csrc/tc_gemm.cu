@@ -43,7 +43,9 @@ struct GemmParams {
     int rows, H, K, N;           // N = full output width per head (R or Dv)
     int n_tile;                  // output columns per CTA (<= 256)
     int out_stride;              // elements between consecutive (r, h) rows: W or Dv
-    int P;                       // absorb: rope width copied from q_pe
+    int P;                       // absorb: rope width copied (or roped) from q_pe
+    const int64_t* positions;    // absorb: null, or each query row's rope position
+    float theta_scale;           // absorb with positions: base^(-2/P)
     int a_rows;                  // rows of the A box (the M tile's real rows, multiple of 8)
     int early;                   // weights may be read before the previous kernel completes
     int32_t* dev_err;            // optional: timeout bit
@@ -192,13 +194,29 @@ __global__ void __launch_bounds__(kGThreads, 1)
                                                        __uint_as_float(v[8 * j + 7])));
                 }
             }
-            if (p.P > 0 && blockIdx.y == 0 && row < p.rows) {
+            if (p.P > 0 && blockIdx.y == 0 && row < p.rows && !p.positions) {
                 // rope tail of the absorbed query: q_abs[r, h, N:N+P] = q_pe[r, h, :]
                 const uint4* src = reinterpret_cast<const uint4*>(
                     p.q_pe + ((long long)row * p.H + h) * p.P);
                 uint4* d = reinterpret_cast<uint4*>(
                     p.out + ((long long)row * p.H + h) * p.out_stride + p.N);
                 for (int j = 0; j < p.P / 8; ++j) d[j] = src[j];
+            } else if (p.P > 0 && blockIdx.y == 0 && row < p.rows) {
+                // the query's rope at its row's position: NEOX pair (j, j + P/2)
+                // turned by theta_j = pos * theta_scale^j (the ratio applied j
+                // times, in f32); products rounded before the sum
+                const __nv_bfloat16* src = p.q_pe + ((long long)row * p.H + h) * p.P;
+                __nv_bfloat16* d = p.out + ((long long)row * p.H + h) * p.out_stride + p.N;
+                const int half = p.P / 2;
+                float theta = (float)p.positions[row];
+                for (int j = 0; j < half; ++j) {
+                    float sn, cs;
+                    sincosf(theta, &sn, &cs);
+                    const float a = __bfloat162float(src[j]), b = __bfloat162float(src[j + half]);
+                    d[j] = __float2bfloat16_rn(__fsub_rn(__fmul_rn(a, cs), __fmul_rn(b, sn)));
+                    d[j + half] = __float2bfloat16_rn(__fadd_rn(__fmul_rn(a, sn), __fmul_rn(b, cs)));
+                    theta = __fmul_rn(theta, p.theta_scale);
+                }
             }
         }
     }
@@ -678,7 +696,8 @@ bool tc_gemm_supported(const mla_dims& d, int32_t rows, bool absorb) {
 
 cudaError_t launch_absorb_tc(void* q_abs, const void* q_nope, const void* q_pe,
                              const void* w_uk, int32_t rows, const mla_dims& d,
-                             cudaStream_t s, bool early) {
+                             cudaStream_t s, bool early, const int64_t* positions,
+                             float theta_scale) {
     const int H = d.n_head, Dn = d.d_nope, R = d.kv_rank, P = d.d_rope;
     CUtensorMap a, b;
     // A: q_nope viewed as {Dn, H, rows}; box {64, 1, a_rows}
@@ -699,6 +718,8 @@ cudaError_t launch_absorb_tc(void* q_abs, const void* q_nope, const void* q_pe,
     p.n_tile = 256;
     p.out_stride = R + P;
     p.P = P;
+    p.positions = positions;
+    p.theta_scale = theta_scale;
     p.a_rows = a_rows;
     p.early = early ? 1 : 0;
     p.dev_err = nullptr;
@@ -729,6 +750,8 @@ cudaError_t launch_decompress_tc(void* out, const void* o_lat, const void* w_uv,
     p.n_tile = n_tile;
     p.out_stride = Dv;
     p.P = 0;
+    p.positions = nullptr;
+    p.theta_scale = 1.f;
     p.a_rows = a_rows;
     p.early = early ? 1 : 0;
     p.dev_err = nullptr;

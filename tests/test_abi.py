@@ -99,6 +99,25 @@ def test_validation_without_launch(lib):
         N.mla_decompress_out(16, 16, 16, 1, odd, 0)
 
 
+def test_absorb_q_rope_validation(lib):
+    """Argument checks of the absorb with the query's rope, before any launch."""
+    d = N.MlaDims(4, 16, 8, 16, 32, 1, 16, N.MLA_BF16)
+    f = N.mla_absorb_q_rope
+    with pytest.raises(N.MlaError):
+        f(256, 512, 768, 1024, 0, 2, 10000.0, d, 0)          # positions NULL with d_rope > 0
+    with pytest.raises(N.MlaError):
+        f(256, 512, 0, 1024, 1280, 2, 10000.0, d, 0)         # q_pe NULL with d_rope > 0
+    with pytest.raises(N.MlaError):
+        f(256, 512, 768, 1024, 1284, 2, 10000.0, d, 0)       # positions misaligned
+    with pytest.raises(N.MlaError):
+        f(256, 512, 768, 1024, 1280, 2, 0.0, d, 0)           # rope_base <= 0
+    with pytest.raises(N.MlaError):
+        f(256, 512, 768, 1024, 1280, 2, float("inf"), d, 0)  # rope_base not finite
+    with pytest.raises(N.MlaError):
+        f(256, 512, 768, 1024, 1280, -1, 10000.0, d, 0)      # negative rows
+    f(0, 0, 0, 0, 0, 0, 10000.0, d, 0)                       # no rows: no-op
+
+
 def test_decode_workspace_and_validation(lib):
     d = N.MlaDims(4, 16, 8, 16, 32, 1, 16, N.MLA_F32)
     n = N.mla_decode_workspace_size(2, 4, d)
