@@ -25,8 +25,11 @@
  *     mla_last_error() then describes the failure (thread-local).
  *   - The GPU device current on the calling thread must be the one that owns
  *     the buffers.
- *   - Element types: MLA_F32 or MLA_BF16 for q, cache, weights and outputs;
- *     the LSE is always f32. Accumulation is always f32.
+ *   - Element types: MLA_F32, MLA_BF16 or MLA_F16 for q, cache, weights and
+ *     outputs (one type per call, dims->dtype); f16 is one of the types the
+ *     "vllm.v1.attention.backends.mla.cpu_mla" page lists for CPUMLABackend.
+ *     The LSE is always f32. Accumulation is always f32. The cache appends
+ *     write f32 or bf16 caches only.
  *   - Results are deterministic: the same inputs on the same device give the
  *     same bits (every reduction has a fixed order).
  *   - Kernels launch as programmatic dependents of the kernel before them on
@@ -54,7 +57,7 @@ typedef enum mla_status {
     MLA_ERR_TIMEOUT = 5        /* reserved for callers mapping dev_err bits */
 } mla_status;
 
-typedef enum mla_dtype { MLA_F32 = 0, MLA_BF16 = 1 } mla_dtype;
+typedef enum mla_dtype { MLA_F32 = 0, MLA_BF16 = 1, MLA_F16 = 2 } mla_dtype;
 
 /*
  * Head geometry ("memra_engine/mla.rs source", struct MlaDims) plus the decode
@@ -154,7 +157,7 @@ mla_status mla_decode_workspace_size(int32_t batch, int32_t max_blocks,
  * dev_err     optional device int32: MLA_DEVERR_* bits are OR-ed in when the
  *             device data is invalid (the row is then zero / -inf); the
  *             library never clears it
- * Supported: R+P in {576, 512} with R == 512 for bf16 (the tensor-core
+ * Supported: R+P in {576, 512} with R == 512 for bf16 and f16 (the tensor-core
  * path, for up to 128 x (SMs / 2) query rows t_q * H per request; larger
  * query blocks take the SIMT kernels); any R <= 1024, R+P <= 1152 for f32.
  * batch * t_q * H must stay below 2^31 and max_blocks below 2^27

@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libmla_gb300.so")
 
 MLA_F32 = 0
 MLA_BF16 = 1
+MLA_F16 = 2
 
 DEVERR_BAD_BLOCK = 1
 DEVERR_SEQ_TOO_LONG = 2
@@ -43,7 +44,7 @@ class MlaDims(ctypes.Structure):
     def from_geometry(cls, g) -> "MlaDims":
         """From a workloads.Geometry (or anything with the same fields)."""
         return cls(g.n_head, g.d_nope, g.d_rope, g.d_v, g.kv_rank, g.t_q, g.block_size,
-                   MLA_BF16 if g.dtype == "bf16" else MLA_F32)
+                   {"bf16": MLA_BF16, "f16": MLA_F16}.get(g.dtype, MLA_F32))
 
 
 class MlaError(RuntimeError):

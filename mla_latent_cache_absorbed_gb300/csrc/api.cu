@@ -49,8 +49,8 @@ mla_status check_dims(const mla_dims* d) {
         set_error("dims: block_size must be 16 (got %d)", d->block_size);
         return MLA_ERR_INVALID_ARG;
     }
-    if (d->dtype != MLA_F32 && d->dtype != MLA_BF16) {
-        set_error("dims: dtype must be MLA_F32 or MLA_BF16 (got %d)", d->dtype);
+    if (d->dtype != MLA_F32 && d->dtype != MLA_BF16 && d->dtype != MLA_F16) {
+        set_error("dims: dtype must be MLA_F32, MLA_BF16 or MLA_F16 (got %d)", d->dtype);
         return MLA_ERR_INVALID_ARG;
     }
     if (d->kv_rank > 1024 || d->kv_rank + d->d_rope > 1152 || d->d_nope > 1024 ||
@@ -111,7 +111,7 @@ mla_status mla_absorb_q(void* q_abs, const void* q_nope, const void* q_pe, const
                 (!q_pe || aligned16(q_pe)),
             "device buffers must be 16-byte aligned");
     cudaStream_t s = (cudaStream_t)stream;
-    if (dims->dtype == MLA_BF16 && tc_gemm_supported(*dims, rows, /*absorb=*/true)) {
+    if (dims->dtype != MLA_F32 && tc_gemm_supported(*dims, rows, /*absorb=*/true)) {
         MLA_CUDA_TRY(launch_absorb_tc(q_abs, q_nope, q_pe, w_uk, rows, *dims, s, /*early=*/false),
                      "absorb (tensor cores)");
         return MLA_OK;
@@ -160,6 +160,10 @@ mla_status mla_cache_append(void* kv_cache, const void* kv_c, const void* k_pe,
     if (mla_status st = check_dims(dims)) return st;
     REQUIRE(n_tokens >= 0 && num_blocks >= 0, "n_tokens and num_blocks must be >= 0");
     REQUIRE(src_dtype == MLA_F32 || src_dtype == MLA_BF16, "src_dtype must be MLA_F32 or MLA_BF16");
+    if (dims->dtype == MLA_F16) {
+        set_error("cache append: f16 caches are not supported (f32 or bf16)");
+        return MLA_ERR_UNSUPPORTED;
+    }
     if (n_tokens == 0) return MLA_OK;
     REQUIRE(kv_cache && kv_c && slot_mapping, "kv_cache, kv_c and slot_mapping must be non-NULL");
     REQUIRE(dims->d_rope == 0 || k_pe, "k_pe may be NULL only when d_rope == 0");
@@ -189,6 +193,10 @@ mla_status mla_cache_append_rmsnorm_rope(void* kv_cache, const void* kv_c, const
     if (mla_status st = check_dims(dims)) return st;
     REQUIRE(n_tokens >= 0 && num_blocks >= 0, "n_tokens and num_blocks must be >= 0");
     REQUIRE(src_dtype == MLA_F32 || src_dtype == MLA_BF16, "src_dtype must be MLA_F32 or MLA_BF16");
+    if (dims->dtype == MLA_F16) {
+        set_error("cache append: f16 caches are not supported (f32 or bf16)");
+        return MLA_ERR_UNSUPPORTED;
+    }
     REQUIRE(std::isfinite(eps) && eps >= 0.f, "eps must be finite and >= 0");
     const int P = dims->d_rope;
     REQUIRE(P == 0 || (std::isfinite(rope_base) && rope_base > 0.f),
@@ -227,7 +235,7 @@ mla_status mla_decompress_out(void* out, const void* o_lat, const void* w_uv, in
     REQUIRE(aligned16(out) && aligned16(o_lat) && aligned16(w_uv),
             "device buffers must be 16-byte aligned");
     cudaStream_t s = (cudaStream_t)stream;
-    if (dims->dtype == MLA_BF16 && tc_gemm_supported(*dims, rows, /*absorb=*/false)) {
+    if (dims->dtype != MLA_F32 && tc_gemm_supported(*dims, rows, /*absorb=*/false)) {
         MLA_CUDA_TRY(launch_decompress_tc(out, o_lat, w_uv, rows, *dims, s, /*early=*/false),
                      "decompress (tensor cores)");
         return MLA_OK;
@@ -256,7 +264,7 @@ mla_status check_decode_shape(int32_t batch, int32_t max_blocks, const mla_dims&
 // request). Larger query blocks, such as long prefill chunks, take the SIMT
 // decode.
 bool use_tc_decode(const mla_dims& d) {
-    if (d.dtype != MLA_BF16 || !tc_decode_supported(d)) return false;
+    if (d.dtype == MLA_F32 || !tc_decode_supported(d)) return false;
     size_t bytes = 0;
     if (tc_decode_workspace(1, 1, d, &bytes) != cudaSuccess) return false;
     const long long pairs = (long long)(bytes / kTcDecodeBytesPerPair);

@@ -14,6 +14,7 @@
 //                    same page's header); empty or invalid rows get 0 / -inf
 //   decompress_simt  out = w_uv[h] o_lat (mla.rs, decompress step)
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <math.h>
 #include <stdint.h>
 
@@ -31,8 +32,17 @@ __device__ __forceinline__ float ld<__nv_bfloat16>(const __nv_bfloat16* p, int64
     return __bfloat162float(p[i]);
 }
 
+template <>
+__device__ __forceinline__ float ld<__half>(const __half* p, int64_t i) {
+    return __half2float(p[i]);
+}
+
 template <typename T>
 __device__ __forceinline__ void st(T* p, int64_t i, float v);
+template <>
+__device__ __forceinline__ void st<__half>(__half* p, int64_t i, float v) {
+    p[i] = __float2half_rn(v);
+}
 template <>
 __device__ __forceinline__ void st<float>(float* p, int64_t i, float v) { p[i] = v; }
 template <>
@@ -319,23 +329,27 @@ SimtDecodePlan simt_decode_plan(int32_t batch, int32_t max_blocks, const mla_dim
     return p;
 }
 
+// the element type of a dtype: f32, bf16 or f16
+template <class F>
+cudaError_t by_dtype(int32_t dt, F&& f) {
+    if (dt == MLA_F32) return f(float{});
+    if (dt == MLA_F16) return f(__half{});
+    return f(__nv_bfloat16{});
+}
+
 cudaError_t launch_absorb_simt(void* q_abs, const void* q_nope, const void* q_pe,
                                const void* w_uk, int32_t rows, const mla_dims& d,
                                cudaStream_t s, const int64_t* positions, float theta_scale) {
     if (rows == 0) return cudaSuccess;
     dim3 grid(d.n_head, (d.kv_rank + 255) / 256, (rows + kRowTile - 1) / kRowTile);
     const size_t smem = (size_t)kRowTile * d.d_nope * sizeof(float);
-    if (d.dtype == MLA_F32) {
-        absorb_simt<float><<<grid, 256, smem, s>>>(
-            (float*)q_abs, (const float*)q_nope, (const float*)q_pe, (const float*)w_uk, rows,
-            d.n_head, d.d_nope, d.d_rope, d.kv_rank, positions, theta_scale);
-    } else {
-        absorb_simt<__nv_bfloat16><<<grid, 256, smem, s>>>(
-            (__nv_bfloat16*)q_abs, (const __nv_bfloat16*)q_nope, (const __nv_bfloat16*)q_pe,
-            (const __nv_bfloat16*)w_uk, rows, d.n_head, d.d_nope, d.d_rope, d.kv_rank, positions,
-            theta_scale);
-    }
-    return cudaGetLastError();
+    return by_dtype(d.dtype, [&](auto t) {
+        using T = decltype(t);
+        absorb_simt<T><<<grid, 256, smem, s>>>((T*)q_abs, (const T*)q_nope, (const T*)q_pe,
+                                                (const T*)w_uk, rows, d.n_head, d.d_nope,
+                                                d.d_rope, d.kv_rank, positions, theta_scale);
+        return cudaGetLastError();
+    });
 }
 
 cudaError_t launch_decompress_simt(void* out, const void* o_lat, const void* w_uv,
@@ -343,22 +357,15 @@ cudaError_t launch_decompress_simt(void* out, const void* o_lat, const void* w_u
     if (rows == 0) return cudaSuccess;
     dim3 grid(d.n_head, (d.d_v + 7) / 8, (rows + kRowTile - 1) / kRowTile);
     const size_t smem = (size_t)kRowTile * d.kv_rank * sizeof(float);
-    if (d.dtype == MLA_F32) {
+    return by_dtype(d.dtype, [&](auto t) {
+        using T = decltype(t);
         if (smem > 48 * 1024)
-            cudaFuncSetAttribute(decompress_simt<float>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        decompress_simt<float><<<grid, 256, smem, s>>>((float*)out, (const float*)o_lat,
-                                                       (const float*)w_uv, rows, d.n_head,
-                                                       d.d_v, d.kv_rank);
-    } else {
-        if (smem > 48 * 1024)
-            cudaFuncSetAttribute(decompress_simt<__nv_bfloat16>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        decompress_simt<__nv_bfloat16><<<grid, 256, smem, s>>>(
-            (__nv_bfloat16*)out, (const __nv_bfloat16*)o_lat, (const __nv_bfloat16*)w_uv, rows,
-            d.n_head, d.d_v, d.kv_rank);
-    }
-    return cudaGetLastError();
+            cudaFuncSetAttribute(decompress_simt<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        decompress_simt<T><<<grid, 256, smem, s>>>((T*)out, (const T*)o_lat, (const T*)w_uv,
+                                                   rows, d.n_head, d.d_v, d.kv_rank);
+        return cudaGetLastError();
+    });
 }
 
 cudaError_t launch_decode_simt(void* out, float* lse, const void* q_abs,
@@ -378,24 +385,17 @@ cudaError_t launch_decode_simt(void* out, float* lse, const void* q_abs,
     const int W = d.kv_rank + d.d_rope;
     dim3 grid((unsigned)p.rows, p.nsplit);
     const size_t smem = (size_t)(W + kDecWarps) * sizeof(float);
-    if (d.dtype == MLA_F32) {
-        decode_split<float><<<grid, kDecWarps * 32, smem, s>>>(
-            (const float*)q_abs, (const float*)kv_cache, block_table, seq_lens, d.t_q,
-            d.n_head, d.kv_rank, d.d_rope, max_blocks, num_blocks, scale, p.nsplit, p.chunk,
-            part_o, part_lse, part_status, dev_err);
+    return by_dtype(d.dtype, [&](auto t) {
+        using T = decltype(t);
+        decode_split<T><<<grid, kDecWarps * 32, smem, s>>>(
+            (const T*)q_abs, (const T*)kv_cache, block_table, seq_lens, d.t_q, d.n_head,
+            d.kv_rank, d.d_rope, max_blocks, num_blocks, scale, p.nsplit, p.chunk, part_o,
+            part_lse, part_status, dev_err);
         if (cudaError_t e = cudaGetLastError()) return e;
-        decode_combine<float><<<(unsigned)p.rows, 256, 0, s>>>(
-            part_o, part_lse, part_status, p.nsplit, d.kv_rank, (float*)out, lse);
-    } else {
-        decode_split<__nv_bfloat16><<<grid, kDecWarps * 32, smem, s>>>(
-            (const __nv_bfloat16*)q_abs, (const __nv_bfloat16*)kv_cache, block_table, seq_lens,
-            d.t_q, d.n_head, d.kv_rank, d.d_rope, max_blocks, num_blocks, scale, p.nsplit,
-            p.chunk, part_o, part_lse, part_status, dev_err);
-        if (cudaError_t e = cudaGetLastError()) return e;
-        decode_combine<__nv_bfloat16><<<(unsigned)p.rows, 256, 0, s>>>(
-            part_o, part_lse, part_status, p.nsplit, d.kv_rank, (__nv_bfloat16*)out, lse);
-    }
-    return cudaGetLastError();
+        decode_combine<T><<<(unsigned)p.rows, 256, 0, s>>>(part_o, part_lse, part_status,
+                                                           p.nsplit, d.kv_rank, (T*)out, lse);
+        return cudaGetLastError();
+    });
 }
 
 }  // namespace mla

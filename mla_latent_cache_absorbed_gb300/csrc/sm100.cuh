@@ -185,6 +185,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
            | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
 
+// The same for A and B of one 16-bit type: f16 (kF16) or bf16. Both operands
+// always share the type (kind::f16 takes no mixed pair).
+template <bool kF16>
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, int a_mn, int b_mn) {
+    return kF16 ? (idesc_bf16_f32(M, N, a_mn, b_mn) & ~((7u << 7) | (7u << 10)))  // formats 0: f16
+                : idesc_bf16_f32(M, N, a_mn, b_mn);
+}
+
 // Shared-memory matrix descriptor with 128-byte swizzling.
 //   K-major: 8-row groups of 128-byte rows, `sbo` = byte stride between
 //            8-row groups (1024 for dense groups); lbo unused (16).
@@ -468,6 +476,37 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// two 16-bit elements of type kF16 ? f16 : bf16 from f32 (round to nearest)
+template <bool kF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    return kF16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+}
+// the low / high 16-bit element of a packed pair, as f32 (exact)
+template <bool kF16>
+__device__ __forceinline__ float elem_lo(uint32_t u) {
+    if (kF16) {
+        float f;
+        asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"((unsigned short)(u & 0xffffu)));
+        return f;
+    }
+    return __uint_as_float(u << 16);
+}
+template <bool kF16>
+__device__ __forceinline__ float elem_hi(uint32_t u) {
+    if (kF16) {
+        float f;
+        asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"((unsigned short)(u >> 16)));
+        return f;
+    }
+    return __uint_as_float(u & 0xffff0000u);
 }
 
 }  // namespace sm100

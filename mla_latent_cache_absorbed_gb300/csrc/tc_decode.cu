@@ -318,7 +318,7 @@ __device__ __forceinline__ int valid_blocks(const Walk& w) {
 //                     to the S-CTA only), so both TMA units share the boxes
 // In both CTAs warp 2 first works out the pair's unit range (walk_init) while
 // the barriers and TMEM are set up; every warp then follows that walk.
-template <int W>
+template <int W, bool kF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_pair_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap qmap,
                        const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
@@ -480,7 +480,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         } else if (warp == 4) {
             // ---------------- MMA issuer: S = Q K^T
             if (elect_one()) {
-                constexpr uint32_t idesc = idesc_bf16_f32(128, kTok, 0, 0);
+                constexpr uint32_t idesc = idesc_f32acc<kF16>(128, kTok, 0, 0);
                 long long i = 0;
                 int seg = 0;
                 for (; w.u < w.u_end; walk_next(p, w), ++i) {
@@ -672,7 +672,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < 16; ++k) {
                     const float mine_lo = x[k], mine_hi = x[16 + k];
                     const float got = __shfl_xor_sync(0xffffffffu, par ? mine_lo : mine_hi, 2);
-                    pk[k] = par ? pack_bf16x2(got, mine_hi) : pack_bf16x2(mine_lo, got);
+                    pk[k] = par ? pack2<kF16>(got, mine_hi) : pack2<kF16>(mine_lo, got);
                 }
                 const int need = (!first_tile && alpha != 1.f) ? 1 : 0;
                 const unsigned any = __ballot_sync(0xffffffffu, need);
@@ -827,7 +827,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         } else if (warp == 4) {
             // ---------------- MMA issuer: O += P V
             if (elect_one()) {
-                constexpr uint32_t idesc = idesc_bf16_f32(128, 256, 0, 1);
+                constexpr uint32_t idesc = idesc_f32acc<kF16>(128, 256, 0, 1);
                 long long i = 0;
                 int nevt = 0, ndone = 0;
                 for (; w.u < w.u_end; walk_next(p, w), ++i) {
@@ -974,10 +974,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         for (int u = 0; u < 8; ++u) {
                             const uint32_t* x = u < 4 ? &v0[8 * u] : &v1[8 * (u - 4)];
                             st_shared_v4(rowa + ((u ^ (lane & 7)) << 4),
-                                         pack_bf16x2(__uint_as_float(x[0]) * inv, __uint_as_float(x[1]) * inv),
-                                         pack_bf16x2(__uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv),
-                                         pack_bf16x2(__uint_as_float(x[4]) * inv, __uint_as_float(x[5]) * inv),
-                                         pack_bf16x2(__uint_as_float(x[6]) * inv, __uint_as_float(x[7]) * inv));
+                                         pack2<kF16>(__uint_as_float(x[0]) * inv, __uint_as_float(x[1]) * inv),
+                                         pack2<kF16>(__uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv),
+                                         pack2<kF16>(__uint_as_float(x[4]) * inv, __uint_as_float(x[5]) * inv),
+                                         pack2<kF16>(__uint_as_float(x[6]) * inv, __uint_as_float(x[7]) * inv));
                         }
                         fence_proxy_async_smem();
                         __syncwarp();
@@ -1046,6 +1046,7 @@ __device__ __forceinline__ uint4 load_part(const Params& p, long long slot, int 
     return reinterpret_cast<const uint4*>(p.ws_o + (slot * 128 + r) * 512)[c8];
 }
 
+template <bool kF16>
 __global__ void __launch_bounds__(kCombineThreads, 2) combine_kernel(const Params p) {
     __shared__ int sh_parts[3];  // first pair, part count, first part's slot offset
     __shared__ float sh_w[4 * kCombineMaxRpt][kCombineMaxParts];
@@ -1157,15 +1158,15 @@ __global__ void __launch_bounds__(kCombineThreads, 2) combine_kernel(const Param
                     const uint32_t u[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        acc[2 * e] += wk * __uint_as_float(u[e] << 16);
-                        acc[2 * e + 1] += wk * __uint_as_float(u[e] & 0xffff0000u);
+                        acc[2 * e] += wk * elem_lo<kF16>(u[e]);
+                        acc[2 * e + 1] += wk * elem_hi<kF16>(u[e]);
                     }
                 }
                 if (++k == nparts) {  // row done: write it
                     if (r < rows) {
                         reinterpret_cast<uint4*>(p.out + (orow0 + r) * 512)[c8] =
-                            make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                                       pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+                            make_uint4(pack2<kF16>(acc[0], acc[1]), pack2<kF16>(acc[2], acc[3]),
+                                       pack2<kF16>(acc[4], acc[5]), pack2<kF16>(acc[6], acc[7]));
                         if (c8 == 0 && p.lse) p.lse[orow0 + r] = sh_lse[cw];
                     }
 #pragma unroll
@@ -1201,14 +1202,14 @@ cudaError_t get_encode(PFN_cuTensorMapEncodeTiled_v12000* fn) {
     return cudaSuccess;
 }
 
-template <int W>
+template <int W, bool kF16>
 cudaError_t setup_kernel(int dev, int* max_pairs) {
     std::lock_guard<std::mutex> lock(g_mu);
     DeviceInfo& di = g_dev[dev & 63];
-    static bool attr_set[2][64] = {};
-    const int wi = W == 576 ? 0 : 1;
+    static bool attr_set[4][64] = {};
+    const int wi = (W == 576 ? 0 : 1) + (kF16 ? 2 : 0);
     if (!attr_set[wi][dev & 63]) {
-        cudaError_t e = cudaFuncSetAttribute(decode_pair_kernel<W>,
+        cudaError_t e = cudaFuncSetAttribute(decode_pair_kernel<W, kF16>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemBytes);
         if (e != cudaSuccess) return e;
@@ -1227,7 +1228,7 @@ cudaError_t setup_kernel(int dev, int* max_pairs) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        cudaError_t e = cudaOccupancyMaxActiveClusters(&n, decode_pair_kernel<W>, &cfg);
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&n, decode_pair_kernel<W, kF16>, &cfg);
         if (e != cudaSuccess) return e;
         if (n <= 0) return cudaErrorNotSupported;
         di.max_pairs = n < kCombineMaxParts ? n : kCombineMaxParts;
@@ -1241,7 +1242,13 @@ int max_pairs_for(const mla_dims& d, cudaError_t* err) {
     *err = cudaGetDevice(&dev);
     if (*err != cudaSuccess) return 0;
     int n = 0;
-    *err = (d.kv_rank + d.d_rope == 576) ? setup_kernel<576>(dev, &n) : setup_kernel<512>(dev, &n);
+    // the f16 and bf16 instances share one layout, so one occupancy answer
+    // serves both; each still gets its shared-memory attribute set
+    const bool f16 = d.dtype == MLA_F16;
+    if (d.kv_rank + d.d_rope == 576)
+        *err = f16 ? setup_kernel<576, true>(dev, &n) : setup_kernel<576, false>(dev, &n);
+    else
+        *err = f16 ? setup_kernel<512, true>(dev, &n) : setup_kernel<512, false>(dev, &n);
     return n;
 }
 
@@ -1249,7 +1256,8 @@ int max_pairs_for(const mla_dims& d, cudaError_t* err) {
 
 bool tc_decode_supported(const mla_dims& d) {
     const int W = d.kv_rank + d.d_rope;
-    return d.dtype == MLA_BF16 && d.kv_rank == 512 && (W == 576 || W == 512) &&
+    return (d.dtype == MLA_BF16 || d.dtype == MLA_F16) && d.kv_rank == 512 &&
+           (W == 576 || W == 512) &&
            d.block_size == 16 && d.t_q * d.n_head <= 1 << 20;
 }
 
@@ -1292,12 +1300,15 @@ cudaError_t launch_decode_tc(void* out, float* lse, const void* q_abs, const voi
     if (e != cudaSuccess) return e;
     PFN_cuTensorMapEncodeTiled_v12000 enc;
     if ((e = get_encode(&enc)) != cudaSuccess) return e;
+    const bool f16 = d.dtype == MLA_F16;
+    const CUtensorMapDataType tdt = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                        : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap tmap;
     cuuint64_t dims[3] = {(cuuint64_t)W, 16, (cuuint64_t)num_blocks};
     cuuint64_t strides[2] = {(cuuint64_t)W * 2, (cuuint64_t)16 * W * 2};
     cuuint32_t box[3] = {64, 16, 1};
     cuuint32_t es[3] = {1, 1, 1};
-    CUresult cr = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(kv_cache),
+    CUresult cr = enc(&tmap, tdt, 3, const_cast<void*>(kv_cache),
                       dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -1314,7 +1325,7 @@ cudaError_t launch_decode_tc(void* out, float* lse, const void* q_abs, const voi
         cuuint64_t qstrides[2] = {(cuuint64_t)W * 2, (cuuint64_t)Mq * W * 2};
         cuuint32_t qbox[3] = {64, (cuuint32_t)(Mq < 128 ? Mq : 128), 1};
         cuuint32_t qes[3] = {1, 1, 1};
-        cr = enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q_abs), qdims,
+        cr = enc(&qmap, tdt, 3, const_cast<void*>(q_abs), qdims,
                  qstrides, qbox, qes, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (cr != CUDA_SUCCESS) {
@@ -1329,7 +1340,7 @@ cudaError_t launch_decode_tc(void* out, float* lse, const void* q_abs, const voi
         cuuint64_t vstrides[3] = {(cuuint64_t)W * 2, 128, (cuuint64_t)16 * W * 2};
         cuuint32_t vbox[4] = {64, 16, 8, 1};
         cuuint32_t ves[4] = {1, 1, 1, 1};
-        cr = enc(&vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(kv_cache), vdims,
+        cr = enc(&vmap, tdt, 4, const_cast<void*>(kv_cache), vdims,
                  vstrides, vbox, ves, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (cr != CUDA_SUCCESS) {
@@ -1349,11 +1360,11 @@ cudaError_t launch_decode_tc(void* out, float* lse, const void* q_abs, const voi
         cuuint64_t wstrides[2] = {512 * 2, 128 * 512 * 2};
         cuuint32_t box[3] = {64, 32, 1};
         cuuint32_t es3[3] = {1, 1, 1};
-        cr = enc(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out, odims, ostrides, box, es3,
+        cr = enc(&omap, tdt, 3, out, odims, ostrides, box, es3,
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (cr == CUDA_SUCCESS)
-            cr = enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, workspace, wdims, wstrides, box,
+            cr = enc(&wmap, tdt, 3, workspace, wdims, wstrides, box,
                      es3, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (cr != CUDA_SUCCESS) {
@@ -1400,9 +1411,15 @@ cudaError_t launch_decode_tc(void* out, float* lse, const void* q_abs, const voi
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     if (W == 576)
-        e = cudaLaunchKernelEx(&cfg, decode_pair_kernel<576>, tmap, qmap, vmap, omap, wmap, p);
+        e = f16 ? cudaLaunchKernelEx(&cfg, decode_pair_kernel<576, true>, tmap, qmap, vmap, omap,
+                                     wmap, p)
+                : cudaLaunchKernelEx(&cfg, decode_pair_kernel<576, false>, tmap, qmap, vmap, omap,
+                                     wmap, p);
     else
-        e = cudaLaunchKernelEx(&cfg, decode_pair_kernel<512>, tmap, qmap, vmap, omap, wmap, p);
+        e = f16 ? cudaLaunchKernelEx(&cfg, decode_pair_kernel<512, true>, tmap, qmap, vmap, omap,
+                                     wmap, p)
+                : cudaLaunchKernelEx(&cfg, decode_pair_kernel<512, false>, tmap, qmap, vmap, omap,
+                                     wmap, p);
     if (e != cudaSuccess) return e;
     if (!combine) return cudaGetLastError();
     const long long G = (d.t_q * d.n_head + 127) / 128;
@@ -1427,7 +1444,8 @@ cudaError_t launch_decode_tc(void* out, float* lse, const void* q_abs, const voi
     ccfg.stream = s;
     ccfg.attrs = cattr;
     ccfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&ccfg, combine_kernel, p);
+    e = f16 ? cudaLaunchKernelEx(&ccfg, combine_kernel<true>, p)
+            : cudaLaunchKernelEx(&ccfg, combine_kernel<false>, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -51,7 +51,7 @@ struct GemmParams {
     int32_t* dev_err;            // optional: timeout bit
 };
 
-template <bool kBMnMajor>
+template <bool kBMnMajor, bool kF16>
 __global__ void __launch_bounds__(kGThreads, 1)
     tc_bgemm_kernel(const __grid_constant__ CUtensorMap amap,
                     const __grid_constant__ CUtensorMap bmap, const GemmParams p) {
@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
     } else if (warp == 1) {
         if (elect_one()) {
-            const uint32_t idesc = idesc_bf16_f32(128, p.n_tile, 0, kBMnMajor ? 1 : 0);
+            const uint32_t idesc = idesc_f32acc<kF16>(128, p.n_tile, 0, kBMnMajor ? 1 : 0);
             for (int kc = 0; kc < nk; ++kc) {
                 const int s = kc % kGStages;
                 if (!mbar_wait(smem_u32(&full[s]), (kc / kGStages) & 1, kGWaitNs)) {
@@ -184,13 +184,13 @@ __global__ void __launch_bounds__(kGThreads, 1)
                     uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        d4[j] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * j]),
+                        d4[j] = make_uint4(pack2<kF16>(__uint_as_float(v[8 * j]),
                                                        __uint_as_float(v[8 * j + 1])),
-                                           pack_bf16x2(__uint_as_float(v[8 * j + 2]),
+                                           pack2<kF16>(__uint_as_float(v[8 * j + 2]),
                                                        __uint_as_float(v[8 * j + 3])),
-                                           pack_bf16x2(__uint_as_float(v[8 * j + 4]),
+                                           pack2<kF16>(__uint_as_float(v[8 * j + 4]),
                                                        __uint_as_float(v[8 * j + 5])),
-                                           pack_bf16x2(__uint_as_float(v[8 * j + 6]),
+                                           pack2<kF16>(__uint_as_float(v[8 * j + 6]),
                                                        __uint_as_float(v[8 * j + 7])));
                 }
             }
@@ -241,17 +241,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     return fn;
 }
 
-// 3-D bf16 tensor map with 128-byte swizzle; dims/strides innermost first
+// 3-D tensor map of 16-bit elements (f16 or bf16) with 128-byte swizzle;
+// dims/strides innermost first
 cudaError_t make_map(CUtensorMap* m, const void* base, cuuint64_t d0, cuuint64_t d1,
                      cuuint64_t d2, cuuint64_t s1_bytes, cuuint64_t s2_bytes, cuuint32_t b0,
-                     cuuint32_t b1, cuuint32_t b2) {
+                     cuuint32_t b1, cuuint32_t b2, bool f16) {
     auto enc = encoder();
     if (!enc) return cudaErrorNotSupported;
     cuuint64_t dims[3] = {d0, d1, d2};
     cuuint64_t strides[2] = {s1_bytes, s2_bytes};
     cuuint32_t box[3] = {b0, b1, b2};
     cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+    CUresult r = enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                      box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
@@ -263,18 +264,19 @@ cudaError_t make_map(CUtensorMap* m, const void* base, cuuint64_t d0, cuuint64_t
 
 int smem_for(int n_tile) { return kGStages * (kAChunk + n_tile * 128) + 256; }
 
-template <bool kBMnMajor>
+template <bool kBMnMajor, bool kF16>
 cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
                    cudaStream_t s) {
     const int smem = smem_for(p.n_tile);
-    static std::once_flag once[2];
-    static cudaError_t attr_err[2] = {cudaSuccess, cudaSuccess};
-    std::call_once(once[kBMnMajor ? 1 : 0], [&] {
-        attr_err[kBMnMajor ? 1 : 0] = cudaFuncSetAttribute(
-            tc_bgemm_kernel<kBMnMajor>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    constexpr int kInst = (kBMnMajor ? 1 : 0) + (kF16 ? 2 : 0);
+    static std::once_flag once[4];
+    static cudaError_t attr_err[4] = {cudaSuccess, cudaSuccess, cudaSuccess, cudaSuccess};
+    std::call_once(once[kInst], [&] {
+        attr_err[kInst] = cudaFuncSetAttribute(
+            tc_bgemm_kernel<kBMnMajor, kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
             smem_for(256));
     });
-    if (attr_err[kBMnMajor ? 1 : 0] != cudaSuccess) return attr_err[kBMnMajor ? 1 : 0];
+    if (attr_err[kInst] != cudaSuccess) return attr_err[kInst];
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -285,7 +287,7 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const GemmParams&
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, tc_bgemm_kernel<kBMnMajor>, a, b, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, tc_bgemm_kernel<kBMnMajor, kF16>, a, b, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -337,7 +339,7 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
 // rows r_g = r0 + step * g (g < G, r_g < mrows), whose parts are loaded KP at
 // a time (G * KP loads in flight). Per row, np: 0 empty (zeros), 1 copied from
 // o_lat (weight 1), more: the parts' partial rows with the weights in sh_w.
-template <int G, int KP>
+template <int G, int KP, bool kF16>
 __device__ __forceinline__ void merge_rows(const MergeParams& p, int h, int m0, int mrows, int r0,
                                            int step, int pc, int np_max, const int* sh_pf,
                                            const int* sh_np, const int* sh_s0, const int* sh_rr,
@@ -384,8 +386,8 @@ __device__ __forceinline__ void merge_rows(const MergeParams& p, int h, int m0, 
                     const uint32_t x[4] = {v[g][kk].x, v[g][kk].y, v[g][kk].z, v[g][kk].w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        acc[g][2 * e] += wk * __uint_as_float(x[e] << 16);
-                        acc[g][2 * e + 1] += wk * __uint_as_float(x[e] & 0xffff0000u);
+                        acc[g][2 * e] += wk * elem_lo<kF16>(x[e]);
+                        acc[g][2 * e + 1] += wk * elem_hi<kF16>(x[e]);
                     }
                 }
             }
@@ -396,8 +398,8 @@ __device__ __forceinline__ void merge_rows(const MergeParams& p, int h, int m0, 
     for (int g = 0; g < G; ++g) {
         const int r = r0 + step * g;
         if (r < mrows) {
-            const uint32_t x0 = pack_bf16x2(acc[g][0], acc[g][1]), x1 = pack_bf16x2(acc[g][2], acc[g][3]);
-            const uint32_t x2 = pack_bf16x2(acc[g][4], acc[g][5]), x3 = pack_bf16x2(acc[g][6], acc[g][7]);
+            const uint32_t x0 = pack2<kF16>(acc[g][0], acc[g][1]), x1 = pack2<kF16>(acc[g][2], acc[g][3]);
+            const uint32_t x2 = pack2<kF16>(acc[g][4], acc[g][5]), x3 = pack2<kF16>(acc[g][6], acc[g][7]);
             const uint32_t at = smem_u32(a_smem + kc * 16384 + r * 128 + ((u ^ (r & 7)) << 4));
             st_shared_v4(at, x0, x1, x2, x3);
             // the same A row in the other CTAs of the cluster
@@ -409,6 +411,7 @@ __device__ __forceinline__ void merge_rows(const MergeParams& p, int h, int m0, 
     }
 }
 
+template <bool kF16>
 __global__ void __launch_bounds__(kMThreads, 1)
     tc_decompress_merge_kernel(const __grid_constant__ CUtensorMap bmap, const MergeParams p) {
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -477,7 +480,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
         }
     } else if (warp == 1) {
         if (elect_one()) {
-            const uint32_t idesc = idesc_bf16_f32(128, p.n_tile, 0, 0);
+            const uint32_t idesc = idesc_f32acc<kF16>(128, p.n_tile, 0, 0);
             ok = mbar_wait_sleep(smem_u32(aready), 0, kGWaitNs);
             for (int kc = 0; kc < kMChunks && ok; ++kc) {
                 const int s = kc % kMStages;
@@ -623,15 +626,15 @@ __global__ void __launch_bounds__(kMThreads, 1)
             const uint32_t ab = smem_u32(aready);
             if (npm <= 4) {
                 for (int j = 0; j < nsteps; j += 4)
-                    merge_rows<4, 4>(p, h, m0, mrows, r0 + step * j, step, pc, npm, sh_pf, sh_np,
+                    merge_rows<4, 4, kF16>(p, h, m0, mrows, r0 + step * j, step, pc, npm, sh_pf, sh_np,
                                      sh_s0, sh_rr, sh_w, a_smem, csize, rank, ab);
             } else if (npm <= 8) {
                 for (int j = 0; j < nsteps; j += 2)
-                    merge_rows<2, 8>(p, h, m0, mrows, r0 + step * j, step, pc, npm, sh_pf, sh_np,
+                    merge_rows<2, 8, kF16>(p, h, m0, mrows, r0 + step * j, step, pc, npm, sh_pf, sh_np,
                                      sh_s0, sh_rr, sh_w, a_smem, csize, rank, ab);
             } else {
                 for (int j = 0; j < nsteps; ++j)
-                    merge_rows<1, 16>(p, h, m0, mrows, r0 + step * j, step, pc, npm, sh_pf, sh_np,
+                    merge_rows<1, 16, kF16>(p, h, m0, mrows, r0 + step * j, step, pc, npm, sh_pf, sh_np,
                                       sh_s0, sh_rr, sh_w, a_smem, csize, rank, ab);
             }
         }
@@ -663,10 +666,10 @@ __global__ void __launch_bounds__(kMThreads, 1)
                         uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            d4[j] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * j]), __uint_as_float(v[8 * j + 1])),
-                                               pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
-                                               pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
-                                               pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+                            d4[j] = make_uint4(pack2<kF16>(__uint_as_float(v[8 * j]), __uint_as_float(v[8 * j + 1])),
+                                               pack2<kF16>(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+                                               pack2<kF16>(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+                                               pack2<kF16>(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
                     }
                 }
             }
@@ -688,7 +691,8 @@ size_t merge_smem_bytes(int n_tile, int np) {
 }  // namespace
 
 bool tc_gemm_supported(const mla_dims& d, int32_t rows, bool absorb) {
-    if (d.dtype != MLA_BF16 || rows <= 0 || d.n_head > 65535) return false;
+    if ((d.dtype != MLA_BF16 && d.dtype != MLA_F16) || rows <= 0 || d.n_head > 65535)
+        return false;
     if (absorb)
         return d.d_nope % 64 == 0 && d.kv_rank % 256 == 0 && d.d_rope % 8 == 0;
     return d.kv_rank % 64 == 0 && (d.d_v == 128 || d.d_v % 256 == 0);
@@ -699,14 +703,15 @@ cudaError_t launch_absorb_tc(void* q_abs, const void* q_nope, const void* q_pe,
                              cudaStream_t s, bool early, const int64_t* positions,
                              float theta_scale) {
     const int H = d.n_head, Dn = d.d_nope, R = d.kv_rank, P = d.d_rope;
+    const bool f16 = d.dtype == MLA_F16;
     CUtensorMap a, b;
     // A: q_nope viewed as {Dn, H, rows}; box {64, 1, a_rows}
     const int a_rows = rows >= 128 ? 128 : (rows + 7) / 8 * 8;
     cudaError_t e = make_map(&a, q_nope, Dn, H, rows, (cuuint64_t)Dn * 2, (cuuint64_t)H * Dn * 2,
-                             64, 1, (cuuint32_t)a_rows);
+                             64, 1, (cuuint32_t)a_rows, f16);
     if (e != cudaSuccess) return e;
     // B: w_uk viewed as {R, Dn, H} (N contiguous); box {64 N, 64 K, 1}
-    e = make_map(&b, w_uk, R, Dn, H, (cuuint64_t)R * 2, (cuuint64_t)Dn * R * 2, 64, 64, 1);
+    e = make_map(&b, w_uk, R, Dn, H, (cuuint64_t)R * 2, (cuuint64_t)Dn * R * 2, 64, 64, 1, f16);
     if (e != cudaSuccess) return e;
     GemmParams p;
     p.out = (__nv_bfloat16*)q_abs;
@@ -723,7 +728,7 @@ cudaError_t launch_absorb_tc(void* q_abs, const void* q_nope, const void* q_pe,
     p.a_rows = a_rows;
     p.early = early ? 1 : 0;
     p.dev_err = nullptr;
-    return launch<true>(a, b, p, s);
+    return f16 ? launch<true, true>(a, b, p, s) : launch<true, false>(a, b, p, s);
 }
 
 cudaError_t launch_decompress_tc(void* out, const void* o_lat, const void* w_uv, int32_t rows,
@@ -733,12 +738,13 @@ cudaError_t launch_decompress_tc(void* out, const void* o_lat, const void* w_uv,
     CUtensorMap a, b;
     // A: o_lat viewed as {R, H, rows}; box {64, 1, a_rows}
     const int a_rows = rows >= 128 ? 128 : (rows + 7) / 8 * 8;
+    const bool f16 = d.dtype == MLA_F16;
     cudaError_t e = make_map(&a, o_lat, R, H, rows, (cuuint64_t)R * 2, (cuuint64_t)H * R * 2, 64,
-                             1, (cuuint32_t)a_rows);
+                             1, (cuuint32_t)a_rows, f16);
     if (e != cudaSuccess) return e;
     // B: w_uv viewed as {R, Dv, H} (K contiguous); box {64 K, n_tile N, 1}
     e = make_map(&b, w_uv, R, Dv, H, (cuuint64_t)R * 2, (cuuint64_t)Dv * R * 2, 64,
-                 (cuuint32_t)n_tile, 1);
+                 (cuuint32_t)n_tile, 1, f16);
     if (e != cudaSuccess) return e;
     GemmParams p;
     p.out = (__nv_bfloat16*)out;
@@ -755,7 +761,7 @@ cudaError_t launch_decompress_tc(void* out, const void* o_lat, const void* w_uv,
     p.a_rows = a_rows;
     p.early = early ? 1 : 0;
     p.dev_err = nullptr;
-    return launch<false>(a, b, p, s);
+    return f16 ? launch<false, true>(a, b, p, s) : launch<false, false>(a, b, p, s);
 }
 
 // Output columns per CTA of the merging decompress. The CTAs of one head
@@ -785,10 +791,11 @@ cudaError_t launch_decompress_merge_tc(void* out, float* lse, const void* o_lat,
     const int H = d.n_head, R = d.kv_rank, Dv = d.d_v;
     const int rows = batch * d.t_q;
     const int n_tile = merge_n_tile(d, rows);
+    const bool f16 = d.dtype == MLA_F16;
     CUtensorMap b;
     // B: w_uv viewed as {R, Dv, H} (K contiguous); box {64 K, n_tile N, 1}
     cudaError_t e = make_map(&b, w_uv, R, Dv, H, (cuuint64_t)R * 2, (cuuint64_t)Dv * R * 2, 64,
-                             (cuuint32_t)n_tile, 1);
+                             (cuuint32_t)n_tile, 1, f16);
     if (e != cudaSuccess) return e;
     MergeParams p;
     p.seq_lens = seq_lens;
@@ -808,13 +815,17 @@ cudaError_t launch_decompress_merge_tc(void* out, float* lse, const void* o_lat,
     p.Dv = Dv;
     p.n_tile = n_tile;
     const size_t smem = merge_smem_bytes(n_tile, info.NP) + 1024;  // + alignment slack
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(tc_decompress_merge_kernel,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    static std::once_flag once[2];
+    static cudaError_t attr_err[2] = {cudaSuccess, cudaSuccess};
+    std::call_once(once[f16 ? 1 : 0], [&] {
+        attr_err[f16 ? 1 : 0] = f16 ? cudaFuncSetAttribute(tc_decompress_merge_kernel<true>,
+                                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                           232448)
+                                    : cudaFuncSetAttribute(tc_decompress_merge_kernel<false>,
+                                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                           232448);
     });
-    if (attr_err != cudaSuccess) return attr_err;
+    if (attr_err[f16 ? 1 : 0] != cudaSuccess) return attr_err[f16 ? 1 : 0];
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -829,7 +840,8 @@ cudaError_t launch_decompress_merge_tc(void* out, float* lse, const void* o_lat,
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, tc_decompress_merge_kernel, b, p);
+    e = f16 ? cudaLaunchKernelEx(&cfg, tc_decompress_merge_kernel<true>, b, p)
+            : cudaLaunchKernelEx(&cfg, tc_decompress_merge_kernel<false>, b, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -19,13 +19,15 @@ def _torch():
 
 def host_to_device(a: np.ndarray, dtype: str, device):
     """Upload a host array. bf16 data may be given as f32 values (exact bf16)
-    or as uint16 bit patterns."""
+    or as uint16 bit patterns; f16 data as f32 values (exact f16)."""
     torch = _torch()
     if dtype == "bf16":
         if a.dtype == np.uint16:
             t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
         else:
             t = torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16)
+    elif dtype == "f16":
+        t = torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.float16)
     else:
         t = torch.from_numpy(np.ascontiguousarray(a, np.float32))
     return t.to(device)
@@ -69,7 +71,7 @@ def upload(wl, device="cuda", kv_cache=None, q_pe=None) -> DeviceCase:
     torch = _torch()
     g = wl.geom
     dims = N.MlaDims.from_geometry(g)
-    tdt = torch.bfloat16 if g.dtype == "bf16" else torch.float32
+    tdt = {"bf16": torch.bfloat16, "f16": torch.float16}.get(g.dtype, torch.float32)
     rows = wl.rows
     H, R, W = g.n_head, g.kv_rank, g.width
     ws = N.mla_decode_workspace_size(wl.batch, wl.max_blocks, dims)

@@ -63,7 +63,7 @@ class Geometry:
     d_v: int
     kv_rank: int
     t_q: int
-    dtype: str  # "f32" or "bf16"
+    dtype: str  # "f32", "bf16" or "f16"
     block_size: int = BLOCK
 
     @property
@@ -80,7 +80,8 @@ class Workload:
     seq_lens: np.ndarray            # int32 [B]
     block_table: np.ndarray         # int32 [B, max_blocks]
     num_blocks: int
-    kv_cache: np.ndarray            # [num_blocks, bs, W]; float32, or uint16 bf16 bits
+    kv_cache: np.ndarray            # [num_blocks, bs, W]; float32 (f16-exact for f16),
+                                    # or uint16 bf16 bits
     q_nope: np.ndarray              # float32 [B*t_q, H, d_nope] (bf16-exact when bf16)
     q_pe: np.ndarray                # float32 [B*t_q, H, d_rope]
     w_uk: np.ndarray                # float32 [H, d_nope, kv_rank]
@@ -162,6 +163,21 @@ def bf16_bits(x: np.ndarray) -> np.ndarray:
     import torch
     t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
     return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def round_f16(x: np.ndarray) -> np.ndarray:
+    """Round f32 values to the nearest f16 (ties to even, numpy's cast);
+    return f32 values."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).astype(np.float32)
+
+
+def round_to(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Values rounded to a 16-bit dtype ("bf16", "f16") as f32; f32 unchanged."""
+    if dtype == "bf16":
+        return round_bf16(x)
+    if dtype == "f16":
+        return round_f16(x)
+    return np.asarray(x, np.float32)
 
 
 def bits_to_f32(bits: np.ndarray) -> np.ndarray:
@@ -279,6 +295,8 @@ def make_workload(name: str, seed: int | None = None, seq_lens=None,
         elif rope == "neox":
             kpe = apply_rope_neox(kpe, pos, 10000.0).astype(np.float32)
         rowsv = np.concatenate([ckv, kpe], axis=1) if P else ckv
+        if g.dtype == "f16":
+            rowsv = round_f16(rowsv)
         cache[c0:c1] = (bf16_bits(rowsv) if bf16 else rowsv).reshape(c1 - c0, bs, W)
 
     if rope == "norm":
@@ -288,11 +306,11 @@ def make_workload(name: str, seed: int | None = None, seq_lens=None,
     else:
         q_pe = q_pe_raw
 
-    if bf16:
-        q_nope, q_pe = round_bf16(q_nope), round_bf16(q_pe)
-        w_uk, w_uv = round_bf16(w_uk), round_bf16(w_uv)
+    if g.dtype != "f32":
+        q_nope, q_pe = round_to(q_nope, g.dtype), round_to(q_pe, g.dtype)
+        w_uk, w_uv = round_to(w_uk, g.dtype), round_to(w_uv, g.dtype)
 
-    poison_rows(cache, sl, bt, used, poison, bf16)
+    poison_rows(cache, sl, bt, used, poison, bf16, g.dtype == "f16")
     return Workload(name=name, geom=g, scale=1.0 / math.sqrt(g.d_nope + g.d_rope),
                     seq_lens=sl, block_table=bt, num_blocks=pool_blocks,
                     kv_cache=cache, q_nope=q_nope, q_pe=q_pe, w_uk=w_uk, w_uv=w_uv,
@@ -303,16 +321,18 @@ def make_workload(name: str, seed: int | None = None, seq_lens=None,
                           "poison": poison, "blocks_needed": need})
 
 
-def poison_value(poison: str, bf16: bool):
-    v = np.float32(1e30) if poison == "big" else np.float32(np.nan)
+def poison_value(poison: str, bf16: bool, f16: bool = False):
+    """A finite huge value (1e30; 60000 for f16, whose largest is 65504) or NaN."""
+    big = 60000.0 if f16 else 1e30
+    v = np.float32(big) if poison == "big" else np.float32(np.nan)
     return bf16_bits(np.array([v]))[0] if bf16 else v
 
 
-def poison_rows(cache, seq_lens, block_table, used, poison, bf16):
+def poison_rows(cache, seq_lens, block_table, used, poison, bf16, f16=False):
     """Overwrite every row no request may read with the poison value."""
     if poison == "none":
         return
-    val = poison_value(poison, bf16)
+    val = poison_value(poison, bf16, f16)
     cache[~used] = val
     bs = cache.shape[1]
     for b in range(seq_lens.shape[0]):
@@ -327,8 +347,8 @@ def neox_side_rope_columns(wl: Workload, permute_cols) -> tuple[np.ndarray, np.n
     permute_cols(x2d) must permute the last axis of a float32 [rows, d_rope]
     array in place with the NORM->NEOX load-time permutation. The permuted
     pre-rope values are then rotated with NEOX pairing at the same positions.
-    Returns (k_pe [num_blocks, bs, P] float32, q_pe [B*t_q, H, P] float32), bf16
-    rounded when the workload is bf16; unused cache rows keep the poison.
+    Returns (k_pe [num_blocks, bs, P] float32, q_pe [B*t_q, H, P] float32),
+    rounded to the workload's 16-bit type; unused cache rows keep the poison.
     """
     assert wl.rope == "norm"
     g = wl.geom
@@ -345,8 +365,7 @@ def neox_side_rope_columns(wl: Workload, permute_cols) -> tuple[np.ndarray, np.n
     k = apply_rope_neox(kraw, row_pos.reshape(-1), wl.rope_base).astype(np.float32)
     qpos = np.repeat(wl.q_pos, g.n_head)
     q = apply_rope_neox(qraw, qpos, wl.rope_base).astype(np.float32)
-    if g.dtype == "bf16":
-        k, q = round_bf16(k), round_bf16(q)
+    k, q = round_to(k, g.dtype), round_to(q, g.dtype)
     return k.reshape(wl.num_blocks, bs, P), q.reshape(wl.rows, g.n_head, P)
 
 
@@ -365,5 +384,5 @@ def cache_with_rope_columns(wl: Workload, k_pe: np.ndarray) -> np.ndarray:
         n = -(-int(wl.seq_lens[b]) // g.block_size)
         used[wl.block_table[b, :n]] = True
     poison_rows(cache, wl.seq_lens, wl.block_table, used, wl.meta["poison"],
-                g.dtype == "bf16")
+                g.dtype == "bf16", g.dtype == "f16")
     return cache

@@ -148,6 +148,27 @@ def test_decode_workspace_and_validation(lib):
     assert N.mla_decode_workspace_size(2, (1 << 27) - 1, d) > 0
 
 
+def test_f16_dims(lib):
+    """f16 geometries pass validation (workspace sizes are computed without a
+    GPU on the SIMT plan); the cache appends refuse an f16 cache before any
+    launch."""
+    d = N.MlaDims(4, 16, 8, 16, 32, 1, 16, N.MLA_F16)
+    assert N.mla_decode_workspace_size(2, 4, d) > 0
+    odd = N.MlaDims(4, 16, 4, 16, 32, 1, 16, N.MLA_F16)   # 8-byte rope rows
+    with pytest.raises(N.MlaError):
+        N.mla_absorb_q(16, 16, 16, 16, 1, odd, 0)
+    with pytest.raises(N.MlaError) as e:
+        N.mla_cache_append(256, 512, 768, 1024, 4, 2, N.MLA_F32, d, None, 0)
+    assert e.value.status == 2 and "f16" in N.mla_last_error()
+    with pytest.raises(N.MlaError) as e:
+        N.mla_cache_append_rmsnorm_rope(256, 512, 768, 1024, 1280, 1536, 4, 2, N.MLA_F32,
+                                        1e-6, 10000.0, d, None, 0)
+    assert e.value.status == 2
+    bad = N.MlaDims(4, 16, 8, 16, 32, 1, 16, 3)            # no such dtype
+    with pytest.raises(N.MlaError):
+        N.mla_decode_workspace_size(2, 4, bad)
+
+
 def test_cache_append_rmsnorm_rope_validation(lib):
     """Argument checks of the fused append, all before any launch."""
     d = N.MlaDims(4, 16, 8, 16, 32, 1, 16, N.MLA_BF16)

@@ -6,6 +6,10 @@ Tolerances (the parity gates, written here):
                the storage quantum of a bf16 output, which a flat 1e-2 cannot
                cover once |ref| >= 2.5); LSE (f32): max abs diff <= 1e-3;
                a -inf LSE must be -inf on both sides.
+  f16 inputs   outputs: |gpu - ref| <= 2e-3 + 2^-10 |ref|: the bf16 gate scaled
+               by f16's finer quantum (f16 keeps 3 more mantissa bits, so its
+               roundings of P and of the output are 8x smaller), the second
+               term again one storage quantum; LSE as for bf16.
 The oracle runs on the same (bf16-rounded) values the GPU stage consumed: each
 stage's input comes from the generator or from the oracle's previous stage,
 never from the GPU.
@@ -24,6 +28,8 @@ ATOL_F32 = 1e-4
 ATOL_BF16 = 1e-2
 RTOL_BF16 = 2.0 ** -8
 ATOL_LSE_BF16 = 1e-3
+ATOL_F16 = 2e-3
+RTOL_F16 = 2.0 ** -10
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -41,6 +47,8 @@ def assert_close(got, ref, dtype, what):
     err = np.abs(got - ref)
     if dtype == "f32":
         bound = ATOL_F32
+    elif dtype == "f16":
+        bound = ATOL_F16 + RTOL_F16 * np.abs(ref)
     else:
         bound = ATOL_BF16 + RTOL_BF16 * np.abs(ref)
     bad = err > bound
@@ -59,7 +67,7 @@ def assert_lse_close(got, ref, dtype, what):
 
 
 def rounded(x, dtype):
-    return W.round_bf16(x) if dtype == "bf16" else np.asarray(x, np.float32)
+    return W.round_to(x, dtype)
 
 
 def gpu_sides(wl):
