@@ -1,6 +1,6 @@
 // Thin inline-PTX wrappers for the sm_100-family features the tensor-core
-// kernels use: mbarriers (with bounded waits), TMA tensor copies (plain and
-// cluster multicast), cluster shared-memory addressing, and tcgen05 (TMEM
+// kernels use: mbarriers (with bounded waits), TMA tensor copies into this
+// CTA's own shared memory, cluster shared-memory addressing, and tcgen05 (TMEM
 // allocation, MMA, commit, loads and stores).
 //
 // Encodings follow the PTX ISA's tcgen05 instruction descriptor (kind::f16)
@@ -161,17 +161,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
         "l"(m), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
-// 3-D tiled load multicast to the CTAs in `mask` (same smem offsets in each;
-// each destination's barrier at offset `bar` receives the complete_tx)
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* m, uint32_t bar,
-                                               int c0, int c1, int c2, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-        "l"(m), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(mask)
-        : "memory");
-}
-
 // ----------------------------------------------------------------- tcgen05
 // Instruction descriptor, kind::f16 with bf16 A and B and f32 D.
 // a_mn / b_mn: operand is MN-major (1) or K-major (0).
@@ -250,15 +239,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
         : "memory");
 }
-// same, arriving on the barrier at offset `bar` in every CTA of `mask`
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster"
-        ".b64 [%0], %1;" ::"r"(bar),
-        "h"(mask)
-        : "memory");
-}
-
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }

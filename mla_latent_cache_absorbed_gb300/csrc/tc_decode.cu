@@ -86,12 +86,12 @@ struct __align__(16) AlphaMsg {
 struct Ctrl {
     AlphaMsg amsg[2];       // O: the messages of the two P slots
     uint64_t full[kNS];     // both: this CTA's part of the tile landed (complete_tx)
-    uint64_t kfree[kNS];    // O: the S-CTA's stage is free (its QK commit, multicast)
-    uint64_t qmoved;        // O: the S-CTA's first queries have left stages 1-2 (1 remote)
+    uint64_t pdone[2];      // O: the P*V reading P slot i finished (MMA commit); the
+                            //    relay warp passes it on to the S-CTA's pempty
     uint64_t empty[kNS];    // both: stage free (own QK / P*V commit)
     uint64_t sfull[2];      // S: scores ready (QK commit)
     uint64_t sfree[2];      // S: scores read (the 256 softmax threads)
-    uint64_t pempty[2];     // S: P slot consumed (O-CTA PV commit)
+    uint64_t pempty[2];     // S: P slot consumed (the O-CTA's relay, 1 remote arrival)
     uint64_t qready;        // S: Q stored in TMEM (256 softmax threads)
     uint64_t qland;         // S: first segment's queries landed in shared memory (TMA)
     uint64_t qfree;         // S: those queries are in TMEM; stages 1-2 reusable (256)
@@ -302,8 +302,7 @@ __device__ __forceinline__ int valid_blocks(const Walk& w) {
 
 // ------------------------------------------------------------------ kernel
 // Role map (13 warps per CTA):
-//   S-CTA  warps 0-3  K loaders: warp k expects block k of each tile; warps 0-1
-//                     load blocks 0-1 (3-D boxes), the O-CTA's warp 3 blocks 2-3
+//   S-CTA  warps 0-3  K loaders: warp k loads block k of each tile (3-D boxes)
 //          warp 4     S = Q K^T MMA issuer; owns the TMEM allocation
 //          warps 5-12 softmax, two threads per query row (32 score columns
 //                     each); P goes to the O-CTA by st.async
@@ -314,8 +313,8 @@ __device__ __forceinline__ int valid_blocks(const Walk& w) {
 //          warp 4     O += P V MMA issuer; owns the TMEM allocation
 //          warps 5-12 rescale and epilogue: warp w takes the TMEM lanes of
 //                     its quadrant (w % 4) and half the 512 columns
-//          warp 3     K helper: loads blocks 2-3 of each S-CTA tile (multicast
-//                     to the S-CTA only), so both TMA units share the boxes
+//          warp 3     relay: passes each P*V completion (its own barrier) on to
+//                     the S-CTA's P-slot barrier by a remote mbarrier arrive
 // In both CTAs warp 2 first works out the pair's unit range (walk_init) while
 // the barriers and TMEM are set up; every warp then follows that walk.
 template <int W, bool kF16>
@@ -341,17 +340,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&c.full[s]), rank == 0 ? 4 : 1);  // S: one per K loader
             mbar_init(smem_u32(&c.empty[s]), 1);
             mbar_init(smem_u32(&c.vready[s]), 1);
-            mbar_init(smem_u32(&c.kfree[s]), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&c.sfull[i]), 1);
             mbar_init(smem_u32(&c.sfree[i]), kSmxWarps * 32);
             mbar_init(smem_u32(&c.pempty[i]), 1);
             mbar_init(smem_u32(&c.pfull[i]), 1);
+            mbar_init(smem_u32(&c.pdone[i]), 1);
         }
         mbar_init(smem_u32(&c.qready), 256);
         mbar_init(smem_u32(&c.qland), 1);
-        mbar_init(smem_u32(&c.qmoved), 1);
         mbar_init(smem_u32(&c.qfree), 256);
         mbar_init(smem_u32(&c.statack), 1);
         mbar_init(smem_u32(&c.odone), 1);
@@ -454,7 +452,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const bool have = kb < valid_blocks(w);
                     mbar_arrive_expect_tx(smem_u32(&c.full[s]), have ? (uint32_t)(NKC * 2048) : 0u);
                     last_issue[s] = i;
-                    if (have && kb < 2) {
+                    if (have) {
                         int32_t blk = p.block_table[(long long)w.b * p.max_blocks + w.tile * 4 + kb];
                         if (blk < 0 || blk >= p.num_blocks) {
                             // load a valid stand-in; the row threads void the segment
@@ -488,7 +486,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const int buf = (int)(i & 1);
                     if (seg_first(w, ub)) {
                         if (!wt.wait(smem_u32(&c.qready), (uint32_t)(seg & 1))) break;
-                        if (seg == 0) mbar_arrive_remote(mapa(smem_u32(&c.qmoved), 1));
                         ++seg;
                     }
                     if (!wt.wait(smem_u32(&c.full[s]), (uint32_t)((i / kNS) & 1))) break;
@@ -506,7 +503,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     mma_commit(smem_u32(&c.sfull[buf]));
                     mma_commit(smem_u32(&c.empty[s]));
-                    mma_commit_mc(smem_u32(&c.kfree[s]), 0x2);  // the O-CTA's helper
                 }
             }
         } else if (warp >= 5) {
@@ -773,33 +769,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
             }
         } else if (warp == 3) {
-            // ---------------- K helper: blocks 2-3 of each tile into the S-CTA's
-            // stage (multicast with only the S-CTA in the mask; its full[s]
-            // receives the bytes), once the S-CTA's QK has freed the stage
+            // ---------------- relay: once the P*V that read P slot i & 1 has
+            // finished (this CTA's pdone), the S-CTA may refill the slot: one
+            // remote arrival on its pempty per tile
             if (elect_one()) {
+                const uint32_t pempty_remote = mapa(smem_u32(&c.pempty[0]), 0);
                 long long i = 0;
                 for (; w.u < w.u_end; walk_next(p, w), ++i) {
-                    const int s = (int)(i % kNS);
-                    if (!wt.wait(smem_u32(&c.kfree[s]), (uint32_t)((i / kNS) & 1) ^ 1)) break;
-                    if (i == 1 || i == 2)  // stages 1-2 held the S-CTA's first queries
-                        if (!wt.wait(smem_u32(&c.qmoved), 0)) break;
-                    const int nb = valid_blocks(w);
-                    const int32_t* bt = p.block_table + (long long)w.b * p.max_blocks + w.tile * 4;
-                    for (int kb = 2; kb < nb; ++kb) {
-                        int32_t blk = bt[kb];
-                        if (blk < 0 || blk >= p.num_blocks) {
-                            // load a valid stand-in; the softmax threads void the segment
-                            if (p.dev_err) atomicOr(p.dev_err, (int32_t)MLA_DEVERR_BAD_BLOCK);
-                            blk = 0;
-                        }
-#pragma unroll
-                        for (int ch = 0; ch < 8; ++ch)
-                            tma_load_3d_mc(smem_u32(smem + s * kStage + ch * kChunk + kb * 2048), &tmap,
-                                           smem_u32(&c.full[s]), ch * 64, 0, blk, 0x1);
-                        if (NKC == 9)
-                            tma_load_3d_mc(smem_u32(smem + kSideOff + s * kChunk + kb * 2048), &tmap,
-                                           smem_u32(&c.full[s]), 512, 0, blk, 0x1);
-                    }
+                    const int slot = (int)(i & 1);
+                    if (!wt.wait(smem_u32(&c.pdone[slot]), (uint32_t)((i >> 1) & 1))) break;
+                    mbar_arrive_remote(pempty_remote + slot * 8);
                 }
             }
         } else if (warp == 2) {
@@ -876,7 +855,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     // the last tile of a segment keeps its stage: the epilogue stages
                     // the output there, then releases it
                     if (!last) mma_commit(smem_u32(&c.empty[s]));
-                    mma_commit_mc(smem_u32(&c.pempty[slot]), 0x1);
+                    mma_commit(smem_u32(&c.pdone[slot]));  // the relay tells the S-CTA
                     if (last) {
                         mma_commit(smem_u32(&c.odone));
                         if (!wt.wait(smem_u32(&c.odone), (uint32_t)(ndone & 1))) break;
