@@ -83,9 +83,12 @@ def page(rows_f32, seq_lens, rng, bs=16, spare=3, poison=1e30):
 
 
 # ------------------------------------------------------------------ pins
-# the two forms must agree to 1e-4 relative (of max(max |out|, 1)), the gate
-# the method's statement sets for naive against absorbed
-FORMS_RTOL = 1e-4
+# the two forms must agree relative to max(max |out|, 1): to 1e-5 on small
+# shapes and to 1e-4 at full model dims, the two gates the mla.rs unit tests
+# set for naive against absorbed (its small-shape cases and its full-dims
+# cases respectively)
+FORMS_RTOL = 1e-5
+FORMS_RTOL_FULL_DIMS = 1e-4
 
 
 def check_naive_equals_absorbed(lib):
@@ -118,7 +121,7 @@ def check_naive_equals_absorbed_full_dims(lib):
         scale = 1.0 / math.sqrt(Dn + P)
         a = oracle.attend_naive(*args, scale, lib=lib)
         b = oracle.attend_absorbed(*args, scale, lib=lib)
-        assert rel_ok(a, b, FORMS_RTOL), (H, Dn, P, maxdiff(a, b))
+        assert rel_ok(a, b, FORMS_RTOL_FULL_DIMS), (H, Dn, P, maxdiff(a, b))
 
 
 def _chain(lib, q_nope, q_pe, w_uk, w_uv, cache, bt, seq_lens, t_q, R, scale):
