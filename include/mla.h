@@ -190,8 +190,10 @@ mla_status mla_decode_paged(void* out, float* lse, const void* q_abs,
  *     batch needs more scratch than MLA_STATIC_SCRATCH_BYTES
  *     (mla_decode_workspace_size tells the need); nothing is enqueued then.
  *   - The first call on a device looks up the array's device address (and
- *     loads the library's module there if needed); make that first call
- *     before any stream capture on that device.
+ *     loads the library's module there if needed) and keeps it for the life
+ *     of the process; make that first call before any stream capture on that
+ *     device. A cudaDeviceReset destroys the context that address belongs to:
+ *     do not call this entry point on a device after resetting it.
  *   - All calls on a device share the array, which keeps the last call's
  *     contents (nothing in it needs clearing between calls). Calls whose GPU
  *     work overlaps race on it: issue them on one stream or order them.

@@ -31,7 +31,10 @@ void* g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of g_decode_scratch on the current device. The first call
 // on a device resolves it (cudaGetSymbolAddress also loads the module there
-// if it is not loaded yet); later calls reuse the cached address.
+// if it is not loaded yet); later calls reuse the cached address. The address
+// belongs to the device's context: after a cudaDeviceReset the module loads
+// again in a new context, possibly elsewhere, so the entry point is not for
+// use on a device that has been reset (its header says so).
 mla_status scratch_address(void** out) {
     int dev = -1;
     MLA_CUDA_TRY(cudaGetDevice(&dev), "cudaGetDevice");
