@@ -3,15 +3,21 @@
 
 One step = one pass of the whole path (absorb -> paged decode with split
 combine -> decompress) over one batch of the workload, as one decoding layer
-would run it. Default workload: GLM-5.2 dims decode (H=64, d_nope 192, d_rope
-64, d_v 256, kv_rank 512, bf16, batch 8, seq_lens U[1,4096] with one empty
-request, 16-row blocks). The KV cache stays resident in HBM (it is the
-server's state); each layer of a model has its own cache, so the benchmark
-cycles through NL distinct layers (own cache and weights, shared block table)
-whose total exceeds 4x the L2 size: every step reads its operands from HBM.
+would run it. The headline workload is the largest of the five: GLM-5.2 dims
+causal multi-token decode (H=64, d_nope 192, d_rope 64, d_v 256, kv_rank 512,
+bf16, t_q=4, batch 32, seq_lens U[8192, 65536], 16-row blocks, interleaved
+rope permuted to NEOX at load). The default run also measures the other four
+workloads (tiny f32, GLM-5.2 decode, DeepSeek-V3 geometry, GLM-5.3-Flash
+NoPE) the same way and reports them under "per_config".
+
+The KV cache stays resident in HBM (it is the server's state); each layer of
+a model has its own cache, so the benchmark cycles through NL distinct layers
+(own cache and weights, shared block table) whose total exceeds 4x the L2
+size, or one layer when one layer's cache alone does: every step reads its
+operands from HBM.
 
 Prints ONE JSON line (rank 0). --impl reference runs the CPU oracle instead,
-on a bounded sample of the same workload, on the host cores.
+on a bounded sample of the headline workload, on the host cores.
 """
 from __future__ import annotations
 
@@ -32,6 +38,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MLA decode tokens/s/GPU & µs/layer; % of max(HBM, bf16-tensor) roofline"
+HEADLINE = "glm52_causal_t4"
+ALL_CONFIGS = ("tiny_f32", "glm52_decode", "deepseek_decode", "glm53_flash_nope",
+               "glm52_causal_t4")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -190,12 +199,34 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- oracle (CPU) leg
-def oracle_sample(wl, budget_s: float, threads: int):
-    """Time the CPU oracle's full path on a bounded sample of query rows.
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or None."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
 
-    The absorb and decompress run on every row; the decode on a growing set
-    of query rows (spread over all requests and heads) until the budget is
-    used. Returns (tokens/s estimate for the whole step, description, threads).
+
+def oracle_sample(wl, budget_s: float, threads: int):
+    """Time the CPU oracle's full path on a bounded sample of the step.
+
+    The absorb and the decompress run on a sample of query rows (all rows
+    when few), the decode on a growing random set of (query row, head) pairs
+    spread over all requests, until the budget is used; each part's time is
+    scaled to the whole step. The oracle runs as it stands: its decode is
+    called from `threads` host threads on disjoint pairs (the C code releases
+    the GIL), the absorb and the decompress are single calls. Returns
+    (tokens/s estimate for the whole step, description, threads, step seconds).
     """
     import oracle
     from concurrent.futures import ThreadPoolExecutor
@@ -203,22 +234,29 @@ def oracle_sample(wl, budget_s: float, threads: int):
     g = wl.geom
     H, R, T = g.n_head, g.kv_rank, g.t_q
     lib = oracle.load()
+    nr = min(wl.rows, 16)
     t0 = time.perf_counter()
-    q_abs = oracle.absorb_q(wl.q_nope, wl.q_pe, wl.w_uk, lib=lib)
-    t_abs = time.perf_counter() - t0
-    q_abs = W.round_bf16(q_abs) if g.dtype == "bf16" else q_abs
-    q4 = q_abs.reshape(wl.batch, T, H, -1)
+    oracle.absorb_q(wl.q_nope[:nr], wl.q_pe[:nr], wl.w_uk, lib=lib)
+    t_abs = (time.perf_counter() - t0) * wl.rows / nr
+    # the decode's queries for every row (the sampled decode reads any row):
+    # the same absorb, untimed, worked out once per workload
+    q4 = getattr(wl, "_oracle_q_abs", None)
+    if q4 is None:
+        q_abs = oracle.absorb_q(wl.q_nope, wl.q_pe, wl.w_uk, lib=lib)
+        q_abs = W.round_to(q_abs, g.dtype) if g.dtype != "f32" else q_abs
+        q4 = q_abs.reshape(wl.batch, T, H, -1)
+        wl._oracle_q_abs = q4
     total_rows = wl.rows * H
     rng = np.random.default_rng(0)
     order = rng.permutation(total_rows)
     chunk = max(1, min(64, total_rows // max(1, threads)))
     done = 0
-    t0 = time.perf_counter()
 
     def work(ids):
         oracle.decode_rows(q4, wl.kv_cache, wl.block_table, wl.seq_lens, T, R, wl.scale,
                            ids, lib=lib, allow_errors=True)
 
+    t0 = time.perf_counter()
     with ThreadPoolExecutor(threads) as ex:
         while done < total_rows and time.perf_counter() - t0 < budget_s:
             batch = [order[done + i * chunk: done + (i + 1) * chunk] for i in range(threads)]
@@ -227,15 +265,25 @@ def oracle_sample(wl, budget_s: float, threads: int):
             done += sum(b.size for b in batch)
     t_dec = time.perf_counter() - t0
     frac = done / total_rows
-    o_in = np.zeros((wl.rows, H, R), np.float32)
+    o_in = np.zeros((nr, H, R), np.float32)
     t0 = time.perf_counter()
     oracle.decompress(o_in, wl.w_uv, lib=lib)
-    t_dcp = time.perf_counter() - t0
+    t_dcp = (time.perf_counter() - t0) * wl.rows / nr
     t_step = t_abs + t_dec / frac + t_dcp
-    desc = (f"absorb and decompress on all {wl.rows} query rows x {H} heads; decode on "
-            f"{done} of {total_rows} (query row, head) pairs ({100 * frac:.2f}%), "
-            f"extrapolated to the whole step")
+    desc = (f"absorb and decompress timed on {nr} of {wl.rows} query rows x {H} heads; "
+            f"decode on {done} of {total_rows} (query row, head) pairs ({100 * frac:.2f}%) "
+            f"from {threads} host thread(s); each part scaled to the whole step")
     return wl.rows / t_step, desc, threads, t_step
+
+
+def cpu_baseline(wl, budget_s: float):
+    """The oracle on all host cores and on one, each on a bounded sample."""
+    threads = os.cpu_count() or 1
+    v, desc, threads, _ = oracle_sample(wl, budget_s, threads)
+    v1, desc1, _, _ = oracle_sample(wl, max(1.0, budget_s / 3), 1)
+    return {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": desc, "cpu_model": cpu_model(),
+            "single_thread": {"value": v1, "unit": "tokens/s", "cores": 1, "sample": desc1}}
 
 
 def run_reference(args, wl):
@@ -245,7 +293,7 @@ def run_reference(args, wl):
     threads = os.cpu_count() or 1
     vals = []
     desc = ""
-    budget = max(2.0, min(20.0, 60.0 / max(1, args.steps + args.warmup)))
+    budget = max(1.0, min(20.0, 60.0 / max(1, args.steps + args.warmup)))
     for i in range(args.warmup + args.steps):
         v, desc, threads, t_step = oracle_sample(wl, budget, threads)
         if i >= args.warmup:
@@ -257,59 +305,68 @@ def run_reference(args, wl):
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": config_dict(wl, world=1),
+        "config": config_dict(wl, world=1, nl=None),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
-                         "kind": "oracle", "sample": desc},
+                         "kind": "oracle", "sample": desc, "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
 
 
-def config_dict(wl, world):
+def layer_count(per_layer_bytes, l2_bytes):
+    """Distinct layers the timed loop cycles through: one when a layer's
+    operands alone exceed 4x L2, else enough to exceed it together (2..64)."""
+    if per_layer_bytes >= 4 * l2_bytes:
+        return 1
+    return max(2, min(64, math.ceil(4 * l2_bytes / max(1, per_layer_bytes))))
+
+
+def stage_steps(nl, steps):
+    """Steps the per-stage timing replays: whole passes over the nl layers
+    (so only the pre-captured full graph runs between the events), at least
+    one pass and about as many steps as the timed loop, at most 20 passes."""
+    return nl * max(1, min(steps, 20 * nl) // nl)
+
+
+def config_dict(wl, world, nl):
     g = wl.geom
+    if nl is None:
+        l2 = "CPU run"
+    elif nl * (wl.kv_cache.nbytes + wl.w_uk.nbytes // 2 + wl.w_uv.nbytes // 2) > (1 << 29):
+        l2 = ("inputs larger than L2: steps cycle through distinct per-layer caches and "
+              "weights totalling > 4x L2")
+        if nl == 1:
+            l2 = "inputs larger than L2: one layer's cache alone exceeds 4x L2"
+    else:
+        l2 = "parity-size workload: its working set fits in L2"
     return {"workload": f"{wl.name}: H={g.n_head} d_nope={g.d_nope} d_rope={g.d_rope} "
                         f"d_v={g.d_v} kv_rank={g.kv_rank} t_q={g.t_q} {g.dtype} "
                         f"batch={wl.batch} block=16",
             "batch": wl.batch, "t_q": g.t_q,
             "seq_lens_sum": int(wl.seq_lens.sum()), "seq_lens_max": int(wl.seq_lens.max()),
-            "l2": "inputs larger than L2: steps cycle through distinct per-layer caches and "
-                  "weights totalling > 4x L2",
+            "l2": l2,
             "parallelism": f"replicas x{world} (requests shard, no collective)"}
 
 
 # ---------------------------------------------------------------- GPU leg
-def run_ours(args, wl):
+def measure_config(args, wl, dev, stream, peaks, peaks_src, world, sample_clocks):
+    """Time one workload: the fused step (the headline value), each stage as
+    its own call, the decode's roofline fraction and the e2e rate."""
     import torch
     import torch.distributed as dist
-    from mla_latent_cache_absorbed_gb300 import _native as N
     from mla_latent_cache_absorbed_gb300 import device as D
-    from mla_latent_cache_absorbed_gb300 import workloads as W
 
-    rank, world, local = dist_env()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=dev)
-    N.load()
     g = wl.geom
-    peaks, peaks_src = load_peaks()
-
+    local = dev.index
     # layers: distinct caches / weights / queries, shared block table
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     per_layer = (wl.kv_cache.nbytes + wl.w_uk.nbytes // 2 + wl.w_uv.nbytes // 2)
-    nl = max(2, min(64, math.ceil(4 * l2 / max(1, per_layer))))
-    base = D.upload(wl, device=dev)
-    layers = [base]
-    for i in range(1, nl):
-        c = D.upload(wl, device=dev)  # same values, distinct memory
-        layers.append(c)
+    nl = layer_count(per_layer, l2)
+    layers = [D.upload(wl, device=dev) for _ in range(nl)]  # same values, distinct memory
     for c in layers:
         D.attend_workspace(c)  # allocated before any graph capture
     torch.cuda.synchronize()
-
-    stream = torch.cuda.Stream(device=dev)
-    torch.cuda.set_stream(stream)
 
     def step(k, which="all"):
         # the step is the fused call a decode step makes; the stage timings
@@ -336,64 +393,69 @@ def run_ours(args, wl):
                 step(k, which)
         return gr
 
+    # every graph a timed region replays is captured before it starts
     g_full = capture(nl)
+    graphs = {}
 
-    def replay(graph_full, n_steps, graph_rem_cache):
-        full, rem = divmod(n_steps, nl)
-        for _ in range(full):
+    def prepare(n_steps, which="all"):
+        rem = n_steps % nl
+        if rem and (which, rem) not in graphs:
+            graphs[(which, rem)] = capture(rem, which)
+
+    def replay(graph_full, n_steps, which="all"):
+        for _ in range(n_steps // nl):
             graph_full.replay()
-        if rem:
-            if rem not in graph_rem_cache:
-                graph_rem_cache[rem] = capture(rem, graph_rem_cache["which"])
-            graph_rem_cache[rem].replay()
+        if n_steps % nl:
+            graphs[(which, n_steps % nl)].replay()
 
-    rem_all = {"which": "all"}
     # timing probe to choose K when not given
-    replay(g_full, nl, rem_all)
+    replay(g_full, nl)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    replay(g_full, 4 * nl, rem_all)
+    replay(g_full, 4 * nl)
     torch.cuda.synchronize()
     est = (time.perf_counter() - t0) / (4 * nl)
     steps = args.steps if args.steps else int(min(200000, max(100, 2.0 / max(est, 1e-7))))
     warmup = max(3, args.warmup)
 
-    replay(g_full, warmup, rem_all)
-    if steps % nl and (steps % nl) not in rem_all:
-        rem_all[steps % nl] = capture(steps % nl)
+    prepare(warmup)
+    prepare(steps)
+    replay(g_full, warmup)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    sampler = ClockSampler(local)
-    sampler.start()
+    sampler = ClockSampler(local) if sample_clocks else None
+    if sampler:
+        sampler.start()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     ev0.record(stream)
-    replay(g_full, steps, rem_all)
+    replay(g_full, steps)
     ev1.record(stream)
     torch.cuda.synchronize()
     ms_total = ev0.elapsed_time(ev1)
-    clocks = sampler.stop()
+    clocks = sampler.stop() if sampler else None
     if world > 1:
         ms_total = max_over_ranks(ms_total, dev)
         dist.barrier()
     ms_per_step = ms_total / steps
     value = whole_job_rate(wl.rows, world, steps, ms_total)
 
-    # per-stage kernel times (same layers, same launch configuration)
+    # per-stage kernel times (same layers, same launch configuration): whole
+    # passes over the layers, all graphs captured before the events
     stage_ms = {}
+    n_stage = stage_steps(nl, steps)
     for which in ("absorb", "decode", "decompress"):
         gs = capture(nl, which)
-        rem = {"which": which}
-        n = max(nl, min(steps, 20 * nl))
-        replay(gs, nl, rem)
+        replay(gs, nl, which)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        replay(gs, n, rem)
+        replay(gs, n_stage, which)
         e1.record(stream)
         torch.cuda.synchronize()
-        stage_ms[which] = e0.elapsed_time(e1) / n
+        stage_ms[which] = e0.elapsed_time(e1) / n_stage
+        del gs
     alg = algorithmic(wl)
     dominant = max(stage_ms, key=stage_ms.get)
     dom_bytes, dom_flops = alg[dominant]
@@ -423,37 +485,96 @@ def run_ours(args, wl):
     t_roof = max(dec_bytes / (hbm_peak * 1e9), dec_flops / (tc_peak * 1e12))
     decode_roofline = {"us_per_layer": stage_ms["decode"] * 1e3,
                        "roofline_us": t_roof * 1e6, "frac": t_roof / dec_s,
+                       "bound": "tensor" if dec_flops / (tc_peak * 1e12) > dec_bytes / (hbm_peak * 1e9)
+                       else "hbm",
                        "bytes": dec_bytes, "flops": dec_flops}
-
-    # the next row of the path: appending new tokens' latent rows to the cache
-    cache_append = measure_cache_append(wl, base, stream, hbm_peak)
+    del g_full
+    graphs.clear()
 
     # end to end through the C ABI with host buffers
     e2e = run_e2e(args, wl, layers, stream, nl, steps)
+    res = {"value": value, "unit": "tokens/s", "steps": steps, "warmup": warmup,
+           "ms_per_step": ms_per_step, "us_per_layer": ms_per_step * 1e3,
+           "dtype": g.dtype, "config": config_dict(wl, world, nl),
+           "roofline": roof, "decode_roofline": decode_roofline, "stages_ms": stage_ms,
+           "e2e": e2e, "gpu_launches": steps * LAUNCHES_PER_STEP(wl), "layers": nl,
+           "clocks": clocks}
+    return res, layers
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from mla_latent_cache_absorbed_gb300 import _native as N
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    N.load()
+    peaks, peaks_src = load_peaks()
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
+
+    headline = args.config or HEADLINE
+    names = [headline] if args.config else [c for c in ALL_CONFIGS if c != headline] + [headline]
+    per_config = {}
+    head = None
+    for name in names:
+        wl = make_bench_workload(name, args.batch, rank)
+        res, layers = measure_config(args, wl, dev, stream, peaks, peaks_src, world,
+                                     sample_clocks=(name == headline))
+        if name == headline:
+            head = (wl, res, layers)
+        else:
+            del layers
+            torch.cuda.empty_cache()
+        per_config[name] = {k: res[k] for k in ("value", "unit", "ms_per_step", "us_per_layer",
+                                                "dtype", "decode_roofline", "stages_ms", "e2e",
+                                                "layers")}
+        per_config[name]["workload"] = res["config"]["workload"]
+        per_config[name]["l2"] = res["config"]["l2"]
+    wl, res, layers = head
+    g = wl.geom
+
+    # the next row of the path: appending new tokens' latent rows to the cache
+    cache_append = measure_cache_append(wl, layers[0], stream, peaks["hbm_gbs"])
 
     # CPU baseline (rank 0, N = 1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, desc, threads, _ = oracle_sample(wl, args.cpu_budget, os.cpu_count() or 1)
-        cpu = {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "sample": desc}
+        cpu = cpu_baseline(wl, args.cpu_budget)
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": steps, "warmup": warmup, "ms_per_step": ms_per_step,
-            "us_per_layer": ms_per_step * 1e3,
+            "metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": world,
+            "steps": res["steps"], "warmup": res["warmup"], "ms_per_step": res["ms_per_step"],
+            "us_per_layer": res["us_per_layer"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if g.dtype == "bf16" else "f32", "data": "synthetic",
-            "config": config_dict(wl, world),
-            "roofline": roof, "decode_roofline": decode_roofline,
-            "stages_ms": stage_ms, "e2e": e2e, "cpu_baseline": cpu,
-            "gpu_launches": steps * LAUNCHES_PER_STEP(wl),
-            "clocks": clocks, "layers": nl, "cache_append": cache_append,
+            "dtype": "bf16" if g.dtype == "bf16" else g.dtype, "data": "synthetic",
+            "config": res["config"],
+            "roofline": res["roofline"], "decode_roofline": res["decode_roofline"],
+            "stages_ms": res["stages_ms"], "e2e": res["e2e"], "cpu_baseline": cpu,
+            "gpu_launches": res["gpu_launches"],
+            "clocks": res["clocks"], "layers": res["layers"], "cache_append": cache_append,
+            "per_config": per_config,
         }
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
+
+
+def make_bench_workload(name, batch, rank):
+    """The named workload (rank > 0: an independent batch of the same shape);
+    with `batch`, only its first `batch` requests (profiling captures)."""
+    from mla_latent_cache_absorbed_gb300 import workloads as W
+    seed = rank_seed(rank)
+    if batch:
+        s = W._SEEDS[name] if seed is None else seed
+        sl = W.default_seq_lens(name, np.random.default_rng(s))[:batch]
+        return W.make_workload(name, seed=seed, seq_lens=sl)
+    return W.make_workload(name, seed=seed)
 
 
 def measure_cache_append(wl, dc, stream, hbm_peak):
@@ -630,26 +751,44 @@ def run_e2e(args, wl, layers, stream, nl, steps):
                       "form one captured CUDA graph"}
 
 
+def spawn_ranks(n):
+    """`--gpus N` without a launcher: run this command as N ranks (one per
+    GPU) under torch.distributed.run on this node and return its exit code."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr=127.0.0.1",
+           f"--master-port={29500 + os.getpid() % 1000}", os.path.abspath(__file__),
+           *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__)
-    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--gpus", type=int, default=1,
+                    help="ranks (one per GPU); without a launcher, N > 1 starts them itself")
     ap.add_argument("--steps", type=int, default=0, help="timed steps (default: ~2 s worth)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="glm52_decode")
-    ap.add_argument("--cpu-budget", type=float, default=15.0,
+    ap.add_argument("--config", default=None,
+                    help=f"one workload only (default: the headline {HEADLINE} plus the "
+                         f"other four under per_config)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="only the workload's first N requests (smaller profiling cases)")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle decode work in the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
-    from mla_latent_cache_absorbed_gb300 import workloads as W
     rank, world, _ = dist_env()
-    wl = W.make_workload(args.config, seed=rank_seed(rank))
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        sys.exit(spawn_ranks(args.gpus))
+    if "WORLD_SIZE" in os.environ and args.gpus != world:
+        sys.exit(f"--gpus {args.gpus} but the launcher started {world} ranks")
     if args.impl == "reference":
         if args.steps == 0:
             args.steps = 3
-        run_reference(args, wl)
+        if rank == 0:  # the other ranks exit without work
+            run_reference(args, make_bench_workload(args.config or HEADLINE, args.batch, rank))
     else:
-        run_ours(args, wl)
+        run_ours(args)
 
 
 if __name__ == "__main__":

@@ -81,3 +81,37 @@ def test_named_workload_work():
             W.default_seq_lens(name, np.random.default_rng(0))[:3]
         wl = W.make_workload(name, seq_lens=lens)
         assert bench.algorithmic(wl)["decode"] == brute_force(wl), name
+
+
+def test_stage_timing_replays_whole_passes():
+    """The per-stage timing replays only the full-pass graph captured before
+    its events: its step count is a whole number of passes over the layers."""
+    for nl in (1, 2, 3, 12, 64):
+        for steps in (1, 5, 8, 20, 100, 1000):
+            n = bench.stage_steps(nl, steps)
+            assert n % nl == 0 and n >= nl and n <= 20 * nl
+
+
+def test_layer_count():
+    """One layer when its operands alone exceed 4x L2; otherwise enough
+    distinct layers to exceed it together (at least two, at most 64)."""
+    l2 = 129 << 20
+    assert bench.layer_count(4 * l2, l2) == 1
+    assert bench.layer_count(10 * l2, l2) == 1
+    assert bench.layer_count(l2, l2) == 4
+    assert bench.layer_count(3 * l2, l2) == 2
+    assert bench.layer_count(1, l2) == 64
+    for per in (1 << 20, 20 << 20, 300 << 20):
+        n = bench.layer_count(per, l2)
+        assert n * per >= 4 * l2 or n == 64
+
+
+def test_default_run_covers_every_workload_with_the_largest_as_headline():
+    assert set(bench.ALL_CONFIGS) == {"tiny_f32", "glm52_decode", "deepseek_decode",
+                                      "glm53_flash_nope", "glm52_causal_t4"}
+    sizes = {}
+    for name in bench.ALL_CONFIGS:
+        lens = W.default_seq_lens(name, np.random.default_rng(W._SEEDS[name]))
+        g = W.geometry(name)
+        sizes[name] = int(lens.sum()) * g.width * (2 if g.dtype == "bf16" else 4)
+    assert bench.HEADLINE == max(sizes, key=sizes.get)
