@@ -332,6 +332,25 @@ mla_status mla_permute_rope_cols(void* x, int32_t elem_bytes, int64_t rows,
 mla_status mla_permute_rope_rows(void* w, int32_t elem_bytes, int64_t row_len,
                                  int32_t row0, int32_t n_dims);
 
+/*
+ * Test hook for the decode's timeout path; the pages have no counterpart (the
+ * CPU kernel of "vllm.cpp cpu_mla_attn.cpp" aborts the process on bad input,
+ * which a GPU kernel cannot do; this library's kernels give every wait a time
+ * limit instead, and report a wait that gave up in dev_err).
+ *   limit_ns  the limit of every bounded wait of the tensor-core decode
+ *             launches issued after this call, in nanoseconds; 0 restores the
+ *             default (2 s)
+ *   stall     nonzero: in those launches the score MMA warp of every CTA pair
+ *             first waits on a barrier that nothing arrives on. That wait gives
+ *             up after limit_ns, so does every wait that depended on it; the
+ *             kernel then drains the copies it issued, frees its tensor memory,
+ *             ORs MLA_DEVERR_TIMEOUT into dev_err and returns. Its outputs are
+ *             undefined; the stream and the context stay usable.
+ * Process-wide and read at launch time; for tests only. Set it back with
+ * (0, 0) before decoding for real. Always returns MLA_OK.
+ */
+mla_status mla_debug_decode_wait_test(uint64_t limit_ns, int32_t stall);
+
 /* Static description of a status code. */
 const char* mla_status_str(mla_status status);
 

@@ -30,8 +30,8 @@ EXPORTS = ("mla_absorb_q", "mla_absorb_q_rope", "mla_decode_workspace_size", "ml
            "mla_decode_paged_static", "mla_decompress_out", "mla_cache_append",
            "mla_cache_append_rmsnorm_rope", "mla_attend_workspace_size", "mla_attend_absorbed",
            "mla_rope_norm_to_neox_perm",
-           "mla_permute_rope_cols", "mla_permute_rope_rows", "mla_status_str",
-           "mla_last_error")
+           "mla_permute_rope_cols", "mla_permute_rope_rows", "mla_debug_decode_wait_test",
+           "mla_status_str", "mla_last_error")
 
 
 class MlaDims(ctypes.Structure):
@@ -82,6 +82,7 @@ def load(path: str = LIB_PATH):
     lib.mla_rope_norm_to_neox_perm.argtypes = [I32, P]
     lib.mla_permute_rope_cols.argtypes = [P, I32, I64, I64, I32, I32]
     lib.mla_permute_rope_rows.argtypes = [P, I32, I64, I32, I32]
+    lib.mla_debug_decode_wait_test.argtypes = [ctypes.c_uint64, I32]
     lib.mla_status_str.argtypes = [ctypes.c_int]
     lib.mla_status_str.restype = ctypes.c_char_p
     lib.mla_last_error.argtypes = []
@@ -244,6 +245,12 @@ def mla_permute_rope_rows(w: np.ndarray, row0: int, n_dims: int):
     _check("mla_permute_rope_rows",
            load().mla_permute_rope_rows(w.ctypes.data_as(ctypes.c_void_p), _host_elem_bytes(w),
                                         w.shape[1], row0, n_dims))
+
+
+def mla_debug_decode_wait_test(limit_ns: int, stall: bool):
+    """Timeout-path test switch of the tensor-core decode (see include/mla.h)."""
+    _check("mla_debug_decode_wait_test",
+           load().mla_debug_decode_wait_test(int(limit_ns), 1 if stall else 0))
 
 
 def mla_status_str(status: int) -> str:

@@ -99,6 +99,11 @@ const char* mla_status_str(mla_status s) {
 
 const char* mla_last_error(void) { return g_last_error; }
 
+mla_status mla_debug_decode_wait_test(uint64_t limit_ns, int32_t stall) {
+    mla::set_decode_wait_test(limit_ns, stall);
+    return MLA_OK;
+}
+
 mla_status mla_absorb_q(void* q_abs, const void* q_nope, const void* q_pe, const void* w_uk,
                         int32_t rows, const mla_dims* dims, void* stream) {
     g_last_error[0] = 0;
@@ -140,7 +145,7 @@ mla_status mla_absorb_q_rope(void* q_abs, const void* q_nope, const void* q_pe,
     // (the same ratio the fused cache append uses for the keys)
     const float theta_scale = powf(rope_base, -2.0f / (float)P);
     cudaStream_t s = (cudaStream_t)stream;
-    if (dims->dtype == MLA_BF16 && tc_gemm_supported(*dims, rows, /*absorb=*/true)) {
+    if (dims->dtype != MLA_F32 && tc_gemm_supported(*dims, rows, /*absorb=*/true)) {
         MLA_CUDA_TRY(launch_absorb_tc(q_abs, q_nope, q_pe, w_uk, rows, *dims, s, /*early=*/false,
                                       positions, theta_scale),
                      "absorb with rope (tensor cores)");

@@ -35,6 +35,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "internal.h"
@@ -58,21 +59,29 @@ using split::pairs_per_set;
 constexpr int kTok = 64;                      // cache tokens per tile
 constexpr int kNS = 3;                        // pipeline stages
 constexpr int kChunk = 64 * 128;              // 64 tokens x 64 columns of bf16
-constexpr int kStage = 8 * kChunk;            // latent 512 columns of a tile
-constexpr int kSideOff = kNS * kStage;        // S-CTA: rope chunks; O-CTA: P slots
+constexpr int kStage = 8 * kChunk;            // O-CTA: V (latent 512 columns) of a tile
+constexpr int kSideOff = kNS * kStage;        // O-CTA: P slots
 constexpr int kPBytes = 128 * 128;            // P [128 rows x 64 tokens] bf16
 constexpr int kCtrlOff = kSideOff + 2 * kPBytes;
 constexpr int kQChunk = 128 * 128;            // 128 query rows x 64 columns of bf16
 constexpr int kVBlock = 8 * 2048;             // O-CTA: one block's V as [8 chunks][16 rows][128 B]
-// the first segment's queries sit in stages 1-2 (latent chunks 0..7) and in
-// the rope chunks of stages 1-2 (chunk 8); tile 0 uses stage 0 meanwhile
-__host__ __device__ constexpr int q_chunk_off(int cc) {
-    return cc < 8 ? kStage + cc * kQChunk : kSideOff + kChunk;
+// S-CTA stage of a tile: its 4 cache blocks, each landed by one 5-D box as
+// [2 halves][nkc chunks][8 rows][128 B] (nkc = W / 64). The 8-row group of
+// tokens 8g..8g+7 of the tile (block g / 2, half g % 2) of chunk kc then sits
+// at g * nkc * 1 KB + kc * 1 KB: a uniform group stride the score MMA's
+// K-major operand takes as its SBO.
+__host__ __device__ constexpr int s_stage_bytes(int nkc) { return nkc * kChunk; }
+// the first segment's queries sit in stages 1-2 (chunk cc at 16 KB * cc);
+// tile 0 uses stage 0 meanwhile
+__host__ __device__ constexpr int q_chunk_off(int nkc, int cc) {
+    return s_stage_bytes(nkc) + cc * kQChunk;
 }
-static_assert(kSideOff + kChunk + kQChunk <= kSideOff + 3 * kChunk, "q chunk 8 placement");
+static_assert(9 * kQChunk <= 2 * s_stage_bytes(9) && 8 * kQChunk <= 2 * s_stage_bytes(8),
+              "queries fit stages 1-2");
+static_assert(kNS * s_stage_bytes(9) <= kCtrlOff, "S-CTA stages below the control block");
 constexpr int kThreads = 416;                 // see the role map in the kernel
 constexpr int kSmxWarps = 8;                  // S-CTA softmax warps: two threads per query row
-constexpr uint64_t kWaitLimit = 2000000000ull;  // ns before a wait gives up
+constexpr uint64_t kWaitLimit = 2000000000ull;  // ns before a wait gives up (default)
 constexpr uint32_t kSuspendHintNs = 1000;     // longest suspension of one wait poll
 constexpr float kRescaleThreshold = 8.0f;     // lazy rescale, log2 units
 constexpr int kPrefetchAhead = 6;             // tiles the L2 prefetcher runs ahead of V landing
@@ -103,6 +112,7 @@ struct Ctrl {
     uint64_t evtdone;       // O: row warps -> MMA warp (256)
     uint64_t statfull;      // O: segment statistics written (1 remote)
     uint64_t rowbar;        // both: barrier among the 256 row threads
+    uint64_t never;         // S: arrived on by nothing (the timeout-path test waits on it)
     uint32_t tmem_base;
     int32_t abort;
     int32_t evt_type;       // 1 = rescale slot evt_slot, 2 = segment epilogue
@@ -134,6 +144,9 @@ struct Params {
     int early;                    // read cache, table and seq_lens before the previous
                                   // kernel completes (it writes none of them)
     float scale_log2;
+    unsigned long long wait_ns;   // a bounded wait gives up after this long
+    int stall;                    // test of the timeout path: the score MMA warp first
+                                  // waits on a barrier nothing arrives on
 };
 
 // ------------------------------------------------------------------ schedule
@@ -246,6 +259,7 @@ __device__ __forceinline__ bool seg_last(const Walk& w) {
 struct Waiter {
     volatile int32_t* abort;
     int32_t* dev_err;
+    uint64_t limit;  // ns
     __device__ bool wait(uint32_t bar, uint32_t parity) {
         if (mbar_try_wait(bar, parity)) return true;
         const uint64_t t0 = globaltimer_ns();
@@ -253,7 +267,7 @@ struct Waiter {
             if (mbar_try_wait_hint(bar, parity, kSuspendHintNs)) return true;
             if ((i & 255) == 0) {
                 if (*abort) return false;
-                if (globaltimer_ns() - t0 > kWaitLimit) break;
+                if (globaltimer_ns() - t0 > limit) break;
             }
         }
         *abort = 1;
@@ -275,7 +289,7 @@ struct Waiter {
                 if (mbar_try_wait(bar, parity)) { ok = true; break; }
                 if ((i & 255) == 0) {
                     if (*abort) break;
-                    if (globaltimer_ns() - t0 > kWaitLimit) {
+                    if (globaltimer_ns() - t0 > limit) {
                         *abort = 1;
                         if (dev_err) atomicOr(dev_err, (int32_t)MLA_DEVERR_TIMEOUT);
                         break;
@@ -328,7 +342,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_ctarank();
     const int pair = blockIdx.x >> 1;
-    Waiter wt{&c.abort, p.dev_err};
+    Waiter wt{&c.abort, p.dev_err, p.wait_ns};
 
     grid_dependents_launch();  // the combine kernel may be scheduled (it waits for this grid)
     if ((smem_u32(smem) & 1023) != 0) {  // swizzled operands need 1 KB alignment
@@ -357,6 +371,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(&c.evtdone), 256);
         mbar_init(smem_u32(&c.statfull), 1);
         mbar_init(smem_u32(&c.rowbar), 256);
+        mbar_init(smem_u32(&c.never), 1);
         c.abort = 0;
         c.landed = 0;
         fence_mbar_init();
@@ -432,7 +447,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const int qrows = Mq < 128 ? Mq : 128;
                     mbar_arrive_expect_tx(smem_u32(&c.qland), (uint32_t)(NKC * qrows * 128));
                     for (int cc = 0; cc < NKC; ++cc)
-                        tma_load_3d(smem_u32(smem + q_chunk_off(cc)), &qmap, smem_u32(&c.qland),
+                        tma_load_3d(smem_u32(smem + q_chunk_off(NKC, cc)), &qmap, smem_u32(&c.qland),
                                     cc * 64, w.g * 128, w.b);
                 }
                 long long i = 0;
@@ -459,21 +474,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             if (p.dev_err) atomicOr(p.dev_err, (int32_t)MLA_DEVERR_BAD_BLOCK);
                             blk = 0;
                         }
-#pragma unroll
-                        for (int ch = 0; ch < 8; ++ch)
-                            tma_load_3d(smem_u32(smem + s * kStage + ch * kChunk + kb * 2048),
-                                        &tmap, smem_u32(&c.full[s]), ch * 64, 0, blk);
-                        if (NKC == 9)
-                            tma_load_3d(smem_u32(smem + kSideOff + s * kChunk + kb * 2048), &tmap,
-                                        smem_u32(&c.full[s]), 512, 0, blk);
+                        // the whole block (all NKC chunks, both 8-row halves) in one box
+                        tma_load_5d(smem_u32(smem + s * s_stage_bytes(NKC) + kb * NKC * 2048),
+                                    &tmap, smem_u32(&c.full[s]), 0, 0, 0, 0, blk);
                     }
                 }
                 // drain: the copies issued into each stage must have landed
-                if (kb == 0) mbar_wait(smem_u32(&c.qland), 0, kWaitLimit);
+                if (kb == 0) mbar_wait(smem_u32(&c.qland), 0, p.wait_ns);
                 for (int s = 0; s < kNS; ++s)
                     if (last_issue[s] >= 0)
                         mbar_wait(smem_u32(&c.full[s]), (uint32_t)((last_issue[s] / kNS) & 1),
-                                  kWaitLimit);
+                                  p.wait_ns);
             }
         } else if (warp == 4) {
             // ---------------- MMA issuer: S = Q K^T
@@ -481,6 +492,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 constexpr uint32_t idesc = idesc_f32acc<kF16>(128, kTok, 0, 0);
                 long long i = 0;
                 int seg = 0;
+                // the timeout-path test: this wait gives up (recording the
+                // timeout and raising the abort flag) and no MMA is issued
+                if (p.stall && !wt.wait(smem_u32(&c.never), 0)) w.u = w.u_end;
                 for (; w.u < w.u_end; walk_next(p, w), ++i) {
                     const int s = (int)(i % kNS);
                     const int buf = (int)(i & 1);
@@ -494,12 +508,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const uint32_t d = ts0 + buf * kTok;
 #pragma unroll 1
                     for (int kc = 0; kc < NKC; ++kc) {
-                        const uint32_t base = kc < 8 ? smem_u32(smem + s * kStage + kc * kChunk)
-                                                     : smem_u32(smem + kSideOff + s * kChunk);
+                        // chunk kc: 8 groups of 8 tokens at a stride of NKC KB
+                        const uint32_t base = smem_u32(smem + s * s_stage_bytes(NKC) + kc * 1024);
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            mma_ts(d, tq + kc * 32 + kk * 8, sdesc_sw128(base + kk * 32, 16, 1024),
-                                   idesc, (kc | kk) != 0);
+                            mma_ts(d, tq + kc * 32 + kk * 8,
+                                   sdesc_sw128(base + kk * 32, 16, NKC * 1024), idesc,
+                                   (kc | kk) != 0);
                     }
                     mma_commit(smem_u32(&c.sfull[buf]));
                     mma_commit(smem_u32(&c.empty[s]));
@@ -557,7 +572,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             if (!wt.wait_warp(smem_u32(&c.qland), 0)) break;
 #pragma unroll 1
                             for (int cc = c0; cc < c1; ++cc) {
-                                const uint32_t rowa = smem_u32(smem + q_chunk_off(cc)) + rq * 128;
+                                const uint32_t rowa = smem_u32(smem + q_chunk_off(NKC, cc)) + rq * 128;
                                 uint32_t v[32];
 #pragma unroll
                                 for (int u = 0; u < 8; ++u) {
@@ -737,7 +752,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int s = 0; s < kNS; ++s)
                     if (last_issue[s] >= 0)
                         mbar_wait(smem_u32(&c.full[s]), (uint32_t)((last_issue[s] / kNS) & 1),
-                                  kWaitLimit);
+                                  p.wait_ns);
             }
         } else if (warp == 1) {
             // ---------------- V landing: the rows of the tile's last cache block
@@ -789,7 +804,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint64_t t_start = globaltimer_ns();
             for (; w.u < w.u_end; walk_next(p, w), ++i) {
                 while (i > *(volatile int32_t*)&c.landed + kPrefetchAhead) {
-                    if (c.abort || globaltimer_ns() - t_start > 4 * kWaitLimit) break;
+                    if (c.abort || globaltimer_ns() - t_start > 4 * p.wait_ns) break;
                     __nanosleep(200);
                 }
                 if (c.abort) break;
@@ -1231,7 +1246,19 @@ int max_pairs_for(const mla_dims& d, cudaError_t* err) {
     return n;
 }
 
+std::atomic<unsigned long long> g_wait_limit_ns{0};
+std::atomic<int> g_stall{0};
+
 }  // namespace
+
+DecodeWaitTest decode_wait_test() {
+    return DecodeWaitTest{g_wait_limit_ns.load(), g_stall.load()};
+}
+
+void set_decode_wait_test(unsigned long long limit_ns, int stall) {
+    g_wait_limit_ns.store(limit_ns);
+    g_stall.store(stall ? 1 : 0);
+}
 
 bool tc_decode_supported(const mla_dims& d) {
     const int W = d.kv_rank + d.d_rope;
@@ -1282,12 +1309,17 @@ cudaError_t launch_decode_tc(void* out, float* lse, const void* q_abs, const voi
     const bool f16 = d.dtype == MLA_F16;
     const CUtensorMapDataType tdt = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                         : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    // the S-CTA's view of the cache: {64 columns, 8 rows, W/64 column chunks,
+    // 2 halves of a block, blocks}; one box is a whole block, landing as
+    // [half][chunk][8 rows][128 B]
     CUtensorMap tmap;
-    cuuint64_t dims[3] = {(cuuint64_t)W, 16, (cuuint64_t)num_blocks};
-    cuuint64_t strides[2] = {(cuuint64_t)W * 2, (cuuint64_t)16 * W * 2};
-    cuuint32_t box[3] = {64, 16, 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    CUresult cr = enc(&tmap, tdt, 3, const_cast<void*>(kv_cache),
+    const int nkc = W / 64;
+    cuuint64_t dims[5] = {64, 8, (cuuint64_t)nkc, 2, (cuuint64_t)num_blocks};
+    cuuint64_t strides[4] = {(cuuint64_t)W * 2, 128, (cuuint64_t)8 * W * 2,
+                             (cuuint64_t)16 * W * 2};
+    cuuint32_t box[5] = {64, 8, (cuuint32_t)nkc, 2, 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    CUresult cr = enc(&tmap, tdt, 5, const_cast<void*>(kv_cache),
                       dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -1372,6 +1404,11 @@ cudaError_t launch_decode_tc(void* out, float* lse, const void* q_abs, const voi
     p.combine_rpt = 1;
     p.early = early ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
+    {
+        const DecodeWaitTest t = decode_wait_test();
+        p.wait_ns = t.limit_ns ? t.limit_ns : kWaitLimit;
+        p.stall = t.stall;
+    }
 
     // a programmatic dependent of the kernel before it: the cache pipeline
     // starts while that kernel finishes; the queries, and every write, wait

@@ -23,6 +23,16 @@ cudaError_t launch_decode_tc(void* out, float* lse, const void* q_abs, const voi
                              const mla_dims& d, float scale, void* workspace,
                              int32_t* dev_err, cudaStream_t s, bool early, bool combine);
 
+// The timeout-path test switch (mla_debug_decode_wait_test): the bounded
+// waits' limit for later decode launches (0: the default, 2 s) and whether
+// their score MMA warp first waits on a barrier nothing arrives on.
+struct DecodeWaitTest {
+    unsigned long long limit_ns;
+    int stall;
+};
+DecodeWaitTest decode_wait_test();
+void set_decode_wait_test(unsigned long long limit_ns, int stall);
+
 // Where the decode keeps its split partial rows in `workspace`, and the split
 // parameters tc_split.cuh needs (pairs of the grid, fewest units per pair).
 struct DecodeSplitInfo {

@@ -205,16 +205,21 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 // the query's rope at its row's position: NEOX pair (j, j + P/2)
                 // turned by theta_j = pos * theta_scale^j (the ratio applied j
                 // times, in f32); products rounded before the sum
-                const __nv_bfloat16* src = p.q_pe + ((long long)row * p.H + h) * p.P;
-                __nv_bfloat16* d = p.out + ((long long)row * p.H + h) * p.out_stride + p.N;
+                // (16-bit elements of the path's type, f16 or bf16)
+                const uint16_t* src = reinterpret_cast<const uint16_t*>(p.q_pe) +
+                                      ((long long)row * p.H + h) * p.P;
+                uint16_t* d = reinterpret_cast<uint16_t*>(p.out) +
+                              ((long long)row * p.H + h) * p.out_stride + p.N;
                 const int half = p.P / 2;
                 float theta = (float)p.positions[row];
                 for (int j = 0; j < half; ++j) {
                     float sn, cs;
                     sincosf(theta, &sn, &cs);
-                    const float a = __bfloat162float(src[j]), b = __bfloat162float(src[j + half]);
-                    d[j] = __float2bfloat16_rn(__fsub_rn(__fmul_rn(a, cs), __fmul_rn(b, sn)));
-                    d[j + half] = __float2bfloat16_rn(__fadd_rn(__fmul_rn(a, sn), __fmul_rn(b, cs)));
+                    const float a = elem_lo<kF16>(src[j]), b = elem_lo<kF16>(src[j + half]);
+                    const uint32_t pr = pack2<kF16>(__fsub_rn(__fmul_rn(a, cs), __fmul_rn(b, sn)),
+                                                    __fadd_rn(__fmul_rn(a, sn), __fmul_rn(b, cs)));
+                    d[j] = (uint16_t)(pr & 0xffffu);
+                    d[j + half] = (uint16_t)(pr >> 16);
                     theta = __fmul_rn(theta, p.theta_scale);
                 }
             }

@@ -2,13 +2,11 @@
 
 Tolerances (the parity gates, tests/tolerances.py):
   f32 inputs   every output and LSE: max abs diff <= 1e-4
-  bf16 inputs  outputs: |gpu - ref| <= 1e-2 wherever one bf16 rounding of the
-               output fits under it (|ref| < 4), one bf16 ulp of |ref| above;
-               LSE (f32): max abs diff <= 1e-3; a -inf LSE must be -inf on
-               both sides.
-  f16 inputs   outputs: <= 2e-3 where one f16 rounding fits under it (|ref| < 8),
-               one f16 ulp above (the bf16 gate scaled by f16's finer quantum);
-               LSE as for bf16.
+  bf16 inputs  outputs: |gpu - ref| <= 1e-2 + half a bf16 ulp of |ref| (the
+               stated bound plus one rounding of the stored output); LSE (f32):
+               max abs diff <= 1e-3; a -inf LSE must be -inf on both sides.
+  f16 inputs   outputs: <= 2e-3 + half an f16 ulp of |ref| (the bf16 gate
+               scaled by f16's finer quantum); LSE as for bf16.
 The oracle runs on the same (bf16-rounded) values the GPU stage consumed: each
 stage's input comes from the generator or from the oracle's previous stage,
 never from the GPU.
@@ -38,9 +36,13 @@ def assert_close(got, ref, dtype, what):
     assert got.shape == ref.shape, (what, got.shape, ref.shape)
     assert np.all(np.isfinite(got)), f"{what}: non-finite GPU output"
     err = np.abs(got - ref)
-    bad = err > output_bound(ref, dtype)
-    assert not bad.any(), (f"{what}: {int(bad.sum())} of {bad.size} outside tolerance, "
-                           f"max err {err.max():.3e}")
+    bound = output_bound(ref, dtype)
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(np.where(bad, err - bound, -np.inf)), err.shape)
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} outside tolerance, max err "
+                             f"{err.max():.3e}; worst at {i}: ref {ref[i]:.6f} gpu {got[i]:.6f} "
+                             f"bound {bound[i]:.3e}")
 
 
 def assert_lse_close(got, ref, dtype, what):
@@ -279,3 +281,48 @@ def test_back_to_back_steps_are_identical_and_right(name, lens):
                  "back-to-back decode out")
     assert_lse_close(snaps[0][1].cpu().numpy(), lse_ref.reshape(-1, H), g.dtype,
                      "back-to-back decode lse")
+
+
+def oracle_decode_threaded(q4, wl, threads=None):
+    """The oracle's decode of every (query row, head) pair, the pairs split
+    over host threads (each call is the oracle's own decode_rows on disjoint
+    pairs; the C code releases the GIL)."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    g = wl.geom
+    n = wl.rows * g.n_head
+    threads = threads or os.cpu_count() or 1
+    parts = np.array_split(np.arange(n, dtype=np.int64), max(1, threads * 4))
+    with ThreadPoolExecutor(threads) as ex:
+        res = list(ex.map(lambda ids: oracle.decode_rows(
+            q4, wl.kv_cache, wl.block_table, wl.seq_lens, g.t_q, g.kv_rank, wl.scale, ids),
+            parts))
+    return np.concatenate([r[0] for r in res]), np.concatenate([r[1] for r in res])
+
+
+@pytest.mark.slow
+def test_deepseek_full_size_all_rows():
+    """The whole DeepSeek-V3 geometry workload (64 requests of 8192 keys, 128
+    heads): every query row of the decode against the oracle, so the full
+    even split over all CTA pairs and its combine are compared row by row;
+    then the fused step's output against the oracle's decompress."""
+    import torch
+    wl = W.make_workload("deepseek_decode")
+    g = wl.geom
+    H, R, T = g.n_head, g.kv_rank, g.t_q
+    dc = D.upload(wl)
+    q = rounded(oracle.absorb_q(wl.q_nope, wl.q_pe, wl.w_uk), g.dtype)
+    dc.q_abs.copy_(D.host_to_device(q, g.dtype, "cuda"))
+    D.decode(dc)
+    torch.cuda.synchronize()
+    assert int(dc.dev_err.item()) == 0
+    o_ref, lse_ref = oracle_decode_threaded(q.reshape(wl.batch, T, H, -1), wl)
+    assert_close(D.device_to_host_f32(dc.o_lat).reshape(-1, R), o_ref, g.dtype,
+                 "deepseek decode out (all rows)")
+    assert_lse_close(dc.lse.cpu().numpy().reshape(-1), lse_ref, g.dtype,
+                     "deepseek decode lse (all rows)")
+    D.attend(dc)
+    torch.cuda.synchronize()
+    assert int(dc.dev_err.item()) == 0
+    out_ref = oracle.decompress(rounded(o_ref.reshape(-1, H, R), g.dtype), wl.w_uv)
+    assert_close(D.device_to_host_f32(dc.out), out_ref, g.dtype, "deepseek fused step out")
