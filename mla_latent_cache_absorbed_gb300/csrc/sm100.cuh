@@ -384,6 +384,32 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void* ptr, uint32_t bytes
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
 }
 
+// packed f32 pairs (one instruction for two lanes of arithmetic; each lane
+// rounds exactly as the scalar operation would)
+__device__ __forceinline__ void mul2(float& a, float& b, float x, float y, float s) {
+    uint64_t u, v, r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(u) : "f"(x), "f"(y));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(v) : "f"(s));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(u), "l"(v));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+// (a, b) -= (m, m)
+__device__ __forceinline__ void sub2(float& a, float& b, float m) {
+    uint64_t u, v, r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(u) : "f"(a), "f"(b));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(v) : "f"(m));
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(u), "l"(v));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+// (a, b) += (x, y)
+__device__ __forceinline__ void add2(float& a, float& b, float x, float y) {
+    uint64_t u, v, r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(u) : "f"(a), "f"(b));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(x), "f"(y));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(u), "l"(v));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+
 // 2^x on the special-function unit (the result feeds a bf16 operand)
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;

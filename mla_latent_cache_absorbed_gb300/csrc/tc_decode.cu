@@ -78,7 +78,10 @@ __host__ __device__ constexpr int q_chunk_off(int nkc, int cc) {
 }
 static_assert(9 * kQChunk <= 2 * s_stage_bytes(9) && 8 * kQChunk <= 2 * s_stage_bytes(8),
               "queries fit stages 1-2");
-static_assert(kNS * s_stage_bytes(9) <= kCtrlOff, "S-CTA stages below the control block");
+// S-CTA: above its stages, 1 KB per softmax warp to regroup P rows (8 rows of
+// 128 B) so that each store to the O-CTA writes 512 contiguous bytes
+__host__ __device__ constexpr int p_regroup_off(int nkc) { return kNS * s_stage_bytes(nkc); }
+static_assert(p_regroup_off(9) + 8 * 1024 <= kCtrlOff, "S-CTA stages and P regrouping below the control block");
 constexpr int kThreads = 416;                 // see the role map in the kernel
 constexpr int kSmxWarps = 8;                  // S-CTA softmax warps: two threads per query row
 constexpr uint64_t kWaitLimit = 2000000000ull;  // ns before a wait gives up (default)
@@ -541,6 +544,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t lstat_remote = mapa(smem_u32(&c.lstat[0]), 1);
             const uint32_t bad_remote = mapa(smem_u32(&c.bad), 1);
             const uint32_t statfull_remote = mapa(smem_u32(&c.statfull), 1);
+            const uint32_t regroup = smem_u32(smem + p_regroup_off(NKC)) + (uint32_t)sw * 1024;
             const float sl2 = p.scale_log2;
             grid_dependency_wait();  // later segments read their queries from global memory
             long long i = 0;
@@ -643,7 +647,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tmem_ld16x64(ts0 + buf * kTok + lane_base16, v);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]) * sl2;
+                    for (int j = 0; j < 32; j += 2)
+                        mul2(x[j], x[j + 1], __uint_as_float(v[j]), __uint_as_float(v[j + 1]), sl2);
                 }
                 tc_fence_before();
                 mbar_arrive(smem_u32(&c.sfree[buf]));
@@ -671,10 +676,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
                 for (int j = 0; j < 32; j += 2) {
-                    x[j] = ex2_approx(x[j] - mref);  // 2^-inf = +0
-                    x[j + 1] = ex2_approx(x[j + 1] - mref);
-                    ps0 += x[j];
-                    ps1 += x[j + 1];
+                    sub2(x[j], x[j + 1], mref);
+                    x[j] = ex2_approx(x[j]);  // 2^-inf = +0
+                    x[j + 1] = ex2_approx(x[j + 1]);
+                    add2(ps0, ps1, x[j], x[j + 1]);
                 }
                 l = l * alpha + (ps0 + ps1);  // this thread's columns; the pair adds at the end
                 // swap halves: the even thread keeps columns 0..31, the odd one 32..63
@@ -690,18 +695,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 // P slot free? (the O-CTA's P*V two tiles back)
                 if (!wt.wait_warp(smem_u32(&c.pempty[buf]), (uint32_t)((i >> 1) & 1) ^ 1)) break;
                 const uint32_t pbar = pfull_remote + buf * 8;
-                if (row_ok) {  // rows past the group are never read back
-                    const uint32_t prow = pslot_remote + buf * kPBytes + R * 128;
+                // The warp's 16 rows go out 8 at a time: the threads of those rows
+                // write their 16-byte pieces into the warp's 1 KB in the P slot's
+                // swizzled layout, then every lane ships two contiguous pieces, so
+                // each store to the O-CTA covers 4 whole rows (512 bytes). Rows past
+                // the group are never read back and are not sent.
+                {
+                    const int grows = min(128, Mq - w.g * 128);
+                    const int rbase = q * 32 + h * 16;  // the warp's first row
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int cu = 4 * par + u;  // 16-byte chunk of the row
-                        st_async_v4(prow + ((cu ^ (R & 7)) << 4), pk[4 * u], pk[4 * u + 1],
-                                    pk[4 * u + 2], pk[4 * u + 3], pbar);
+                    for (int half = 0; half < 2; ++half) {
+                        if ((lane & 1) == half) {
+                            const int a = lane >> 2;  // this thread's row, rbase + a + 8 half
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                st_shared_v4(regroup + a * 128 + (((4 * par + u) ^ a) << 4), pk[4 * u],
+                                             pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                        }
+                        __syncwarp();
+#pragma unroll
+                        for (int v = 0; v < 2; ++v) {
+                            const int a = 4 * v + (lane >> 3);
+                            const int row = rbase + 8 * half + a;
+                            const uint4 d = ld_shared_v4(regroup + a * 128 + ((lane & 7) << 4));
+                            if (row < grows)
+                                st_async_v4(pslot_remote + buf * kPBytes + row * 128 + ((lane & 7) << 4),
+                                            d.x, d.y, d.z, d.w, pbar);
+                        }
+                        __syncwarp();  // the next half overwrites the warp's 1 KB
                     }
-                    if (par == 0)
-                        st_async_b32(amsg_remote + buf * (uint32_t)sizeof(AlphaMsg) + R * 4,
-                                     __float_as_uint(alpha), pbar);
                 }
+                if (row_ok && par == 0)
+                    st_async_b32(amsg_remote + buf * (uint32_t)sizeof(AlphaMsg) + R * 4,
+                                 __float_as_uint(alpha), pbar);
                 if (lane == 0)
                     st_async_b32(amsg_remote + buf * (uint32_t)sizeof(AlphaMsg) + 512 + sw * 4,
                                  any ? 1u : 0u, pbar);
