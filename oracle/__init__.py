@@ -83,6 +83,8 @@ def _declare(lib):
     lib.oracle_norm_to_neox_perm.argtypes = [_I, _P]
     lib.oracle_cache_append.argtypes = [_P, _I, _P, _P, _I, _P, _I, _I64, _I, _I]
     lib.oracle_kv_prolog_row.argtypes = [_P, _P, _P, _P, _I, _I64, _I64, _I, _I, _D, _F]
+    lib.oracle_rmsnorm_rows.argtypes = [_P, _P, _P, _I, _I, _I, _D]
+    lib.oracle_project.argtypes = [_P, _P, _P, _I, _I, _I]
     lib.oracle_cache_append_rmsnorm_rope.argtypes = [_P, _I, _P, _P, _P, _I, _P, _P, _I, _I64,
                                                      _I, _I, _D, _F]
     for name in ("oracle_absorb_q", "oracle_decode_range", "oracle_decode_rows",
@@ -162,6 +164,33 @@ def absorb_q_rope(q_nope, q_pe, w_uk, positions, rope_base, lib=None) -> np.ndar
     _check(lib.oracle_absorb_q_rope(_ptr(out), _ptr(q_nope), _ptr(q_pe), _ptr(w_uk), _ptr(pos),
                                     rows, H, Dn, P, R, float(rope_base)), False)
     return out
+
+
+def rmsnorm_rows(x, gamma, eps, lib=None) -> np.ndarray:
+    """c^Q = RmsNorm(x) per row (the "aclnnMlaProlog" page's RmsNorm formula,
+    f64 arithmetic, f32 result). x [rows, n] and gamma [n] are f32 arrays, or
+    uint16 arrays of bf16 bit patterns (both the same kind)."""
+    lib = lib or load()
+    xa, dt = _elem(np.asarray(x))
+    ga, gdt = _elem(np.asarray(gamma))
+    assert dt == gdt, "x and gamma must be of one element type"
+    rows, n = xa.shape
+    out = np.empty((rows, n), np.float32)
+    _check(lib.oracle_rmsnorm_rows(_ptr(out), _ptr(xa), _ptr(ga), dt, rows, n, float(eps)), False)
+    return out
+
+
+def project(x, w, lib=None) -> np.ndarray:
+    """y = x W for x [rows, k] and a projection weight W [k, n] (f32 sums in
+    k order): q^C = c^Q W^UQ or c^Q W^QR of the "aclnnMlaProlog" page."""
+    lib = lib or load()
+    xa, wa = _f32(x), _f32(w)
+    rows, k = xa.shape
+    n = wa.shape[1]
+    assert wa.shape[0] == k
+    y = np.empty((rows, n), np.float32)
+    _check(lib.oracle_project(_ptr(y), _ptr(xa), _ptr(wa), rows, k, n), False)
+    return y
 
 
 def decode_rows(q_abs, kv_cache, block_table, seq_lens, t_q, kv_rank, scale,

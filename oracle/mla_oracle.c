@@ -44,6 +44,11 @@
  *                          the query (q^N = q^C W^UK; q^R = ROPE(c^Q W^QR)):
  *                          the absorb above with the mla.rs NEOX rope of the
  *                          query's rope part at the row's position.
+ *   oracle_rmsnorm_rows / oracle_project
+ *                          the "aclnnMlaProlog" page, computation formulas of
+ *                          the query before the absorb: c^Q = RmsNorm(x W^DQ)
+ *                          (its RmsNorm formula, in f64) and the projections
+ *                          q^C = c^Q W^UQ, c^Q W^QR (plain f32 sums).
  *   oracle_kv_prolog_row / oracle_cache_append_rmsnorm_rope
  *                          the "aclnnMlaProlog" page, computation formulas of
  *                          the key (RmsNorm of the latent, rope of k^R, both
@@ -526,6 +531,40 @@ int oracle_absorb_q_rope(float* q_abs, const float* q_nope, const float* q_pe,
         for (int h = 0; h < n_head; ++h)
             oracle_rope_neox(q_abs + ((int64_t)r * n_head + h) * W + kv_rank, d_rope,
                              (float)positions[r], rope_base);
+    return ORACLE_OK;
+}
+
+/* c^Q = RmsNorm(x W^DQ), one query row r at a time: out[r][i] = gamma_i x_i /
+ * RMS(x) with RMS(x) = sqrt(sum_k x_k^2 / n + eps) over the row's n elements
+ * x = xin[r] (the page's RmsNorm formula; f64 arithmetic, the result stored as
+ * f32). xin and gamma are of src_dtype (f32, or bf16 bit patterns). */
+int oracle_rmsnorm_rows(float* out, const void* xin, const void* gamma, int src_dtype, int rows,
+                        int n, double eps) {
+    if (rows < 0 || n <= 0 || !(eps >= 0.0)) return ORACLE_BAD_ARG;
+    for (int r = 0; r < rows; ++r) {
+        double ss = 0.0;
+        for (int k = 0; k < n; ++k) {
+            const double x = load_elem(xin, src_dtype, (int64_t)r * n + k);
+            ss += x * x;
+        }
+        const double rms = sqrt(ss / (double)n + eps);
+        for (int i = 0; i < n; ++i) {
+            const double x = load_elem(xin, src_dtype, (int64_t)r * n + i);
+            const double g = load_elem(gamma, src_dtype, i);
+            out[(int64_t)r * n + i] = (float)(g * x / rms);
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* A projection of the prolog (q^C = c^Q W^UQ, or c^Q W^QR): y[r][j] =
+ * sum_k x[r][k] w[k][j], the weight stored (k, n) as the page lays out its
+ * projection weights; one f32 sum per output in k order. */
+int oracle_project(float* y, const float* x, const float* w, int rows, int k, int n) {
+    if (rows < 0 || k <= 0 || n <= 0) return ORACLE_BAD_ARG;
+    for (int r = 0; r < rows; ++r)
+        for (int j = 0; j < n; ++j)
+            y[(int64_t)r * n + j] = dot_from(0.0f, x + (int64_t)r * k, 1, w + j, n, k);
     return ORACLE_OK;
 }
 

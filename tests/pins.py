@@ -711,10 +711,76 @@ def check_q_prolog(lib):
     assert np.array_equal(nope, O.absorb_q(qn, qp[:, :, :0], w, lib=lib))
 
 
+def check_q_prolog_full(lib):
+    """The query half of the MLA prolog from c^Q's row before the norm
+    ("aclnnMlaProlog" page, query formulas: c^Q = RmsNorm(x W^DQ),
+    q^C = c^Q W^UQ, q^N = q^C W^UK, q^R = ROPE(c^Q W^QR)):
+      * RmsNorm against closed forms: a constant row c gives gamma c /
+        sqrt(c^2 + eps); with gamma = 1 and eps = 0 every row has unit mean
+        square; scaling a row by 3.5 changes nothing (eps = 0); a zero row
+        stays zero;
+      * the projection against an f64 matmul within the bound of a sequential
+        f32 sum (k 2^-24 sum |x_k w_kj| plus rounding of the result), and an
+        identity weight returns its input exactly;
+      * norm, both projections, the absorb and the rope composed by the oracle
+        against the whole formula restated in f64 (numpy, the rope as a
+        rotation), relative 1e-4."""
+    import oracle as O
+    rng = np.random.default_rng(77)
+    # --- RmsNorm closed forms
+    n = 48
+    g = (rng.random(n) + 0.5).astype(np.float32)
+    for c, eps in ((2.5, 0.0), (-0.75, 1e-2), (3.0, 9.0)):
+        out = O.rmsnorm_rows(np.full((1, n), c, np.float32), g, eps, lib=lib)[0]
+        ref = g.astype(np.float64) * c / math.sqrt(c * c + eps)
+        assert np.all(np.abs(out - ref) <= 2e-7 * np.abs(ref) + 1e-30), (c, eps)
+    x = rng.standard_normal((6, n)).astype(np.float32)
+    ones = np.ones(n, np.float32)
+    unit = O.rmsnorm_rows(x, ones, 0.0, lib=lib).astype(np.float64)
+    assert np.all(np.abs(np.mean(unit * unit, axis=1) - 1.0) <= 1e-6)
+    a = O.rmsnorm_rows(x, g, 0.0, lib=lib)
+    b = O.rmsnorm_rows((x * 3.5).astype(np.float32), g, 0.0, lib=lib)
+    assert np.all(np.abs(a - b) <= 2e-7 * np.abs(a) + 1e-30)
+    assert np.all(O.rmsnorm_rows(np.zeros((2, n), np.float32), g, 1e-6, lib=lib) == 0)
+    # --- projection
+    k, m = 40, 24
+    xs = rng.standard_normal((5, k)).astype(np.float32)
+    w = (rng.standard_normal((k, m)) / math.sqrt(k)).astype(np.float32)
+    y = O.project(xs, w, lib=lib).astype(np.float64)
+    ref = xs.astype(np.float64) @ w.astype(np.float64)
+    bound = k * 2.0 ** -24 * (np.abs(xs).astype(np.float64) @ np.abs(w).astype(np.float64)) \
+        + 2.0 ** -24 * np.abs(ref)
+    assert np.all(np.abs(y - ref) <= bound)
+    eye = np.eye(k, dtype=np.float32)
+    assert np.array_equal(O.project(xs, eye, lib=lib), xs)
+    # --- the whole query half against f64
+    rows, H, Dn, P, R, qr = 5, 3, 8, 16, 24, 40
+    base, eps = 10000.0, 1e-6
+    cq = rng.standard_normal((rows, qr)).astype(np.float32)
+    gq = (rng.random(qr) + 0.5).astype(np.float32)
+    w_uq = (rng.standard_normal((qr, H * Dn)) / math.sqrt(qr)).astype(np.float32)
+    w_qr = (rng.standard_normal((qr, H * P)) / math.sqrt(qr)).astype(np.float32)
+    w_uk = (rng.standard_normal((H, Dn, R)) / math.sqrt(R)).astype(np.float32)
+    pos = np.array([0, 3, 77, 4095, 12345], np.int64)
+    cn = O.rmsnorm_rows(cq, gq, eps, lib=lib)
+    qc = O.project(cn, w_uq, lib=lib).reshape(rows, H, Dn)
+    qpe = O.project(cn, w_qr, lib=lib).reshape(rows, H, P)
+    got = O.absorb_q_rope(qc, qpe, w_uk, pos, base, lib=lib).astype(np.float64)
+    c64 = cq.astype(np.float64)
+    cn64 = gq.astype(np.float64) * c64 / np.sqrt(np.mean(c64 * c64, axis=1, keepdims=True) + eps)
+    qc64 = (cn64 @ w_uq.astype(np.float64)).reshape(rows, H, Dn)
+    qpe64 = (cn64 @ w_qr.astype(np.float64)).reshape(rows, H, P)
+    lat64 = np.einsum("rhd,hdl->rhl", qc64, w_uk.astype(np.float64))
+    rope64 = np.stack([np.stack([_rotation_f64(qpe64[r, h], pos[r], base) for h in range(H)])
+                       for r in range(rows)])
+    want = np.concatenate([lat64, rope64], axis=2)
+    assert rel_ok(want, got, 1e-4), maxdiff(want, got)
+
+
 QUICK_CHECKS = [check_naive_equals_absorbed, check_paged_chain_equals_naive,
                 check_bruteforce_f64, check_sdpa_reduction, check_closed_forms,
                 check_split_combine, check_paged_equals_contiguous,
                 check_decode_rows_consistent, check_invalid_requests,
                 check_absorb_decompress_unit_weights, check_rope_permutation,
                 check_rope_against_rotation, check_cache_append, check_kv_prolog,
-                check_causal_prefill, check_q_prolog]
+                check_causal_prefill, check_q_prolog, check_q_prolog_full]

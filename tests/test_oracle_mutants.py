@@ -75,6 +75,16 @@ MUTANTS = [
     ("prolog_position_of_token0", "d_rope > 0 ? positions[n] : 0", "d_rope > 0 ? positions[0] : 0", 0),
     ("prolog_writes_padding", "const int64_t s = slots[n];\n        if (s < 0) continue;",
      "const int64_t s = slots[n] < 0 ? 0 : slots[n];", 1),
+    ("q_norm_sum_not_mean", "sqrt(ss / (double)n + eps)", "sqrt(ss + eps)", 0),
+    ("q_norm_no_gamma", "out[(int64_t)r * n + i] = (float)(g * x / rms);",
+     "out[(int64_t)r * n + i] = (float)(x / rms);", 0),
+    ("q_norm_eps_outside", "sqrt(ss / (double)n + eps)", "(sqrt(ss / (double)n) + eps)", 0),
+    ("q_norm_row0_stats", "const double x = load_elem(xin, src_dtype, (int64_t)r * n + k);",
+     "const double x = load_elem(xin, src_dtype, k);", 0),
+    ("project_transposed", "dot_from(0.0f, x + (int64_t)r * k, 1, w + j, n, k)",
+     "dot_from(0.0f, x + (int64_t)r * k, 1, w + (int64_t)j * k % ((int64_t)k * n), 1, k)", 0),
+    ("project_drops_last_term", "dot_from(0.0f, x + (int64_t)r * k, 1, w + j, n, k)",
+     "dot_from(0.0f, x + (int64_t)r * k, 1, w + j, n, k - 1)", 0),
 ]
 
 
