@@ -124,6 +124,38 @@ mla_status mla_absorb_q_rope(void* q_abs, const void* q_nope, const void* q_pe,
                              float rope_base, const mla_dims* dims, void* stream);
 
 /*
+ * The query half of the MLA prolog in one call ("aclnnMlaProlog", computation
+ * formulas of the query), from each query row's x W^DQ (the down-projected
+ * query before its norm) to the decode's query row:
+ *   c^Q = RmsNorm(c_q[r]):  gamma_q[i] c_q[r][i] / sqrt(sum_k c_q[r][k]^2 / q_rank + eps)
+ *   q^C = c^Q W^UQ (head h: columns h Dn .. h Dn + Dn - 1), q^N = q^C W^UK[h]
+ *   q^R = ROPE(c^Q W^QR) (head h: columns h P .. h P + P - 1), the NEOX rope of
+ *         mla_absorb_q_rope at positions[r] (the rope columns of W^QR carry
+ *         the load-time permutation)
+ *   q_abs[r][h] = [ q^N | q^R ]
+ * Arithmetic: f32 sums; on the 16-bit paths c^Q and q^C are rounded to the
+ * path's type before they enter their products (they are tensor-core
+ * operands), q^R is turned in f32 and rounded once.
+ * q_abs     [rows][H][R+P]   out, dims->dtype
+ * c_q       [rows][q_rank]   in, dims->dtype
+ * gamma_q   [q_rank]         in, dims->dtype
+ * w_uq      [q_rank][H*Dn]   in, dims->dtype (the page's (k, n) layout)
+ * w_qr      [q_rank][H*P]    in, dims->dtype; may be NULL only when P == 0
+ * w_uk      [H][Dn][R]       in, dims->dtype
+ * positions [rows] int64     in, device, 8-byte aligned; may be NULL only when P == 0
+ * q_rank    > 0; a multiple of 8 (of 64 on the tensor-core path: bf16/f16,
+ *           kv_rank 512, d_nope and d_rope multiples of 64, d_nope + d_rope <= 256)
+ * eps       >= 0, finite; rope_base > 0 (unused when P == 0)
+ * dev_err   optional device int32: MLA_DEVERR_TIMEOUT if a bounded wait of the
+ *           tensor-core kernel gave up (its output is then undefined)
+ * rows == 0 is a no-op. Buffers 16-byte aligned. Stream-ordered, no sync.
+ */
+mla_status mla_prolog_q(void* q_abs, const void* c_q, const void* gamma_q, const void* w_uq,
+                        const void* w_qr, const void* w_uk, const int64_t* positions,
+                        int32_t rows, int32_t q_rank, float eps, float rope_base,
+                        const mla_dims* dims, int32_t* dev_err, void* stream);
+
+/*
  * Scratch bytes mla_decode_paged needs for this batch shape on the current
  * device (split-KV partial outputs and LSEs). The contents need no
  * initialisation and are dead after the call's work completes on the stream.

@@ -26,7 +26,8 @@ DEVERR_SEQ_SHORT = 4
 DEVERR_TIMEOUT = 8
 
 # Every exported symbol of include/mla.h.
-EXPORTS = ("mla_absorb_q", "mla_absorb_q_rope", "mla_decode_workspace_size", "mla_decode_paged",
+EXPORTS = ("mla_absorb_q", "mla_absorb_q_rope", "mla_prolog_q", "mla_decode_workspace_size",
+           "mla_decode_paged",
            "mla_decode_paged_static", "mla_decompress_out", "mla_cache_append",
            "mla_cache_append_rmsnorm_rope", "mla_attend_workspace_size", "mla_attend_absorbed",
            "mla_rope_norm_to_neox_perm",
@@ -69,6 +70,7 @@ def load(path: str = LIB_PATH):
     D = ctypes.POINTER(MlaDims)
     lib.mla_absorb_q.argtypes = [P, P, P, P, I32, D, P]
     lib.mla_absorb_q_rope.argtypes = [P, P, P, P, P, I32, F, D, P]
+    lib.mla_prolog_q.argtypes = [P, P, P, P, P, P, P, I32, I32, F, F, D, P, P]
     lib.mla_decode_workspace_size.argtypes = [I32, I32, D, ctypes.POINTER(ctypes.c_size_t)]
     lib.mla_decode_paged.argtypes = [P, P, P, P, P, P, I32, I32, I32, D, F, P,
                                      ctypes.c_size_t, P, P]
@@ -137,6 +139,16 @@ def mla_absorb_q_rope(q_abs, q_nope, q_pe, w_uk, positions, rows: int, rope_base
            load().mla_absorb_q_rope(_ptr(q_abs), _ptr(q_nope), _ptr(q_pe), _ptr(w_uk),
                                     _ptr(positions), rows, float(rope_base), ctypes.byref(dims),
                                     _stream(stream)))
+
+
+def mla_prolog_q(q_abs, c_q, gamma_q, w_uq, w_qr, w_uk, positions, rows: int, q_rank: int,
+                 eps: float, rope_base: float, dims: MlaDims, dev_err=None, stream=None):
+    """The query half of the prolog: RmsNorm of c_q, W^UQ / W^QR, absorb, rope."""
+    _check("mla_prolog_q",
+           load().mla_prolog_q(_ptr(q_abs), _ptr(c_q), _ptr(gamma_q), _ptr(w_uq), _ptr(w_qr),
+                               _ptr(w_uk), _ptr(positions), rows, q_rank, float(eps),
+                               float(rope_base), ctypes.byref(dims), _ptr(dev_err),
+                               _stream(stream)))
 
 
 def mla_decode_workspace_size(batch: int, max_blocks: int, dims: MlaDims) -> int:

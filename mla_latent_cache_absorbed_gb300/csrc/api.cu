@@ -157,6 +157,33 @@ mla_status mla_absorb_q_rope(void* q_abs, const void* q_nope, const void* q_pe,
     return MLA_OK;
 }
 
+mla_status mla_prolog_q(void* q_abs, const void* c_q, const void* gamma_q, const void* w_uq,
+                        const void* w_qr, const void* w_uk, const int64_t* positions,
+                        int32_t rows, int32_t q_rank, float eps, float rope_base,
+                        const mla_dims* dims, int32_t* dev_err, void* stream) {
+    g_last_error[0] = 0;
+    if (mla_status st = check_dims(dims)) return st;
+    REQUIRE(rows >= 0, "rows must be >= 0 (got %d)", rows);
+    REQUIRE(q_rank > 0 && q_rank % 8 == 0 && q_rank <= 16384,
+            "q_rank must be a positive multiple of 8, at most 16384 (got %d)", q_rank);
+    const int P = dims->d_rope;
+    REQUIRE(std::isfinite(eps) && eps >= 0.f, "eps must be finite and >= 0");
+    REQUIRE(P == 0 || (std::isfinite(rope_base) && rope_base > 0.f),
+            "rope_base must be finite and > 0");
+    REQUIRE((P & 1) == 0, "d_rope must be even");
+    if (rows == 0) return MLA_OK;
+    REQUIRE(q_abs && c_q && gamma_q && w_uq && w_uk, "q_abs, c_q, gamma_q, w_uq and w_uk must be non-NULL");
+    REQUIRE(P == 0 || (w_qr && positions), "w_qr and positions may be NULL only when d_rope == 0");
+    REQUIRE(aligned16(q_abs) && aligned16(c_q) && aligned16(gamma_q) && aligned16(w_uq) &&
+                aligned16(w_uk) && (!w_qr || aligned16(w_qr)) && ((uintptr_t)positions & 7u) == 0,
+            "device buffers must be 16-byte aligned, positions 8-byte aligned");
+    const float theta_scale = P > 0 ? powf(rope_base, -2.0f / (float)P) : 1.f;
+    MLA_CUDA_TRY(launch_prolog_q(q_abs, c_q, gamma_q, w_uq, w_qr, w_uk, positions, rows, q_rank,
+                                 eps, theta_scale, *dims, dev_err, (cudaStream_t)stream),
+                 "query prolog");
+    return MLA_OK;
+}
+
 mla_status mla_cache_append(void* kv_cache, const void* kv_c, const void* k_pe,
                             const int64_t* slot_mapping, int32_t n_tokens, int32_t num_blocks,
                             int32_t src_dtype, const mla_dims* dims, int32_t* dev_err,

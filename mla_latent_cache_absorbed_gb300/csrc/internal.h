@@ -46,6 +46,13 @@ cudaError_t launch_absorb_simt(void* q_abs, const void* q_nope, const void* q_pe
                                const void* w_uk, int32_t rows, const mla_dims& d,
                                cudaStream_t s, const int64_t* positions = nullptr,
                                float theta_scale = 1.f);
+// The query half of the prolog (tc_prolog.cu): the tensor-core kernel when
+// tc_prolog_supported, else the SIMT form.
+bool tc_prolog_supported(const mla_dims& d, int32_t q_rank);
+cudaError_t launch_prolog_q(void* q_abs, const void* c_q, const void* gamma_q, const void* w_uq,
+                            const void* w_qr, const void* w_uk, const int64_t* positions,
+                            int32_t rows, int32_t q_rank, float eps, float theta_scale,
+                            const mla_dims& d, int32_t* dev_err, cudaStream_t s);
 cudaError_t launch_decompress_simt(void* out, const void* o_lat, const void* w_uv,
                                    int32_t rows, const mla_dims& d, cudaStream_t s);
 cudaError_t launch_decode_simt(void* out, float* lse, const void* q_abs,

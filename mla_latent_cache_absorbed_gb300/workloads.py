@@ -386,3 +386,51 @@ def cache_with_rope_columns(wl: Workload, k_pe: np.ndarray) -> np.ndarray:
     poison_rows(cache, wl.seq_lens, wl.block_table, used, wl.meta["poison"],
                 g.dtype == "bf16", g.dtype == "f16")
     return cache
+
+
+# --------------------------------------------------------------------------
+# inputs of the query half of the prolog
+# --------------------------------------------------------------------------
+@dataclass
+class PrologQInputs:
+    """Inputs of the query half of the MLA prolog for one geometry: each query
+    row's x W^DQ before its norm (c_q), the norm's gamma, the projection
+    weights W^UQ [q_rank][H*d_nope] and W^QR [q_rank][H*d_rope] in the page's
+    (k, n) layout, W^UK [H][d_nope][kv_rank] and each row's position. Values
+    are f32, already rounded to the geometry's dtype."""
+    geom: Geometry
+    c_q: np.ndarray
+    gamma_q: np.ndarray
+    w_uq: np.ndarray
+    w_qr: np.ndarray
+    w_uk: np.ndarray
+    positions: np.ndarray
+    q_rank: int
+    eps: float
+    rope_base: float
+
+    @property
+    def rows(self) -> int:
+        return self.c_q.shape[0]
+
+
+def make_prolog_q(geom: Geometry, rows: int, q_rank: int = 1536, seed: int = 11,
+                  eps: float = 1e-6, rope_base: float = 10000.0) -> PrologQInputs:
+    """Seeded inputs of the query half of the prolog. The pages give no query
+    rank; 1536 is the default. c_q ~ 3 N(0, 1) (a down-projection's output,
+    not yet normed); gamma ~ U(0.5, 1.5); W^UQ, W^QR ~ N(0, sd = 1/sqrt(q_rank));
+    W^UK ~ N(0, sd = 1/sqrt(kv_rank)); positions U[0, 65536)."""
+    rng = np.random.default_rng(seed)
+    H, Dn, P, R = geom.n_head, geom.d_nope, geom.d_rope, geom.kv_rank
+    c_q = (3.0 * rng.standard_normal((rows, q_rank))).astype(np.float32)
+    gamma = (rng.random(q_rank) + 0.5).astype(np.float32)
+    s = 1.0 / math.sqrt(q_rank)
+    w_uq = (rng.standard_normal((q_rank, H * Dn)) * s).astype(np.float32)
+    w_qr = (rng.standard_normal((q_rank, H * P)) * s).astype(np.float32)
+    w_uk = (rng.standard_normal((H, Dn, R)) / math.sqrt(R)).astype(np.float32)
+    positions = rng.integers(0, 65536, rows).astype(np.int64)
+    if geom.dtype != "f32":
+        c_q, gamma = round_to(c_q, geom.dtype), round_to(gamma, geom.dtype)
+        w_uq, w_qr, w_uk = round_to(w_uq, geom.dtype), round_to(w_qr, geom.dtype), \
+            round_to(w_uk, geom.dtype)
+    return PrologQInputs(geom, c_q, gamma, w_uq, w_qr, w_uk, positions, q_rank, eps, rope_base)
