@@ -48,6 +48,8 @@ struct GemmParams {
     float theta_scale;           // absorb with positions: base^(-2/P)
     int a_rows;                  // rows of the A box (the M tile's real rows, multiple of 8)
     int early;                   // weights may be read before the previous kernel completes
+    int ns;                      // ring stages in use: min(kGStages, K / 64), so that a short
+                                 // K (the absorb's d_nope) leaves room for 2 CTAs per SM
     int32_t* dev_err;            // optional: timeout bit
 };
 
@@ -64,14 +66,15 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const int bchunk = p.n_tile * 128;  // bytes of one B chunk (n_tile x 64 K)
     const int stage_bytes = kAChunk + bchunk;
     const uint32_t a_bytes = (uint32_t)p.a_rows * 128;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kGStages * stage_bytes);
+    const int ns = p.ns;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + ns * stage_bytes);
     uint64_t* empty = full + kGStages;
     uint64_t* done = empty + kGStages;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(done + 1);
     grid_dependents_launch();  // the next kernel may start its own prologue
     if ((smem_u32(smem) & 1023) != 0) return;
     if (tid == 0) {
-        for (int s = 0; s < kGStages; ++s) {
+        for (int s = 0; s < ns; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
         }
@@ -108,7 +111,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 grid_dependency_wait();
             }
             auto load_b = [&](int kc) {
-                const int s = kc % kGStages;
+                const int s = kc % ns;
                 unsigned char* st = smem + s * stage_bytes;
                 if (kBMnMajor) {
                     // weight [K][N] (N contiguous): n_tile/64 boxes of [64 K rows][64 N]
@@ -121,16 +124,16 @@ __global__ void __launch_bounds__(kGThreads, 1)
                                 n0, h);
                 }
             };
-            const int early = nk < kGStages ? nk : kGStages;
+            const int early = nk < ns ? nk : ns;
             for (int kc = 0; kc < early; ++kc) {
                 mbar_arrive_expect_tx(smem_u32(&full[kc]), (uint32_t)bchunk + a_bytes);
                 load_b(kc);
             }
             grid_dependency_wait();
             for (int kc = 0; kc < nk; ++kc) {
-                const int s = kc % kGStages;
+                const int s = kc % ns;
                 if (kc >= early) {
-                    if (!mbar_wait(smem_u32(&empty[s]), ((kc / kGStages) & 1) ^ 1, kGWaitNs)) {
+                    if (!mbar_wait(smem_u32(&empty[s]), ((kc / ns) & 1) ^ 1, kGWaitNs)) {
                         ok = false;
                         break;
                     }
@@ -146,8 +149,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
         if (elect_one()) {
             const uint32_t idesc = idesc_f32acc<kF16>(128, p.n_tile, 0, kBMnMajor ? 1 : 0);
             for (int kc = 0; kc < nk; ++kc) {
-                const int s = kc % kGStages;
-                if (!mbar_wait(smem_u32(&full[s]), (kc / kGStages) & 1, kGWaitNs)) {
+                const int s = kc % ns;
+                if (!mbar_wait(smem_u32(&full[s]), (kc / ns) & 1, kGWaitNs)) {
                     ok = false;
                     break;
                 }
@@ -267,19 +270,19 @@ cudaError_t make_map(CUtensorMap* m, const void* base, cuuint64_t d0, cuuint64_t
     return cudaSuccess;
 }
 
-int smem_for(int n_tile) { return kGStages * (kAChunk + n_tile * 128) + 256; }
+int smem_for(int n_tile, int ns) { return ns * (kAChunk + n_tile * 128) + 256; }
 
 template <bool kBMnMajor, bool kF16>
 cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
                    cudaStream_t s) {
-    const int smem = smem_for(p.n_tile);
+    const int smem = smem_for(p.n_tile, p.ns);
     constexpr int kInst = (kBMnMajor ? 1 : 0) + (kF16 ? 2 : 0);
     static std::once_flag once[4];
     static cudaError_t attr_err[4] = {cudaSuccess, cudaSuccess, cudaSuccess, cudaSuccess};
     std::call_once(once[kInst], [&] {
         attr_err[kInst] = cudaFuncSetAttribute(
             tc_bgemm_kernel<kBMnMajor, kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-            smem_for(256));
+            smem_for(256, kGStages));
     });
     if (attr_err[kInst] != cudaSuccess) return attr_err[kInst];
     cudaLaunchConfig_t cfg = {};
@@ -732,6 +735,7 @@ cudaError_t launch_absorb_tc(void* q_abs, const void* q_nope, const void* q_pe,
     p.theta_scale = theta_scale;
     p.a_rows = a_rows;
     p.early = early ? 1 : 0;
+    p.ns = Dn / 64 < kGStages ? Dn / 64 : kGStages;
     p.dev_err = nullptr;
     return f16 ? launch<true, true>(a, b, p, s) : launch<true, false>(a, b, p, s);
 }
@@ -765,6 +769,7 @@ cudaError_t launch_decompress_tc(void* out, const void* o_lat, const void* w_uv,
     p.theta_scale = 1.f;
     p.a_rows = a_rows;
     p.early = early ? 1 : 0;
+    p.ns = R / 64 < kGStages ? R / 64 : kGStages;
     p.dev_err = nullptr;
     return f16 ? launch<false, true>(a, b, p, s) : launch<false, false>(a, b, p, s);
 }

@@ -10,11 +10,14 @@
 // and writes the decode's query row q_abs[r][h] = [q^N | q^R].
 //
 // Tensor-core kernel (bf16 / f16): one CTA per (head, 128 query rows).
-//   warps 2..5  one query row per thread: the row's sum of squares, then the
-//               A operand of the first GEMM (c^Q, normed, 64 columns at a
-//               time) into a 3-stage ring; after it, the epilogues
-//   warp 0      TMA of the weights: [W^UQ | W^QR] of the head for the first
-//               GEMM, W^UK[h] for the second, through the same ring
+//   warp 0      TMA through a 3-stage ring: first the tile's rows of c_q
+//               (64 columns a stage) for the norm's sums; then, for the first
+//               GEMM, the same rows again with the head's [W^UQ | W^QR]
+//               columns; then W^UK[h] for the second GEMM
+//   warps 2..5  one query row per thread: the row's sum of squares over the
+//               first sweep, then gamma x / RMS(x) in place in each stage of
+//               the second (the A operand of the first GEMM, rounded to the
+//               path's type); after it, the epilogues
 //   warp 1      tcgen05 MMAs (TMEM accumulators) and the TMEM allocation
 // GEMM 1: D1 [128 x (Dn + P)] = c^Q [128 x q_rank] . [W^UQ_h | W^QR_h].
 // Epilogue 1: q^C (Dn columns of D1) is rounded to the path's type into shared
@@ -51,7 +54,9 @@ constexpr int kPStage = kPAChunk + kPBChunk;
 constexpr int kPA2Off = kPStages * kPStage;  // q^C as GEMM 2's A: Dn / 64 chunks of 16 KB
 constexpr int kPMaxDn = 256;
 constexpr int kPBarOff = kPA2Off + (kPMaxDn / 64) * kPAChunk;
-constexpr int kPSmem = kPBarOff + 256;
+constexpr int kPGammaOff = kPBarOff + 256;     // gamma [q_rank], 16-bit
+constexpr int kPMaxQRank = 8192;
+constexpr int kPSmem = kPGammaOff + kPMaxQRank * 2;
 constexpr uint64_t kPWaitNs = 2000000000ull;
 static_assert(kPSmem <= 232448 - 1024, "shared memory budget (with alignment slack)");
 
@@ -61,6 +66,7 @@ struct PrologParams {
     uint16_t* q_abs;            // [rows][H][R + P]
     const int64_t* positions;   // [rows] (P > 0)
     int rows, q_rank, H, Dn, P, R;
+    int a_rows;                 // rows of the c_q box: the tile's rows, rounded up to 8
     float eps, theta_scale;
     int32_t* dev_err;
 };
@@ -72,19 +78,22 @@ __device__ __forceinline__ float to_f32(uint32_t bits16) {
 
 template <bool kF16>
 __global__ void __launch_bounds__(kPThreads, 1)
-    tc_prolog_q_kernel(const __grid_constant__ CUtensorMap uqmap,
+    tc_prolog_q_kernel(const __grid_constant__ CUtensorMap cqmap,
+                       const __grid_constant__ CUtensorMap uqmap,
                        const __grid_constant__ CUtensorMap qrmap,
                        const __grid_constant__ CUtensorMap ukmap, const PrologParams p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // the swizzled operands need a 1 KB-aligned base
     unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint64_t* fullA = reinterpret_cast<uint64_t*>(smem + kPBarOff);  // row threads (128)
-    uint64_t* fullB = fullA + kPStages;                              // TMA bytes (1)
+    uint64_t* fullB = fullA + kPStages;                              // TMA bytes (1): c_q + weights
     uint64_t* empty = fullB + kPStages;                              // MMA commit (1)
     uint64_t* d1done = empty + kPStages;
     uint64_t* a2ready = d1done + 1;
     uint64_t* d2done = a2ready + 1;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(d2done + 1);
+    uint64_t* ssfull = d2done + 1;       // first sweep: c_q chunk landed (TMA bytes)
+    uint64_t* ssfree = ssfull + kPStages;  // first sweep: chunk read (row threads, 128)
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(ssfree + kPStages);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = blockIdx.x;
     const int m0 = blockIdx.y * 128;
@@ -100,6 +109,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
         mbar_init(smem_u32(d1done), 1);
         mbar_init(smem_u32(a2ready), 128);
         mbar_init(smem_u32(d2done), 1);
+        for (int s = 0; s < kPStages; ++s) {
+            mbar_init(smem_u32(&ssfull[s]), 1);
+            mbar_init(smem_u32(&ssfree[s]), 128);
+        }
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -115,9 +128,27 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (warp == 0) {
         // ---------------- weights: GEMM 1 chunks, then GEMM 2 chunks, one ring
         if (elect_one()) {
+            tma_prefetch_desc(&cqmap);
             tma_prefetch_desc(&uqmap);
             if (p.P) tma_prefetch_desc(&qrmap);
             tma_prefetch_desc(&ukmap);
+            // first sweep: c_q chunks for the norm's sums
+            for (int j = 0; j < nk1 && ok; ++j) {
+                const int s = j % kPStages;
+                if (j >= kPStages &&
+                    !mbar_wait_sleep(smem_u32(&ssfree[s]), ((j / kPStages) - 1) & 1, kPWaitNs)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(smem_u32(&ssfull[s]), (uint32_t)(p.a_rows * 128));
+                tma_load_2d(smem_u32(smem + s * kPStage), &cqmap, smem_u32(&ssfull[s]), j * 64, m0);
+            }
+            // each stage's last use in the first sweep must be read before the
+            // second sweep refills it
+            for (int s = 0; s < kPStages && s < nk1 && ok; ++s) {
+                const int jl = s + ((nk1 - 1 - s) / kPStages) * kPStages;  // last chunk in stage s
+                if (!mbar_wait_sleep(smem_u32(&ssfree[s]), (jl / kPStages) & 1, kPWaitNs)) ok = false;
+            }
             const int nload = nk1 + 2 * nk2;
             for (int j = 0; j < nload && ok; ++j) {
                 const int s = j % kPStages;
@@ -127,8 +158,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 }
                 unsigned char* b = smem + s * kPStage + kPAChunk;
                 if (j < nk1) {
-                    // [64 K rows][64 N] boxes: W^UQ's Dn columns of head h, then W^QR's P
-                    mbar_arrive_expect_tx(smem_u32(&fullB[s]), (uint32_t)(N1 * 128));
+                    // the tile's rows of c_q, columns 64 j .. +63 (rows past the
+                    // batch read as zeros), then [64 K rows][64 N] boxes: W^UQ's Dn
+                    // columns of head h and W^QR's P
+                    mbar_arrive_expect_tx(smem_u32(&fullB[s]), (uint32_t)(p.a_rows * 128 + N1 * 128));
+                    tma_load_2d(smem_u32(smem + s * kPStage), &cqmap, smem_u32(&fullB[s]), j * 64, m0);
                     for (int c = 0; c < p.Dn / 64; ++c)
                         tma_load_2d(smem_u32(b + c * 8192), &uqmap, smem_u32(&fullB[s]),
                                     h * p.Dn + c * 64, j * 64);
@@ -199,13 +233,25 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const int row = m0 + r;
         const bool valid = row < p.rows;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        const uint4* xrow = reinterpret_cast<const uint4*>(p.cq + (long long)(valid ? row : 0) * p.q_rank);
-        const uint4* g4 = reinterpret_cast<const uint4*>(p.gamma);
-        // 1. RMS of the row (f32 sum of squares in column order)
+        // gamma into shared memory once (the 128 row threads; read back after
+        // the first sweep)
+        const uint32_t gsm = smem_u32(smem + kPGammaOff);
+        for (int i = q * 32 + lane; i < p.q_rank / 8; i += 128) {
+            const uint4 g = reinterpret_cast<const uint4*>(p.gamma)[i];
+            st_shared_v4(gsm + i * 16, g.x, g.y, g.z, g.w);
+        }
+        // 1. the row's sum of squares (f32, in column order) over the first sweep
         float ss = 0.f;
-        if (valid)
-            for (int c8 = 0; c8 < p.q_rank / 8; ++c8) {
-                const uint4 v = xrow[c8];
+        for (int j = 0; j < nk1; ++j) {
+            const int s = j % kPStages;
+            if (!__all_sync(0xffffffffu, mbar_wait_sleep(smem_u32(&ssfull[s]), (j / kPStages) & 1, kPWaitNs))) {
+                ok = false;
+                break;
+            }
+            const uint32_t arow = smem_u32(smem + s * kPStage) + r * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint4 v = ld_shared_v4(arow + ((c ^ (r & 7)) << 4));
                 const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -214,30 +260,34 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     ss = fmaf(b, b, ss);
                 }
             }
+            mbar_arrive(smem_u32(&ssfree[s]));
+        }
+        // the row's norm factor 1 / RMS (zero for rows past the batch)
         const float inv = valid ? 1.0f / sqrtf(ss / (float)p.q_rank + p.eps) : 0.f;
-        // 2. A operand of GEMM 1: 64 columns of gamma x / RMS per stage
-        for (int j = 0; j < nk1; ++j) {
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // gamma is in shared memory
+        // 2. the A operand of GEMM 1, gamma x / RMS, in place in each stage of
+        //    the second sweep as it lands (rows past the box hold stale values:
+        //    their products are never stored)
+        for (int j = 0; j < nk1 && ok; ++j) {
             const int s = j % kPStages;
-            if (!__all_sync(0xffffffffu,
-                            mbar_wait_sleep(smem_u32(&empty[s]), ((j / kPStages) & 1) ^ 1, kPWaitNs))) {
+            if (!__all_sync(0xffffffffu, mbar_wait_sleep(smem_u32(&fullB[s]), (j / kPStages) & 1, kPWaitNs))) {
                 ok = false;
                 break;
             }
             const uint32_t arow = smem_u32(smem + s * kPStage) + r * 128;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                uint32_t o[4] = {0u, 0u, 0u, 0u};
-                if (valid) {
-                    const uint4 v = xrow[j * 8 + c];
-                    const uint4 gv = g4[j * 8 + c];
-                    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-                    const uint32_t gu[4] = {gv.x, gv.y, gv.z, gv.w};
+                const uint32_t at = arow + ((c ^ (r & 7)) << 4);
+                const uint4 v = ld_shared_v4(at);
+                const uint4 gv = ld_shared_v4(gsm + (j * 8 + c) * 16);
+                const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+                const uint32_t gu[4] = {gv.x, gv.y, gv.z, gv.w};
+                uint32_t o[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        o[e] = pack2<kF16>(elem_lo<kF16>(gu[e]) * elem_lo<kF16>(u[e]) * inv,
-                                           elem_hi<kF16>(gu[e]) * elem_hi<kF16>(u[e]) * inv);
-                }
-                st_shared_v4(arow + ((c ^ (r & 7)) << 4), o[0], o[1], o[2], o[3]);
+                for (int e = 0; e < 4; ++e)
+                    o[e] = pack2<kF16>(elem_lo<kF16>(gu[e]) * elem_lo<kF16>(u[e]) * inv,
+                                       elem_hi<kF16>(gu[e]) * elem_hi<kF16>(u[e]) * inv);
+                st_shared_v4(at, o[0], o[1], o[2], o[3]);
             }
             fence_proxy_async_smem();
             mbar_arrive(smem_u32(&fullA[s]));
@@ -252,14 +302,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 tmem_ld32(tbase + lane_off + cb, v);
                 tmem_wait_ld();
                 const uint32_t chunk = smem_u32(smem + kPA2Off + (cb >> 6) * kPAChunk) + r * 128;
+                float f[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(v[e]);  // q^C
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int c = ((cb & 63) >> 3) + u;  // 16-byte piece within the 128-byte row
-                    st_shared_v4(chunk + ((c ^ (r & 7)) << 4),
-                                 pack2<kF16>(__uint_as_float(v[8 * u]), __uint_as_float(v[8 * u + 1])),
-                                 pack2<kF16>(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3])),
-                                 pack2<kF16>(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5])),
-                                 pack2<kF16>(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7])));
+                    st_shared_v4(chunk + ((c ^ (r & 7)) << 4), pack2<kF16>(f[8 * u], f[8 * u + 1]),
+                                 pack2<kF16>(f[8 * u + 2], f[8 * u + 3]),
+                                 pack2<kF16>(f[8 * u + 4], f[8 * u + 5]),
+                                 pack2<kF16>(f[8 * u + 6], f[8 * u + 7]));
                 }
             }
             if (p.P > 0) {
@@ -456,6 +508,7 @@ cudaError_t prolog_map(CUtensorMap* m, const void* base, int rank, const cuuint6
 bool tc_prolog_supported(const mla_dims& d, int32_t q_rank) {
     return d.dtype != MLA_F32 && d.kv_rank == 512 && d.d_nope % 64 == 0 && d.d_rope % 64 == 0 &&
            d.d_nope + d.d_rope <= 256 && d.d_nope <= kPMaxDn && q_rank % 64 == 0 && q_rank > 0 &&
+           q_rank <= kPMaxQRank &&
            d.n_head <= 65535;
 }
 
@@ -467,7 +520,14 @@ cudaError_t launch_prolog_q(void* q_abs, const void* c_q, const void* gamma_q, c
     const int H = d.n_head, Dn = d.d_nope, P = d.d_rope, R = d.kv_rank;
     if (tc_prolog_supported(d, q_rank)) {
         const bool f16 = d.dtype == MLA_F16;
-        CUtensorMap uq, qr, uk;
+        CUtensorMap cqm, uq, qr, uk;
+        {
+            // c_q [rows][q_rank]: {q_rank, rows}, boxes of 64 columns x 128 rows
+            cuuint64_t dims[2] = {(cuuint64_t)q_rank, (cuuint64_t)rows};
+            cuuint64_t str[1] = {(cuuint64_t)q_rank * 2};
+            cuuint32_t box[2] = {64, (cuuint32_t)(rows >= 128 ? 128 : (rows + 7) / 8 * 8)};
+            if (cudaError_t e = prolog_map(&cqm, c_q, 2, dims, str, box, f16)) return e;
+        }
         {
             // W^UQ [q_rank][H * Dn]: {H * Dn, q_rank}, boxes of 64 columns x 64 rows
             cuuint64_t dims[2] = {(cuuint64_t)H * Dn, (cuuint64_t)q_rank};
@@ -501,6 +561,7 @@ cudaError_t launch_prolog_q(void* q_abs, const void* c_q, const void* gamma_q, c
         p.Dn = Dn;
         p.P = P;
         p.R = R;
+        p.a_rows = rows >= 128 ? 128 : (rows + 7) / 8 * 8;
         p.eps = eps;
         p.theta_scale = theta_scale;
         p.dev_err = dev_err;
@@ -517,9 +578,9 @@ cudaError_t launch_prolog_q(void* q_abs, const void* c_q, const void* gamma_q, c
         if (attr_err[f16 ? 1 : 0] != cudaSuccess) return attr_err[f16 ? 1 : 0];
         const dim3 grid((unsigned)H, (unsigned)((rows + 127) / 128), 1);
         if (f16)
-            tc_prolog_q_kernel<true><<<grid, kPThreads, smem, s>>>(uq, qr, uk, p);
+            tc_prolog_q_kernel<true><<<grid, kPThreads, smem, s>>>(cqm, uq, qr, uk, p);
         else
-            tc_prolog_q_kernel<false><<<grid, kPThreads, smem, s>>>(uq, qr, uk, p);
+            tc_prolog_q_kernel<false><<<grid, kPThreads, smem, s>>>(cqm, uq, qr, uk, p);
         return cudaGetLastError();
     }
     const size_t smem = (size_t)(q_rank + Dn + P + 8) * sizeof(float);
