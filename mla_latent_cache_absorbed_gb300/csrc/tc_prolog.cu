@@ -47,18 +47,24 @@ namespace {
 using namespace sm100;
 
 constexpr int kPThreads = 192;
-constexpr int kPStages = 3;
-constexpr int kPAChunk = 128 * 128;          // A: 128 rows x 64 columns, 16-bit
+// Shared memory (worked out at launch from the tile's rows, rounded to 8):
+//   ns ring stages, each [A: the tile's rows x 64 columns | B: 32 KB]
+//   q^C, GEMM 2's A: Dn / 64 chunks of the tile's rows x 64 columns
+//   barriers, then gamma
+// A tile of fewer than 128 rows keeps only its rows; the MMAs (M = 128) then
+// read the memory after them as the rows past the tile, whose results are
+// never used, and the ring gets more stages: more weight bytes in flight.
+constexpr int kPAFull = 128 * 128;           // A of a full tile: 128 rows x 64 columns, 16-bit
 constexpr int kPBChunk = 256 * 128;          // B: up to 256 output columns x 64 K
-constexpr int kPStage = kPAChunk + kPBChunk;
-constexpr int kPA2Off = kPStages * kPStage;  // q^C as GEMM 2's A: Dn / 64 chunks of 16 KB
+constexpr int kPMaxStages = 6;
 constexpr int kPMaxDn = 256;
-constexpr int kPBarOff = kPA2Off + (kPMaxDn / 64) * kPAChunk;
-constexpr int kPGammaOff = kPBarOff + 256;     // gamma [q_rank], 16-bit
 constexpr int kPMaxQRank = 8192;
-constexpr int kPSmem = kPGammaOff + kPMaxQRank * 2;
+constexpr int kPSmemMax = 232448 - 1024;     // with the alignment slack
+constexpr int kPBarBytes = 1024;             // barriers and the TMEM slot, then 1/RMS of 128 rows
+constexpr int kPInvOff = 512;
+static_assert((5 * kPMaxStages + 3) * 8 + 4 <= kPInvOff && kPInvOff + 128 * 4 <= kPBarBytes,
+              "barrier area");
 constexpr uint64_t kPWaitNs = 2000000000ull;
-static_assert(kPSmem <= 232448 - 1024, "shared memory budget (with alignment slack)");
 
 struct PrologParams {
     const uint16_t* cq;         // [rows][q_rank], 16-bit elements
@@ -67,6 +73,8 @@ struct PrologParams {
     const int64_t* positions;   // [rows] (P > 0)
     int rows, q_rank, H, Dn, P, R;
     int a_rows;                 // rows of the c_q box: the tile's rows, rounded up to 8
+    int ns, stage, areg;        // ring stages, bytes per stage, bytes of its A part
+    int a2, a2s, bar, gam;      // offsets of q^C, its chunk stride, barriers, gamma
     float eps, theta_scale;
     int32_t* dev_err;
 };
@@ -85,15 +93,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // the swizzled operands need a 1 KB-aligned base
     unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    uint64_t* fullA = reinterpret_cast<uint64_t*>(smem + kPBarOff);  // row threads (128)
-    uint64_t* fullB = fullA + kPStages;                              // TMA bytes (1): c_q + weights
-    uint64_t* empty = fullB + kPStages;                              // MMA commit (1)
-    uint64_t* d1done = empty + kPStages;
+    const int ns = p.ns;
+    uint64_t* fullA = reinterpret_cast<uint64_t*>(smem + p.bar);  // row threads (128)
+    uint64_t* fullB = fullA + kPMaxStages;                        // TMA bytes (1): c_q + weights
+    uint64_t* empty = fullB + kPMaxStages;                        // MMA commit (1)
+    uint64_t* d1done = empty + ns;
     uint64_t* a2ready = d1done + 1;
     uint64_t* d2done = a2ready + 1;
-    uint64_t* ssfull = d2done + 1;       // first sweep: c_q chunk landed (TMA bytes)
-    uint64_t* ssfree = ssfull + kPStages;  // first sweep: chunk read (row threads, 128)
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(ssfree + kPStages);
+    uint64_t* ssfull = d2done + 1;          // first sweep: c_q chunk landed (TMA bytes)
+    uint64_t* ssfree = ssfull + kPMaxStages;  // first sweep: chunk read (row threads, 128)
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(ssfree + kPMaxStages);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = blockIdx.x;
     const int m0 = blockIdx.y * 128;
@@ -101,7 +110,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int nk1 = p.q_rank / 64;       // GEMM 1 K chunks
     const int nk2 = p.Dn / 64;           // GEMM 2 K chunks (each in two 256-column halves)
     if (tid == 0) {
-        for (int s = 0; s < kPStages; ++s) {
+        for (int s = 0; s < ns; ++s) {
             mbar_init(smem_u32(&fullA[s]), 128);
             mbar_init(smem_u32(&fullB[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
@@ -109,7 +118,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         mbar_init(smem_u32(d1done), 1);
         mbar_init(smem_u32(a2ready), 128);
         mbar_init(smem_u32(d2done), 1);
-        for (int s = 0; s < kPStages; ++s) {
+        for (int s = 0; s < ns; ++s) {
             mbar_init(smem_u32(&ssfull[s]), 1);
             mbar_init(smem_u32(&ssfree[s]), 128);
         }
@@ -134,35 +143,35 @@ __global__ void __launch_bounds__(kPThreads, 1)
             tma_prefetch_desc(&ukmap);
             // first sweep: c_q chunks for the norm's sums
             for (int j = 0; j < nk1 && ok; ++j) {
-                const int s = j % kPStages;
-                if (j >= kPStages &&
-                    !mbar_wait_sleep(smem_u32(&ssfree[s]), ((j / kPStages) - 1) & 1, kPWaitNs)) {
+                const int s = j % ns;
+                if (j >= ns &&
+                    !mbar_wait_sleep(smem_u32(&ssfree[s]), ((j / ns) - 1) & 1, kPWaitNs)) {
                     ok = false;
                     break;
                 }
                 mbar_arrive_expect_tx(smem_u32(&ssfull[s]), (uint32_t)(p.a_rows * 128));
-                tma_load_2d(smem_u32(smem + s * kPStage), &cqmap, smem_u32(&ssfull[s]), j * 64, m0);
+                tma_load_2d(smem_u32(smem + s * p.stage), &cqmap, smem_u32(&ssfull[s]), j * 64, m0);
             }
             // each stage's last use in the first sweep must be read before the
             // second sweep refills it
-            for (int s = 0; s < kPStages && s < nk1 && ok; ++s) {
-                const int jl = s + ((nk1 - 1 - s) / kPStages) * kPStages;  // last chunk in stage s
-                if (!mbar_wait_sleep(smem_u32(&ssfree[s]), (jl / kPStages) & 1, kPWaitNs)) ok = false;
+            for (int s = 0; s < ns && s < nk1 && ok; ++s) {
+                const int jl = s + ((nk1 - 1 - s) / ns) * ns;  // last chunk in stage s
+                if (!mbar_wait_sleep(smem_u32(&ssfree[s]), (jl / ns) & 1, kPWaitNs)) ok = false;
             }
             const int nload = nk1 + 2 * nk2;
             for (int j = 0; j < nload && ok; ++j) {
-                const int s = j % kPStages;
-                if (!mbar_wait_sleep(smem_u32(&empty[s]), ((j / kPStages) & 1) ^ 1, kPWaitNs)) {
+                const int s = j % ns;
+                if (!mbar_wait_sleep(smem_u32(&empty[s]), ((j / ns) & 1) ^ 1, kPWaitNs)) {
                     ok = false;
                     break;
                 }
-                unsigned char* b = smem + s * kPStage + kPAChunk;
+                unsigned char* b = smem + s * p.stage + p.areg;
                 if (j < nk1) {
                     // the tile's rows of c_q, columns 64 j .. +63 (rows past the
                     // batch read as zeros), then [64 K rows][64 N] boxes: W^UQ's Dn
                     // columns of head h and W^QR's P
                     mbar_arrive_expect_tx(smem_u32(&fullB[s]), (uint32_t)(p.a_rows * 128 + N1 * 128));
-                    tma_load_2d(smem_u32(smem + s * kPStage), &cqmap, smem_u32(&fullB[s]), j * 64, m0);
+                    tma_load_2d(smem_u32(smem + s * p.stage), &cqmap, smem_u32(&fullB[s]), j * 64, m0);
                     for (int c = 0; c < p.Dn / 64; ++c)
                         tma_load_2d(smem_u32(b + c * 8192), &uqmap, smem_u32(&fullB[s]),
                                     h * p.Dn + c * 64, j * 64);
@@ -185,16 +194,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const uint32_t idesc1 = idesc_f32acc<kF16>(128, N1, 0, 1);
             constexpr uint32_t idesc2 = idesc_f32acc<kF16>(128, 256, 0, 1);
             for (int j = 0; j < nk1; ++j) {
-                const int s = j % kPStages;
-                const uint32_t par = (j / kPStages) & 1;
+                const int s = j % ns;
+                const uint32_t par = (j / ns) & 1;
                 if (!mbar_wait(smem_u32(&fullB[s]), par, kPWaitNs) ||
                     !mbar_wait(smem_u32(&fullA[s]), par, kPWaitNs)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a = smem_u32(smem + s * kPStage);
-                const uint32_t b = a + kPAChunk;
+                const uint32_t a = smem_u32(smem + s * p.stage);
+                const uint32_t b = a + p.areg;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_ss(tbase, sdesc_sw128(a + kk * 32, 16, 1024),
@@ -206,15 +215,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
             if (ok && mbar_wait_sleep(smem_u32(a2ready), 0, kPWaitNs)) {
                 tc_fence_after();
                 for (int t = 0; t < 2 * nk2; ++t) {
-                    const int j = nk1 + t, s = j % kPStages;
+                    const int j = nk1 + t, s = j % ns;
                     const int kc = t >> 1, half = t & 1;
-                    if (!mbar_wait(smem_u32(&fullB[s]), (j / kPStages) & 1, kPWaitNs)) {
+                    if (!mbar_wait(smem_u32(&fullB[s]), (j / ns) & 1, kPWaitNs)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a = smem_u32(smem + kPA2Off + kc * kPAChunk);
-                    const uint32_t b = smem_u32(smem + s * kPStage + kPAChunk);
+                    const uint32_t a = smem_u32(smem + p.a2 + kc * p.a2s);
+                    const uint32_t b = smem_u32(smem + s * p.stage + p.areg);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         mma_ss(tbase + half * 256, sdesc_sw128(a + kk * 32, 16, 1024),
@@ -235,59 +244,96 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         // gamma into shared memory once (the 128 row threads; read back after
         // the first sweep)
-        const uint32_t gsm = smem_u32(smem + kPGammaOff);
+        const uint32_t gsm = smem_u32(smem + p.gam);
+        const bool in_box = r < p.a_rows;  // the row has its place in the stages and in q^C
         for (int i = q * 32 + lane; i < p.q_rank / 8; i += 128) {
             const uint4 g = reinterpret_cast<const uint4*>(p.gamma)[i];
             st_shared_v4(gsm + i * 16, g.x, g.y, g.z, g.w);
         }
-        // 1. the row's sum of squares (f32, in column order) over the first sweep
-        float ss = 0.f;
+        // The sweeps take the stage's 16-byte pieces as work items: thread rt
+        // of the 128 handles piece rt % 8 of rows rt / 8 + 16 k, so that every
+        // row's eight pieces sit in eight lanes of one warp and a tile of few
+        // rows still spreads over many threads; each thread issues all its
+        // loads of a stage before it uses them.
+        const int rt = (warp - 2) * 32 + lane;
+        const int pc = rt & 7, g16 = rt >> 3;
+        float* inv_sh = reinterpret_cast<float*>(smem + p.bar + kPInvOff);
+        // 1. each row's sum of squares over the first sweep (f32; the row's
+        //    pieces summed in order of their columns, then across the pieces)
+        float ssk[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ssk[k] = 0.f;
         for (int j = 0; j < nk1; ++j) {
-            const int s = j % kPStages;
-            if (!__all_sync(0xffffffffu, mbar_wait_sleep(smem_u32(&ssfull[s]), (j / kPStages) & 1, kPWaitNs))) {
+            const int s = j % ns;
+            if (!__all_sync(0xffffffffu, mbar_wait_sleep(smem_u32(&ssfull[s]), (j / ns) & 1, kPWaitNs))) {
                 ok = false;
                 break;
             }
-            const uint32_t arow = smem_u32(smem + s * kPStage) + r * 128;
+            const uint32_t st = smem_u32(smem + s * p.stage);
+            uint4 v[8];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint4 v = ld_shared_v4(arow + ((c ^ (r & 7)) << 4));
-                const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+            for (int k = 0; k < 8; ++k) {
+                const int rr = g16 + 16 * k;
+                v[k] = rr < p.a_rows ? ld_shared_v4(st + rr * 128 + ((pc ^ (rr & 7)) << 4))
+                                     : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t u[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float a = elem_lo<kF16>(u[e]), b = elem_hi<kF16>(u[e]);
-                    ss = fmaf(a, a, ss);
-                    ss = fmaf(b, b, ss);
+                    ssk[k] = fmaf(a, a, ssk[k]);
+                    ssk[k] = fmaf(b, b, ssk[k]);
                 }
             }
             mbar_arrive(smem_u32(&ssfree[s]));
         }
-        // the row's norm factor 1 / RMS (zero for rows past the batch)
-        const float inv = valid ? 1.0f / sqrtf(ss / (float)p.q_rank + p.eps) : 0.f;
-        asm volatile("bar.sync 1, 128;" ::: "memory");  // gamma is in shared memory
+        // each row's norm factor 1 / RMS (zero for rows past the batch)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            float t = ssk[k];
+            t += __shfl_xor_sync(0xffffffffu, t, 1);
+            t += __shfl_xor_sync(0xffffffffu, t, 2);
+            t += __shfl_xor_sync(0xffffffffu, t, 4);
+            const int rr = g16 + 16 * k;
+            if (pc == 0) inv_sh[rr] = (m0 + rr < p.rows) ? 1.0f / sqrtf(t / (float)p.q_rank + p.eps) : 0.f;
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // gamma and 1/RMS are in shared memory
+        float invk[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) invk[k] = inv_sh[g16 + 16 * k];
         // 2. the A operand of GEMM 1, gamma x / RMS, in place in each stage of
-        //    the second sweep as it lands (rows past the box hold stale values:
-        //    their products are never stored)
+        //    the second sweep as it lands (rows past the box are not touched:
+        //    the MMA reads whatever follows them, and those rows are never stored)
         for (int j = 0; j < nk1 && ok; ++j) {
-            const int s = j % kPStages;
-            if (!__all_sync(0xffffffffu, mbar_wait_sleep(smem_u32(&fullB[s]), (j / kPStages) & 1, kPWaitNs))) {
+            const int s = j % ns;
+            if (!__all_sync(0xffffffffu, mbar_wait_sleep(smem_u32(&fullB[s]), (j / ns) & 1, kPWaitNs))) {
                 ok = false;
                 break;
             }
-            const uint32_t arow = smem_u32(smem + s * kPStage) + r * 128;
+            const uint32_t st = smem_u32(smem + s * p.stage);
+            const uint4 gv = ld_shared_v4(gsm + (j * 8 + pc) * 16);
+            const uint32_t gu[4] = {gv.x, gv.y, gv.z, gv.w};
+            uint4 v[8];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint32_t at = arow + ((c ^ (r & 7)) << 4);
-                const uint4 v = ld_shared_v4(at);
-                const uint4 gv = ld_shared_v4(gsm + (j * 8 + c) * 16);
-                const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-                const uint32_t gu[4] = {gv.x, gv.y, gv.z, gv.w};
-                uint32_t o[4];
+            for (int k = 0; k < 8; ++k) {
+                const int rr = g16 + 16 * k;
+                v[k] = rr < p.a_rows ? ld_shared_v4(st + rr * 128 + ((pc ^ (rr & 7)) << 4))
+                                     : make_uint4(0u, 0u, 0u, 0u);
+            }
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    o[e] = pack2<kF16>(elem_lo<kF16>(gu[e]) * elem_lo<kF16>(u[e]) * inv,
-                                       elem_hi<kF16>(gu[e]) * elem_hi<kF16>(u[e]) * inv);
-                st_shared_v4(at, o[0], o[1], o[2], o[3]);
+            for (int k = 0; k < 8; ++k) {
+                const int rr = g16 + 16 * k;
+                if (rr < p.a_rows) {
+                    const uint32_t u[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        o[e] = pack2<kF16>(elem_lo<kF16>(gu[e]) * elem_lo<kF16>(u[e]) * invk[k],
+                                           elem_hi<kF16>(gu[e]) * elem_hi<kF16>(u[e]) * invk[k]);
+                    st_shared_v4(st + rr * 128 + ((pc ^ (rr & 7)) << 4), o[0], o[1], o[2], o[3]);
+                }
             }
             fence_proxy_async_smem();
             mbar_arrive(smem_u32(&fullA[s]));
@@ -301,7 +347,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 uint32_t v[32];
                 tmem_ld32(tbase + lane_off + cb, v);
                 tmem_wait_ld();
-                const uint32_t chunk = smem_u32(smem + kPA2Off + (cb >> 6) * kPAChunk) + r * 128;
+                const uint32_t chunk = smem_u32(smem + p.a2 + (cb >> 6) * p.a2s) + r * 128;
+                if (!in_box) continue;  // (the TMEM load above is warp-wide)
                 float f[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(v[e]);  // q^C
@@ -562,18 +609,41 @@ cudaError_t launch_prolog_q(void* q_abs, const void* c_q, const void* gamma_q, c
         p.P = P;
         p.R = R;
         p.a_rows = rows >= 128 ? 128 : (rows + 7) / 8 * 8;
+        {
+            // the layout above: A parts and q^C chunks of the tile's rows
+            // (whole 8-row groups), the ring as deep as the rest allows
+            const int areg = (p.a_rows * 128 + 1023) / 1024 * 1024;
+            p.areg = areg;
+            p.stage = areg + kPBChunk;
+            const int nk2 = Dn / 64;
+            const int a2_bytes = nk2 * areg + (kPAFull - areg);  // the last chunk's MMA reads 16 KB
+            const int tail = a2_bytes + kPBarBytes + q_rank * 2;
+            int ns = (kPSmemMax - tail) / p.stage;
+            ns = ns > kPMaxStages ? kPMaxStages : ns;
+            if (ns < 2) {
+                set_error("mla_prolog_q: shared memory for the ring does not fit");
+                return cudaErrorInvalidValue;
+            }
+            p.ns = ns;
+            p.a2 = ns * p.stage;
+            p.a2s = areg;
+            p.bar = p.a2 + a2_bytes;
+            p.gam = p.bar + kPBarBytes;
+        }
         p.eps = eps;
         p.theta_scale = theta_scale;
         p.dev_err = dev_err;
-        const int smem = kPSmem + 1024;  // + alignment slack
+        const int smem = p.gam + q_rank * 2 + 1024;  // + alignment slack
         static std::once_flag once[2];
         static cudaError_t attr_err[2] = {cudaSuccess, cudaSuccess};
         std::call_once(once[f16 ? 1 : 0], [&] {
             attr_err[f16 ? 1 : 0] =
                 f16 ? cudaFuncSetAttribute(tc_prolog_q_kernel<true>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kPSmemMax + 1024)
                     : cudaFuncSetAttribute(tc_prolog_q_kernel<false>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kPSmemMax + 1024);
         });
         if (attr_err[f16 ? 1 : 0] != cudaSuccess) return attr_err[f16 ? 1 : 0];
         const dim3 grid((unsigned)H, (unsigned)((rows + 127) / 128), 1);
