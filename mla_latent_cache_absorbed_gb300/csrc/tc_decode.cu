@@ -16,8 +16,10 @@
 // tiles). In each pair:
 //   CTA 0 ("S-CTA") holds the 128 query rows in TMEM (A operand) and computes
 //     S = Q K^T for each tile (M=128, N=64, K=576 or 512) into TMEM, runs the
-//     online softmax (two threads per query row, lazy rescaling), and writes
-//     the bf16 probabilities P [128 x 64] into CTA 1's shared memory.
+//     online softmax (two threads per query row, lazy rescaling) and stages
+//     the bf16 probabilities P [128 x 64] in TMEM; four sender warps copy
+//     them into CTA 1's shared memory, so the SM-to-SM transfer (tens of
+//     GB/s) overlaps the next tile's softmax instead of stalling it.
 //   CTA 1 ("O-CTA") holds O [128 x 512] f32 in all 512 TMEM columns and
 //     computes O += P V (M=128, N=2x256, K=64) with V the leading 512 columns
 //     of the same tile, which it loads itself (L2 hits: its prefetcher warp
@@ -57,12 +59,14 @@ using split::aligned_decide;
 using split::pairs_per_set;
 
 constexpr int kTok = 64;                      // cache tokens per tile
-constexpr int kNS = 3;                        // pipeline stages
+constexpr int kNS = 3;                        // S-CTA pipeline stages (K of a tile)
+constexpr int kNV = 2;                        // O-CTA pipeline stages (V of a tile)
+constexpr int kNP = 5;                        // O-CTA P slots
 constexpr int kChunk = 64 * 128;              // 64 tokens x 64 columns of bf16
 constexpr int kStage = 8 * kChunk;            // O-CTA: V (latent 512 columns) of a tile
-constexpr int kSideOff = kNS * kStage;        // O-CTA: P slots
+constexpr int kSideOff = kNV * kStage;        // O-CTA: P slots
 constexpr int kPBytes = 128 * 128;            // P [128 rows x 64 tokens] bf16
-constexpr int kCtrlOff = kSideOff + 2 * kPBytes;
+constexpr int kPSlot = kPBytes + 1024;        // a P slot: P, then its AlphaMsg (1 KB aligned)
 constexpr int kQChunk = 128 * 128;            // 128 query rows x 64 columns of bf16
 constexpr int kVBlock = 8 * 2048;             // O-CTA: one block's V as [8 chunks][16 rows][128 B]
 // S-CTA stage of a tile: its 4 cache blocks, each landed by one 5-D box as
@@ -78,12 +82,14 @@ __host__ __device__ constexpr int q_chunk_off(int nkc, int cc) {
 }
 static_assert(9 * kQChunk <= 2 * s_stage_bytes(9) && 8 * kQChunk <= 2 * s_stage_bytes(8),
               "queries fit stages 1-2");
-// S-CTA: above its stages, 1 KB per softmax warp to regroup P rows (8 rows of
+// S-CTA: above its stages, 2 KB per sender warp to regroup P rows (16 rows of
 // 128 B) so that each store to the O-CTA writes 512 contiguous bytes
 __host__ __device__ constexpr int p_regroup_off(int nkc) { return kNS * s_stage_bytes(nkc); }
-static_assert(p_regroup_off(9) + 8 * 1024 <= kCtrlOff, "S-CTA stages and P regrouping below the control block");
-constexpr int kThreads = 416;                 // see the role map in the kernel
+constexpr int kCtrlOff = p_regroup_off(9) + 8 * 1024;  // both CTAs: the control block
+static_assert(kSideOff + kNP * kPSlot <= kCtrlOff, "O-CTA V stages and P slots below the control block");
+constexpr int kThreads = 448;                 // see the role map in the kernel
 constexpr int kSmxWarps = 8;                  // S-CTA softmax warps: two threads per query row
+constexpr int kSenders = 4;                   // S-CTA P senders: one per TMEM lane quadrant
 constexpr uint64_t kWaitLimit = 2000000000ull;  // ns before a wait gives up (default)
 constexpr uint32_t kSuspendHintNs = 1000;     // longest suspension of one wait poll
 constexpr float kRescaleThreshold = 8.0f;     // lazy rescale, log2 units
@@ -92,23 +98,24 @@ constexpr int kPrefetchAhead = 6;             // tiles the L2 prefetcher runs ah
 // per-tile rescale message from the S-CTA's softmax to the O-CTA (st.async)
 struct __align__(16) AlphaMsg {
     float alpha[128];           // per-row rescale factors of the P slot
-    int32_t flags[kSmxWarps];   // per softmax warp, some row needs a rescale
+    int32_t flags[kSenders];    // per sender warp (32 rows), some row needs a rescale
 };
 
 struct Ctrl {
-    AlphaMsg amsg[2];       // O: the messages of the two P slots
     uint64_t full[kNS];     // both: this CTA's part of the tile landed (complete_tx)
-    uint64_t pdone[2];      // O: the P*V reading P slot i finished (MMA commit); the
+    uint64_t pdone[kNP];    // O: the P*V reading P slot k finished (MMA commit); the
                             //    relay warp passes it on to the S-CTA's pempty
     uint64_t empty[kNS];    // both: stage free (own QK / P*V commit)
     uint64_t sfull[2];      // S: scores ready (QK commit)
     uint64_t sfree[2];      // S: scores read (the 256 softmax threads)
-    uint64_t pempty[2];     // S: P slot consumed (the O-CTA's relay, 1 remote arrival)
+    uint64_t pempty[kNP];   // S: O-CTA P slot k consumed (its relay, 1 remote arrival)
+    uint64_t pstaged[2];    // S: P + alpha of a tile in its TMEM slot (256 softmax threads)
+    uint64_t pfree[2];      // S: that TMEM slot read by the senders (128 threads)
     uint64_t qready;        // S: Q stored in TMEM (256 softmax threads)
     uint64_t qland;         // S: first segment's queries landed in shared memory (TMA)
     uint64_t qfree;         // S: those queries are in TMEM; stages 1-2 reusable (256)
     uint64_t statack;       // S: O-CTA has read the segment statistics (1 remote)
-    uint64_t pfull[2];      // O: P + alpha written (1 remote arrival per tile)
+    uint64_t pfull[kNP];    // O: P slot k written: P, alpha, flags (st.async bytes)
     uint64_t vready[kNS];   // O: tile tail zeroed (fix warp)
     uint64_t odone;         // O: all issued P*V complete (MMA commit)
     uint64_t evt;           // O: MMA warp -> row warps event
@@ -318,11 +325,14 @@ __device__ __forceinline__ int valid_blocks(const Walk& w) {
 }
 
 // ------------------------------------------------------------------ kernel
-// Role map (13 warps per CTA):
-//   S-CTA  warps 0-3  K loaders: warp k loads block k of each tile (3-D boxes)
+// Role map (14 warps per CTA):
+//   S-CTA  warps 0-3  P senders: warp q reads the staged P rows of TMEM lanes
+//                     32q..32q+31 and writes them (and their rescale factors)
+//                     into the O-CTA's P slot by st.async
 //          warp 4     S = Q K^T MMA issuer; owns the TMEM allocation
 //          warps 5-12 softmax, two threads per query row (32 score columns
-//                     each); P goes to the O-CTA by st.async
+//                     each); P and alpha go to a TMEM slot
+//          warp 13    K loader: one 5-D box per cache block of each tile
 //   O-CTA  warp 0     V loader: one 4-D box per cache block
 //          warp 1     V landing: zeroes the rows of a partial last block past
 //                     the request, releases the stage
@@ -332,6 +342,7 @@ __device__ __forceinline__ int valid_blocks(const Walk& w) {
 //                     its quadrant (w % 4) and half the 512 columns
 //          warp 3     relay: passes each P*V completion (its own barrier) on to
 //                     the S-CTA's P-slot barrier by a remote mbarrier arrive
+//          warp 13    idle
 // In both CTAs warp 2 first works out the pair's unit range (walk_init) while
 // the barriers and TMEM are set up; every warp then follows that walk.
 template <int W, bool kF16>
@@ -354,16 +365,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     if (tid == 0) {
         for (int s = 0; s < kNS; ++s) {
-            mbar_init(smem_u32(&c.full[s]), rank == 0 ? 4 : 1);  // S: one per K loader
+            mbar_init(smem_u32(&c.full[s]), 1);
             mbar_init(smem_u32(&c.empty[s]), 1);
             mbar_init(smem_u32(&c.vready[s]), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&c.sfull[i]), 1);
             mbar_init(smem_u32(&c.sfree[i]), kSmxWarps * 32);
-            mbar_init(smem_u32(&c.pempty[i]), 1);
-            mbar_init(smem_u32(&c.pfull[i]), 1);
-            mbar_init(smem_u32(&c.pdone[i]), 1);
+            mbar_init(smem_u32(&c.pstaged[i]), kSmxWarps * 32);
+            mbar_init(smem_u32(&c.pfree[i]), kSenders * 32);
+        }
+        for (int k = 0; k < kNP; ++k) {
+            mbar_init(smem_u32(&c.pempty[k]), 1);
+            mbar_init(smem_u32(&c.pfull[k]), 1);
+            mbar_init(smem_u32(&c.pdone[k]), 1);
         }
         mbar_init(smem_u32(&c.qready), 256);
         mbar_init(smem_u32(&c.qland), 1);
@@ -386,7 +401,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (rank == 1 && warp != 2) {
         // O-CTA: clear the V stages once, so a block past a request's end that
         // the P*V MMA reads (under P = 0) never holds a NaN
-        for (int i = tid - (warp > 2 ? 32 : 0); i < kNS * kStage / 16; i += kThreads - 32)
+        for (int i = tid - (warp > 2 ? 32 : 0); i < kNV * kStage / 16; i += kThreads - 32)
             reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
     }
@@ -435,18 +450,82 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // =============================== S-CTA ===============================
         const uint32_t tq = tbase;              // Q: columns [0, W/2)
         const uint32_t ts0 = tbase + W / 2;     // S buffers: 2 x 64 columns
+        const uint32_t tp0 = ts0 + 2 * kTok;    // P slots: 2 x 32 columns (bf16 pairs)
+        const uint32_t ta0 = tp0 + 64;          // alpha: 2 x 2 columns
+        static_assert(W / 2 + 2 * kTok + 64 + 4 <= 512, "S-CTA TMEM columns");
         if (warp < 4) {
-            // ---------------- K loaders: warp k brings block k of every tile
-            const int kb = warp;
+            // ---------------- P senders: warp q ships the P rows of TMEM lanes
+            // 32q..32q+31 and their rescale factors to the O-CTA's P slot
+            const int q = warp;
+            const uint32_t lane_q = (uint32_t)(q * 32) << 16;
+            const int row = q * 32 + lane;
+            const uint32_t pslot_remote = mapa(smem_u32(smem + kSideOff), 1);
+            const uint32_t pfull_remote = mapa(smem_u32(&c.pfull[0]), 1);
+            const uint32_t regroup = smem_u32(smem + p_regroup_off(NKC)) + (uint32_t)q * 2048;
+            long long i = 0;
+            for (; w.u < w.u_end; walk_next(p, w), ++i) {
+                const int buf = (int)(i & 1);
+                if (!wt.wait_warp(smem_u32(&c.pstaged[buf]), (uint32_t)((i >> 1) & 1))) break;
+                tc_fence_after();
+                uint32_t v[32], av;
+                tmem_ld32(tp0 + buf * 32 + lane_q, v);  // this row's 32 bf16 pairs
+                tmem_ld1(ta0 + buf * 2 + lane_q, av);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(smem_u32(&c.pfree[buf]));
+                // the O-CTA's P slot free? (its P*V kNP tiles back)
+                const int slot = (int)(i % kNP);
+                if (!wt.wait_warp(smem_u32(&c.pempty[slot]), (uint32_t)((i / kNP) & 1) ^ 1)) break;
+                const uint32_t pbar = pfull_remote + slot * 8;
+                const uint32_t dst = pslot_remote + slot * kPSlot;
+                const int grows = min(128, Mq - w.g * 128);
+                // The rows go out 16 at a time: the 16 threads holding them write
+                // them into the warp's 2 KB in the P slot's swizzled layout, then
+                // every lane ships four 16-byte pieces, so that each store covers 4
+                // whole rows (512 contiguous bytes). Rows past the group are never
+                // read back and are not sent.
+#pragma unroll
+                for (int a = 0; a < 2; ++a) {
+                    if ((lane >> 4) == a) {
+                        const int rr = lane & 15;  // row 32q + 16a + rr: its swizzle phase is rr & 7
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            st_shared_v4(regroup + rr * 128 + ((u ^ (rr & 7)) << 4), v[4 * u], v[4 * u + 1],
+                                         v[4 * u + 2], v[4 * u + 3]);
+                    }
+                    __syncwarp();
+                    uint4 d[4];
+#pragma unroll
+                    for (int h2 = 0; h2 < 4; ++h2)
+                        d[h2] = ld_shared_v4(regroup + (4 * h2 + (lane >> 3)) * 128 + ((lane & 7) << 4));
+#pragma unroll
+                    for (int h2 = 0; h2 < 4; ++h2) {
+                        const int r = q * 32 + 16 * a + 4 * h2 + (lane >> 3);
+                        if (r < grows)
+                            st_async_v4(dst + r * 128 + ((lane & 7) << 4), d[h2].x, d[h2].y, d[h2].z, d[h2].w,
+                                        pbar);
+                    }
+                    __syncwarp();  // the next round overwrites the warp's 2 KB
+                }
+                // alpha is 1 on a segment's first tile (no running max yet), so a
+                // factor other than 1 is a rescale of the rows' earlier P*V
+                if (row < grows) st_async_b32(dst + kPBytes + row * 4, av, pbar);
+                const unsigned any = __ballot_sync(0xffffffffu, row < grows && __uint_as_float(av) != 1.f);
+                if (lane == 0)
+                    st_async_b32(dst + kPBytes + (uint32_t)offsetof(AlphaMsg, flags) + q * 4, any ? 1u : 0u,
+                                 pbar);
+            }
+        } else if (warp == 13) {
+            // ---------------- K loader: the tile's cache blocks, one box each
             if (elect_one()) {
-                if (kb == 0) {
-                    tma_prefetch_desc(&tmap);
-                    tma_prefetch_desc(&qmap);
-                    // the first segment's queries: TMA into stages 1 and 2 (free until
-                    // the rows move them to TMEM), while tile 0 goes to stage 0.
-                    // They come from the previous kernel (programmatic launch).
-                    // (a request's rows past t_q * n_head are outside the map)
-                    grid_dependency_wait();
+                tma_prefetch_desc(&tmap);
+                tma_prefetch_desc(&qmap);
+                // the first segment's queries: TMA into stages 1 and 2 (free until
+                // the rows move them to TMEM), while tile 0 goes to stage 0.
+                // They come from the previous kernel (programmatic launch).
+                // (a request's rows past t_q * n_head are outside the map)
+                grid_dependency_wait();
+                {
                     const int qrows = Mq < 128 ? Mq : 128;
                     mbar_arrive_expect_tx(smem_u32(&c.qland), (uint32_t)(NKC * qrows * 128));
                     for (int cc = 0; cc < NKC; ++cc)
@@ -461,29 +540,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (!wt.wait(smem_u32(&c.empty[s]), (uint32_t)((i / kNS) & 1) ^ 1)) break;
                     if (i == 1 || i == 2)  // first use of a stage that held the queries
                         if (!wt.wait(smem_u32(&c.qfree), 0)) break;
-                    if (kb == 0 && i > 0 && w.tile == 0) {
+                    if (i > 0 && w.tile == 0) {
                         // a later segment: warm L2 with its queries for the row threads
                         const int rows = min(128, Mq - w.g * 128);
                         prefetch_l2_bulk(p.q_abs + ((long long)w.b * Mq + w.g * 128) * W,
                                          (uint32_t)(rows * W * 2));
                     }
-                    const bool have = kb < valid_blocks(w);
-                    mbar_arrive_expect_tx(smem_u32(&c.full[s]), have ? (uint32_t)(NKC * 2048) : 0u);
+                    const int nb = valid_blocks(w);
+                    const int32_t* bt = p.block_table + (long long)w.b * p.max_blocks + w.tile * 4;
+                    int32_t blk[4];
+#pragma unroll
+                    for (int kb = 0; kb < 4; ++kb) blk[kb] = kb < nb ? bt[kb] : 0;
+                    mbar_arrive_expect_tx(smem_u32(&c.full[s]), (uint32_t)(nb * NKC * 2048));
                     last_issue[s] = i;
-                    if (have) {
-                        int32_t blk = p.block_table[(long long)w.b * p.max_blocks + w.tile * 4 + kb];
-                        if (blk < 0 || blk >= p.num_blocks) {
+#pragma unroll
+                    for (int kb = 0; kb < 4; ++kb) {
+                        if (kb >= nb) break;
+                        int32_t b = blk[kb];
+                        if (b < 0 || b >= p.num_blocks) {
                             // load a valid stand-in; the row threads void the segment
                             if (p.dev_err) atomicOr(p.dev_err, (int32_t)MLA_DEVERR_BAD_BLOCK);
-                            blk = 0;
+                            b = 0;
                         }
                         // the whole block (all NKC chunks, both 8-row halves) in one box
-                        tma_load_5d(smem_u32(smem + s * s_stage_bytes(NKC) + kb * NKC * 2048),
-                                    &tmap, smem_u32(&c.full[s]), 0, 0, 0, 0, blk);
+                        tma_load_5d(smem_u32(smem + s * s_stage_bytes(NKC) + kb * NKC * 2048), &tmap,
+                                    smem_u32(&c.full[s]), 0, 0, 0, 0, b);
                     }
                 }
                 // drain: the copies issued into each stage must have landed
-                if (kb == 0) mbar_wait(smem_u32(&c.qland), 0, p.wait_ns);
+                mbar_wait(smem_u32(&c.qland), 0, p.wait_ns);
                 for (int s = 0; s < kNS; ++s)
                     if (last_issue[s] >= 0)
                         mbar_wait(smem_u32(&c.full[s]), (uint32_t)((last_issue[s] / kNS) & 1),
@@ -523,12 +608,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     mma_commit(smem_u32(&c.empty[s]));
                 }
             }
-        } else if (warp >= 5) {
+        } else if (warp >= 5 && warp <= 12) {
             // ---------------- softmax (warps 5..12): warp w reads the 16 TMEM lanes
             // 32 (w % 4) + 16 h (h = 0 for warps 5..8, 1 for 9..12) with the 16x64b
             // shape; the two threads of a query row hold its even and odd score
-            // columns, share the row max by one shuffle and swap halves so each
-            // packs 32 adjacent columns of P
+            // columns, share the row max by one shuffle and trade columns so each
+            // holds the bf16 pairs it stores back in the same layout
             const int q = warp & 3;
             const int h = warp >= 9 ? 1 : 0;
             const int sw = warp - 5;                                  // 0..7
@@ -537,14 +622,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t lane_base16 = (uint32_t)(q * 32 + h * 16) << 16;
             const uint32_t lane_off = (uint32_t)(q * 32) << 16;      // Q moves
             const int rq = q * 32 + lane;                             // their row
-            const uint32_t pslot_remote = mapa(smem_u32(smem + kSideOff), 1);
-            const uint32_t pfull_remote = mapa(smem_u32(&c.pfull[0]), 1);
-            const uint32_t amsg_remote = mapa(smem_u32(&c.amsg[0]), 1);
             const uint32_t mstat_remote = mapa(smem_u32(&c.mstat[0]), 1);
             const uint32_t lstat_remote = mapa(smem_u32(&c.lstat[0]), 1);
             const uint32_t bad_remote = mapa(smem_u32(&c.bad), 1);
             const uint32_t statfull_remote = mapa(smem_u32(&c.statfull), 1);
-            const uint32_t regroup = smem_u32(smem + p_regroup_off(NKC)) + (uint32_t)sw * 1024;
             const float sl2 = p.scale_log2;
             grid_dependency_wait();  // later segments read their queries from global memory
             long long i = 0;
@@ -682,55 +763,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     add2(ps0, ps1, x[j], x[j + 1]);
                 }
                 l = l * alpha + (ps0 + ps1);  // this thread's columns; the pair adds at the end
-                // swap halves: the even thread keeps columns 0..31, the odd one 32..63
+                // P into the TMEM slot, in the 16x64b layout the scores came in:
+                // register k of thread `par` is bf16 pair 2k + par of its row (pair
+                // c = columns 2c, 2c + 1), so the two threads trade one value per pair
                 uint32_t pk[16];
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
-                    const float mine_lo = x[k], mine_hi = x[16 + k];
-                    const float got = __shfl_xor_sync(0xffffffffu, par ? mine_lo : mine_hi, 2);
-                    pk[k] = par ? pack2<kF16>(got, mine_hi) : pack2<kF16>(mine_lo, got);
+                    const float got = __shfl_xor_sync(0xffffffffu, par ? x[2 * k] : x[2 * k + 1], 2);
+                    pk[k] = par ? pack2<kF16>(got, x[2 * k + 1]) : pack2<kF16>(x[2 * k], got);
                 }
-                const int need = (!first_tile && alpha != 1.f) ? 1 : 0;
-                const unsigned any = __ballot_sync(0xffffffffu, need);
-                // P slot free? (the O-CTA's P*V two tiles back)
-                if (!wt.wait_warp(smem_u32(&c.pempty[buf]), (uint32_t)((i >> 1) & 1) ^ 1)) break;
-                const uint32_t pbar = pfull_remote + buf * 8;
-                // The warp's 16 rows go out 8 at a time: the threads of those rows
-                // write their 16-byte pieces into the warp's 1 KB in the P slot's
-                // swizzled layout, then every lane ships two contiguous pieces, so
-                // each store to the O-CTA covers 4 whole rows (512 bytes). Rows past
-                // the group are never read back and are not sent.
-                {
-                    const int grows = min(128, Mq - w.g * 128);
-                    const int rbase = q * 32 + h * 16;  // the warp's first row
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        if ((lane & 1) == half) {
-                            const int a = lane >> 2;  // this thread's row, rbase + a + 8 half
-#pragma unroll
-                            for (int u = 0; u < 4; ++u)
-                                st_shared_v4(regroup + a * 128 + (((4 * par + u) ^ a) << 4), pk[4 * u],
-                                             pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-                        }
-                        __syncwarp();
-#pragma unroll
-                        for (int v = 0; v < 2; ++v) {
-                            const int a = 4 * v + (lane >> 3);
-                            const int row = rbase + 8 * half + a;
-                            const uint4 d = ld_shared_v4(regroup + a * 128 + ((lane & 7) << 4));
-                            if (row < grows)
-                                st_async_v4(pslot_remote + buf * kPBytes + row * 128 + ((lane & 7) << 4),
-                                            d.x, d.y, d.z, d.w, pbar);
-                        }
-                        __syncwarp();  // the next half overwrites the warp's 1 KB
-                    }
-                }
-                if (row_ok && par == 0)
-                    st_async_b32(amsg_remote + buf * (uint32_t)sizeof(AlphaMsg) + R * 4,
-                                 __float_as_uint(alpha), pbar);
-                if (lane == 0)
-                    st_async_b32(amsg_remote + buf * (uint32_t)sizeof(AlphaMsg) + 512 + sw * 4,
-                                 any ? 1u : 0u, pbar);
+                // the slot free? (its senders have read tile i - 2)
+                if (!wt.wait_warp(smem_u32(&c.pfree[buf]), (uint32_t)((i >> 1) & 1) ^ 1)) break;
+                tc_fence_after();
+                tmem_st16x64_x16(tp0 + buf * 32 + lane_base16, pk);
+                tmem_st16x64_x1(ta0 + buf * 2 + lane_base16, __float_as_uint(alpha));  // both columns
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(smem_u32(&c.pstaged[buf]));
                 if (seg_last(w)) {
                     const float l_row = l + __shfl_xor_sync(0xffffffffu, l, 2);
                     if (!rows_sync(wt, smem_u32(&c.rowbar), rphase)) break;
@@ -759,11 +808,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (elect_one()) {
                 tma_prefetch_desc(&vmap);
                 long long i = 0;
-                long long last_issue[kNS];
-                for (int s = 0; s < kNS; ++s) last_issue[s] = -1;
+                long long last_issue[kNV];
+                for (int s = 0; s < kNV; ++s) last_issue[s] = -1;
                 for (; w.u < w.u_end; walk_next(p, w), ++i) {
-                    const int s = (int)(i % kNS);
-                    if (!wt.wait(smem_u32(&c.empty[s]), (uint32_t)((i / kNS) & 1) ^ 1)) break;
+                    const int s = (int)(i % kNV);
+                    if (!wt.wait(smem_u32(&c.empty[s]), (uint32_t)((i / kNV) & 1) ^ 1)) break;
                     const int nb = valid_blocks(w);
                     const int32_t* bt = p.block_table + (long long)w.b * p.max_blocks + w.tile * 4;
                     mbar_arrive_expect_tx(smem_u32(&c.full[s]), (uint32_t)(nb * kVBlock));
@@ -775,9 +824,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                     smem_u32(&c.full[s]), 0, 0, 0, blk);
                     }
                 }
-                for (int s = 0; s < kNS; ++s)
+                for (int s = 0; s < kNV; ++s)
                     if (last_issue[s] >= 0)
-                        mbar_wait(smem_u32(&c.full[s]), (uint32_t)((last_issue[s] / kNS) & 1),
+                        mbar_wait(smem_u32(&c.full[s]), (uint32_t)((last_issue[s] / kNV) & 1),
                                   p.wait_ns);
             }
         } else if (warp == 1) {
@@ -788,8 +837,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // an earlier tile, all finite.
             long long i = 0;
             for (; w.u < w.u_end; walk_next(p, w), ++i) {
-                const int s = (int)(i % kNS);
-                if (!wt.wait_warp(smem_u32(&c.full[s]), (uint32_t)((i / kNS) & 1))) break;
+                const int s = (int)(i % kNV);
+                if (!wt.wait_warp(smem_u32(&c.full[s]), (uint32_t)((i / kNV) & 1))) break;
                 const int nvalid = min(kTok, w.S - w.tile * kTok);
                 const int r0 = nvalid & 15;  // first row past the request in its block
                 if (r0 != 0) {
@@ -810,15 +859,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
             }
         } else if (warp == 3) {
-            // ---------------- relay: once the P*V that read P slot i & 1 has
+            // ---------------- relay: once the P*V that read P slot i % kNP has
             // finished (this CTA's pdone), the S-CTA may refill the slot: one
             // remote arrival on its pempty per tile
             if (elect_one()) {
                 const uint32_t pempty_remote = mapa(smem_u32(&c.pempty[0]), 0);
                 long long i = 0;
                 for (; w.u < w.u_end; walk_next(p, w), ++i) {
-                    const int slot = (int)(i & 1);
-                    if (!wt.wait(smem_u32(&c.pdone[slot]), (uint32_t)((i >> 1) & 1))) break;
+                    const int slot = (int)(i % kNP);
+                    if (!wt.wait(smem_u32(&c.pdone[slot]), (uint32_t)((i / kNP) & 1))) break;
                     mbar_arrive_remote(pempty_remote + slot * 8);
                 }
             }
@@ -851,21 +900,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 long long i = 0;
                 int nevt = 0, ndone = 0;
                 for (; w.u < w.u_end; walk_next(p, w), ++i) {
-                    const int s = (int)(i % kNS);
-                    const int slot = (int)(i & 1);
+                    const int s = (int)(i % kNV);
+                    const int slot = (int)(i % kNP);
                     // this tile's P rows, rescale factors and flags arrive by st.async
                     {
                         const int grows = min(128, Mq - w.g * 128);
                         mbar_arrive_expect_tx(smem_u32(&c.pfull[slot]),
-                                              (uint32_t)(grows * (128 + 4) + kSmxWarps * 4));
+                                              (uint32_t)(grows * (128 + 4) + kSenders * 4));
                     }
-                    if (!wt.wait(smem_u32(&c.vready[s]), (uint32_t)((i / kNS) & 1))) break;
-                    if (!wt.wait(smem_u32(&c.pfull[slot]), (uint32_t)((i >> 1) & 1))) break;
+                    if (!wt.wait(smem_u32(&c.vready[s]), (uint32_t)((i / kNV) & 1))) break;
+                    if (!wt.wait(smem_u32(&c.pfull[slot]), (uint32_t)((i / kNP) & 1))) break;
                     const bool first = seg_first(w, ub);
-                    const volatile int32_t* fl = c.amsg[slot].flags;
+                    const volatile int32_t* fl =
+                        reinterpret_cast<const AlphaMsg*>(smem + kSideOff + slot * kPSlot + kPBytes)->flags;
                     int any_flag = 0;
 #pragma unroll
-                    for (int k = 0; k < kSmxWarps; ++k) any_flag |= fl[k];
+                    for (int k = 0; k < kSenders; ++k) any_flag |= fl[k];
                     if (!first && any_flag) {
                         // rows whose max moved: rescale O once the issued P*V is done
                         mma_commit(smem_u32(&c.odone));
@@ -879,7 +929,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     fence_proxy_async_smem();
                     tc_fence_after();
-                    const uint32_t pa = smem_u32(smem + kSideOff + slot * kPBytes);
+                    const uint32_t pa = smem_u32(smem + kSideOff + slot * kPSlot);
                     const uint32_t va = smem_u32(smem + s * kStage);
                     // V: K-step kk is cache block kk of the tile; its latent columns
                     // sit in 8 chunks of [16 rows][128 B] at a 2 KB stride. A block
@@ -910,7 +960,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-        } else if (warp >= 5) {
+        } else if (warp >= 5 && warp <= 12) {
             // ---------------- row warps: rescale and epilogue. Warps 5..8 take
             // columns 0..255 of their 32 rows, warps 9..12 columns 256..511.
             const int q = warp & 3;
@@ -932,7 +982,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const int type = *(volatile int32_t*)&c.evt_type;
                 if (type == 1) {
                     const int slot = *(volatile int32_t*)&c.evt_slot;
-                    const float a = c.amsg[slot].alpha[r];
+                    const float a =
+                        reinterpret_cast<const AlphaMsg*>(smem + kSideOff + slot * kPSlot + kPBytes)->alpha[r];
                     if (a != 1.f) {
 #pragma unroll 1
                         for (int cc = c_lo; cc < c_lo + 256; cc += 32) {
