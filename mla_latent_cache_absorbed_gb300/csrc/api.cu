@@ -289,18 +289,15 @@ mla_status check_decode_shape(int32_t batch, int32_t max_blocks, const mla_dims&
     return MLA_OK;
 }
 
-// The bf16 tensor-core decode gives each row group of a request (128 of its
-// t_q * n_head query rows) a set of CTA pairs of its own, so it serves a
-// geometry only while the row groups number no more than the pairs of its
-// grid on this device (76 pairs on 152 SMs: up to 9728 query rows per
-// request). Larger query blocks, such as long prefill chunks, take the SIMT
-// decode.
+// The 16-bit types take the tensor-core decode. It gives each row group of a
+// request (128 of its t_q * n_head query rows) a set of CTA pairs of its own;
+// with more row groups than the grid has pairs (more than 9728 query rows per
+// request on 152 SMs, a long prefill chunk), each row group gets one pair and
+// a pair walks several row groups in turn.
 bool use_tc_decode(const mla_dims& d) {
     if (d.dtype == MLA_F32 || !tc_decode_supported(d)) return false;
     size_t bytes = 0;
-    if (tc_decode_workspace(1, 1, d, &bytes) != cudaSuccess) return false;
-    const long long pairs = (long long)(bytes / kTcDecodeBytesPerPair);
-    return ((long long)d.t_q * d.n_head + 127) / 128 <= pairs;
+    return tc_decode_workspace(1, 1, d, &bytes) == cudaSuccess;
 }
 }  // namespace
 

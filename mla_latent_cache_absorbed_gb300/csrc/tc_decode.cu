@@ -132,8 +132,9 @@ struct Ctrl {
     int32_t landed;         // O: tiles whose V has landed (paces the L2 prefetcher)
     float mstat[128];       // O: segment max (log2 units) per row
     float lstat[128];       // O: segment sum per row
-    long long walk_u, walk_ue;  // both: the pair's unit range (see walk_init)
+    long long walk_u, walk_ue, walk_pe;  // both: the pair's unit range (see walk_init)
     int32_t walk_b, walk_g, walk_tile, walk_S, walk_nt, walk_ok;  // and its first unit
+    int32_t walk_U, walk_b0, walk_S0, walk_nt0;                  // and its passes
 };
 constexpr int kSmemBytes = kCtrlOff + (int)sizeof(Ctrl);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -168,6 +169,10 @@ static_assert(kTok == split::kTok, "unit size");
 struct Walk {
     int b, g, tile, ntiles, S;
     long long u, u_end;
+    // more row groups than pairs: pair k walks sets k, k + NP, ... one after
+    // the other, U units each; pass_end is where the current set's units end
+    long long pass_end;
+    int U, b0, S0, nt0;
 };
 
 // This pair's set and unit range; warp-cooperative, at most two passes over
@@ -242,6 +247,18 @@ __device__ bool walk_init(const Params& p, int pair, Walk& w) {
     w.tile = ub - first;
     w.u = ub;
     w.u_end = ue;
+    w.pass_end = ue;
+    w.U = U;
+    w.b0 = fb;
+    w.S0 = S;
+    w.nt0 = w.ntiles;
+    if (G > p.NP) {
+        // one pair per set (np_g = 1: the pair's range is the whole set, from
+        // the first request with tiles), and this pair also takes sets
+        // pair + NP, pair + 2 NP, ...
+        const int npass = (G - 1 - pair) / p.NP + 1;
+        w.u_end = (long long)npass * U;
+    }
     return true;
 }
 
@@ -249,6 +266,16 @@ __device__ bool walk_init(const Params& p, int pair, Walk& w) {
 __device__ __forceinline__ void walk_next(const Params& p, Walk& w) {
     ++w.u;
     if (w.u >= w.u_end) return;
+    if (w.u == w.pass_end) {
+        // the pair's next row group: the same requests and tiles again
+        w.pass_end += w.U;
+        w.g += p.NP;
+        w.b = w.b0;
+        w.S = w.S0;
+        w.ntiles = w.nt0;
+        w.tile = 0;
+        return;
+    }
     if (++w.tile < w.ntiles) return;
     w.tile = 0;
     do {
@@ -421,6 +448,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 c.walk_tile = w0.tile;
                 c.walk_S = w0.S;
                 c.walk_nt = w0.ntiles;
+                c.walk_pe = w0.pass_end;
+                c.walk_U = w0.U;
+                c.walk_b0 = w0.b0;
+                c.walk_S0 = w0.S0;
+                c.walk_nt0 = w0.nt0;
             }
         }
     }
@@ -442,6 +474,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         w.ntiles = c.walk_nt;
         w.u = c.walk_u;
         w.u_end = c.walk_ue;
+        w.pass_end = c.walk_pe;
+        w.U = c.walk_U;
+        w.b0 = c.walk_b0;
+        w.S0 = c.walk_S0;
+        w.nt0 = c.walk_nt0;
     }
     const long long ub = has_work ? w.u : 0;
     const int Mq = p.T * p.H;

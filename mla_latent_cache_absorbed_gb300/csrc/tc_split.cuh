@@ -45,6 +45,7 @@ __device__ __forceinline__ int ntiles_of(int S, int T, int max_blocks) {
 template <class P>
 __device__ __forceinline__ int pairs_per_set(const P& p, int G, long long U) {
     int np_g = p.NP / G;
+    if (np_g < 1) np_g = 1;  // more row groups than pairs: one pair per set, pairs walk several sets
     const long long cap = (U + p.min_units - 1) / p.min_units;
     if (cap < np_g) np_g = (int)(cap > 0 ? cap : 1);
     return np_g;

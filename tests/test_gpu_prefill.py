@@ -4,10 +4,11 @@ The queries of a chunk are the request's last t_q positions and query t sees
 keys 0 .. seq_len - t_q + t; a first chunk has t_q == seq_len (query t sees
 keys 0 .. t). The decode entry points take such blocks as they are: on the
 tensor-core path the t_q * n_head query rows of a request form row groups of
-128 and each row group gets a set of CTA pairs of its own; a request with more
-row groups than the grid has pairs (more than 9728 query rows on 152 SMs)
-takes the SIMT decode. Parity is against the oracle on the same bf16 values,
-with the tolerances of test_gpu_parity.py.
+128 and each row group gets a set of CTA pairs of its own; with more row
+groups than the grid has pairs (more than 9728 query rows on 152 SMs) each
+row group gets one pair and a pair walks several row groups in turn. Parity
+is against the oracle on the same bf16 values, with the tolerances of
+test_gpu_parity.py.
 """
 import numpy as np
 import pytest
@@ -91,6 +92,13 @@ CHUNKS = [
     ("deepseek_decode", 32, [32, 200]),
     # NoPE rows (512 wide), 16 queries
     ("glm53_flash_nope", 16, [16, 300, 0]),
+    # more row groups than the 76 pairs of 152 SMs: 80 row groups a request,
+    # pairs 0-3 walk two of them (a first chunk and a later one)
+    ("glm52_decode", 160, [160, 300]),
+    # 160 row groups: pairs 0-7 walk three
+    ("glm52_decode", 320, [320]),
+    # DeepSeek geometry, 80 queries of 128 heads: 80 row groups
+    ("deepseek_decode", 80, [80, 129]),
 ]
 
 
@@ -102,8 +110,8 @@ def test_chunk_all_rows(name, t_q, lens):
 
 def test_chunk_beyond_row_group_limit_sampled():
     """160 queries of 64 heads are 80 row groups, more than the 76 pairs of
-    the tensor-core grid on 152 SMs: the decode takes the SIMT kernels and
-    must still match the oracle."""
+    the tensor-core grid on 152 SMs: pairs 0-3 walk two row groups each. A
+    longer request than the all-rows case, on sampled rows."""
     wl = chunk_workload("glm52_decode", 160, [160, 500])
     sampled_stages(wl, parity.sample_rows(wl, 24, 5))
 
