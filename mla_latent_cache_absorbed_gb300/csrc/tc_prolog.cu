@@ -25,6 +25,11 @@
 // f32 and stored as the rope tail of q_abs.
 // GEMM 2: D2 [128 x 512] = q^C . W^UK[h] in all 512 TMEM columns (D1 is read
 // out by then); epilogue 2 stores it as the latent part of q_abs.
+// While heads and row tiles leave half the SMs idle, a head is split over a
+// CTA pair (a cluster of 2): GEMM 1's 64-column blocks (W^UQ's, then W^QR's)
+// go half to each CTA, all rope columns to CTA 1; each CTA writes its q^C
+// columns into both CTAs' GEMM 2 operand (st.async into the partner's), and
+// computes one 256-column half of the latent part.
 //
 // A SIMT kernel serves f32 and the geometries the tensor-core kernel does not
 // (one CTA per (head, query row)), rounding at the same points.
@@ -75,6 +80,8 @@ struct PrologParams {
     int a_rows;                 // rows of the c_q box: the tile's rows, rounded up to 8
     int ns, stage, areg;        // ring stages, bytes per stage, bytes of its A part
     int a2, a2s, bar, gam;      // offsets of q^C, its chunk stride, barriers, gamma
+    int split;                  // a head split over a CTA pair (cluster of 2)
+    int ab1;                    // split: the first of GEMM 1's 64-column blocks CTA 1 takes
     float eps, theta_scale;
     int32_t* dev_err;
 };
@@ -104,11 +111,20 @@ __global__ void __launch_bounds__(kPThreads, 1)
     uint64_t* ssfree = ssfull + kPMaxStages;  // first sweep: chunk read (row threads, 128)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(ssfree + kPMaxStages);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.x;
+    const uint32_t crank = p.split ? cluster_ctarank() : 0u;
+    const int h = p.split ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
     const int m0 = blockIdx.y * 128;
-    const int N1 = p.Dn + p.P;           // GEMM 1 output columns
+    const int nuq = p.Dn / 64;           // GEMM 1's 64-column blocks of W^UQ; W^QR's follow
+    const int nat = (p.Dn + p.P) / 64;
+    const int ab = crank == 0 ? 0 : p.ab1;                    // this CTA's blocks [ab, ae)
+    const int ae = (p.split && crank == 0) ? p.ab1 : nat;
+    const int N1 = 64 * (ae - ab);       // GEMM 1 output columns of this CTA
+    const int qc0 = 64 * ab, qc1 = 64 * min(ae, nuq);          // its q^C columns
+    const bool rope_here = p.P > 0 && ae == nat;
     const int nk1 = p.q_rank / 64;       // GEMM 1 K chunks
-    const int nk2 = p.Dn / 64;           // GEMM 2 K chunks (each in two 256-column halves)
+    const int nk2 = p.Dn / 64;           // GEMM 2 K chunks
+    const int nhalf = p.split ? 1 : 2;   // GEMM 2's 256-column halves of this CTA
+    const int half0 = p.split ? (int)crank : 0;
     if (tid == 0) {
         for (int s = 0; s < ns; ++s) {
             mbar_init(smem_u32(&fullA[s]), 128);
@@ -116,7 +132,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
             mbar_init(smem_u32(&empty[s]), 1);
         }
         mbar_init(smem_u32(d1done), 1);
-        mbar_init(smem_u32(a2ready), 128);
+        // the row threads' q^C writes, and on a split the partner's (bytes)
+        mbar_init(smem_u32(a2ready), p.split ? 129 : 128);
         mbar_init(smem_u32(d2done), 1);
         for (int s = 0; s < ns; ++s) {
             mbar_init(smem_u32(&ssfull[s]), 1);
@@ -129,10 +146,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();  // (a CTA alone is a cluster of one) the partner's barriers are set up
     tc_fence_after();
     const uint32_t tbase = *tslot;
     bool ok = true;
+    if (p.split && tid == 0) {
+        // the partner's q^C columns, a_rows rows of them
+        const int pab = crank == 0 ? p.ab1 : 0, pae = crank == 0 ? nat : p.ab1;
+        const int pcols = 64 * (min(pae, nuq) - min(pab, nuq));
+        mbar_arrive_expect_tx(smem_u32(a2ready), (uint32_t)(p.a_rows * pcols * 2));
+    }
 
     if (warp == 0) {
         // ---------------- weights: GEMM 1 chunks, then GEMM 2 chunks, one ring
@@ -158,7 +181,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 const int jl = s + ((nk1 - 1 - s) / ns) * ns;  // last chunk in stage s
                 if (!mbar_wait_sleep(smem_u32(&ssfree[s]), (jl / ns) & 1, kPWaitNs)) ok = false;
             }
-            const int nload = nk1 + 2 * nk2;
+            const int nload = nk1 + nhalf * nk2;
             for (int j = 0; j < nload && ok; ++j) {
                 const int s = j % ns;
                 if (!mbar_wait_sleep(smem_u32(&empty[s]), ((j / ns) & 1) ^ 1, kPWaitNs)) {
@@ -172,15 +195,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     // columns of head h and W^QR's P
                     mbar_arrive_expect_tx(smem_u32(&fullB[s]), (uint32_t)(p.a_rows * 128 + N1 * 128));
                     tma_load_2d(smem_u32(smem + s * p.stage), &cqmap, smem_u32(&fullB[s]), j * 64, m0);
-                    for (int c = 0; c < p.Dn / 64; ++c)
-                        tma_load_2d(smem_u32(b + c * 8192), &uqmap, smem_u32(&fullB[s]),
-                                    h * p.Dn + c * 64, j * 64);
-                    for (int c = 0; c < p.P / 64; ++c)
-                        tma_load_2d(smem_u32(b + (p.Dn / 64 + c) * 8192), &qrmap,
-                                    smem_u32(&fullB[s]), h * p.P + c * 64, j * 64);
+                    for (int a = ab; a < ae; ++a) {
+                        if (a < nuq)
+                            tma_load_2d(smem_u32(b + (a - ab) * 8192), &uqmap, smem_u32(&fullB[s]),
+                                        h * p.Dn + a * 64, j * 64);
+                        else
+                            tma_load_2d(smem_u32(b + (a - ab) * 8192), &qrmap, smem_u32(&fullB[s]),
+                                        h * p.P + (a - nuq) * 64, j * 64);
+                    }
                 } else {
                     // W^UK[h] rows 64 kc .. +63, columns 256 half .. +255
-                    const int t = j - nk1, kc = t >> 1, half = t & 1;
+                    const int t = j - nk1;
+                    const int kc = nhalf == 2 ? t >> 1 : t, half = nhalf == 2 ? t & 1 : half0;
                     mbar_arrive_expect_tx(smem_u32(&fullB[s]), 256u * 128u);
                     for (int c = 0; c < 4; ++c)
                         tma_load_3d(smem_u32(b + c * 8192), &ukmap, smem_u32(&fullB[s]),
@@ -213,10 +239,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
             mma_commit(smem_u32(d1done));
             // GEMM 2 once epilogue 1 has read D1 and written q^C
             if (ok && mbar_wait_sleep(smem_u32(a2ready), 0, kPWaitNs)) {
+                fence_proxy_async_smem();  // the partner's q^C columns came by st.async
                 tc_fence_after();
-                for (int t = 0; t < 2 * nk2; ++t) {
+                for (int t = 0; t < nhalf * nk2; ++t) {
                     const int j = nk1 + t, s = j % ns;
-                    const int kc = t >> 1, half = t & 1;
+                    const int kc = nhalf == 2 ? t >> 1 : t, half = nhalf == 2 ? t & 1 : 0;
                     if (!mbar_wait(smem_u32(&fullB[s]), (j / ns) & 1, kPWaitNs)) {
                         ok = false;
                         break;
@@ -343,9 +370,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
         tc_fence_after();
         uint16_t* qrow = p.q_abs + ((long long)(valid ? row : 0) * p.H + h) * (p.R + p.P);
         if (ok) {
-            for (int cb = 0; cb < p.Dn; cb += 32) {
+            const uint32_t peer_bar = p.split ? mapa(smem_u32(a2ready), crank ^ 1u) : 0u;
+            for (int cb = qc0; cb < qc1; cb += 32) {
                 uint32_t v[32];
-                tmem_ld32(tbase + lane_off + cb, v);
+                tmem_ld32(tbase + lane_off + (cb - qc0), v);
                 tmem_wait_ld();
                 const uint32_t chunk = smem_u32(smem + p.a2 + (cb >> 6) * p.a2s) + r * 128;
                 if (!in_box) continue;  // (the TMEM load above is warp-wide)
@@ -355,21 +383,24 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int c = ((cb & 63) >> 3) + u;  // 16-byte piece within the 128-byte row
-                    st_shared_v4(chunk + ((c ^ (r & 7)) << 4), pack2<kF16>(f[8 * u], f[8 * u + 1]),
-                                 pack2<kF16>(f[8 * u + 2], f[8 * u + 3]),
-                                 pack2<kF16>(f[8 * u + 4], f[8 * u + 5]),
-                                 pack2<kF16>(f[8 * u + 6], f[8 * u + 7]));
+                    const uint32_t a = chunk + ((c ^ (r & 7)) << 4);
+                    const uint32_t w0 = pack2<kF16>(f[8 * u], f[8 * u + 1]);
+                    const uint32_t w1 = pack2<kF16>(f[8 * u + 2], f[8 * u + 3]);
+                    const uint32_t w2 = pack2<kF16>(f[8 * u + 4], f[8 * u + 5]);
+                    const uint32_t w3 = pack2<kF16>(f[8 * u + 6], f[8 * u + 7]);
+                    st_shared_v4(a, w0, w1, w2, w3);
+                    if (p.split) st_async_v4(mapa(a, crank ^ 1u), w0, w1, w2, w3, peer_bar);
                 }
             }
-            if (p.P > 0) {
+            if (rope_here) {
                 // NEOX pairs (j, j + P/2), theta_j = pos * theta_scale^j (the ratio
                 // applied j times in f32), products rounded before the sum
                 const int half = p.P / 2;
                 float theta = valid ? (float)p.positions[row] : 0.f;
                 for (int j0 = 0; j0 < half; j0 += 32) {
                     uint32_t a[32], b[32];
-                    tmem_ld32(tbase + lane_off + p.Dn + j0, a);
-                    tmem_ld32(tbase + lane_off + p.Dn + half + j0, b);
+                    tmem_ld32(tbase + lane_off + (p.Dn - qc0) + j0, a);
+                    tmem_ld32(tbase + lane_off + (p.Dn - qc0) + half + j0, b);
                     tmem_wait_ld();
                     const int n = min(32, half - j0);
 #pragma unroll
@@ -396,8 +427,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         ok = __all_sync(0xffffffffu, ok && mbar_wait_sleep(smem_u32(d2done), 0, kPWaitNs));
         tc_fence_after();
         if (ok) {
-            uint4* dst = reinterpret_cast<uint4*>(qrow);
-            for (int cb = 0; cb < p.R; cb += 32) {
+            uint4* dst = reinterpret_cast<uint4*>(qrow) + half0 * 32;  // latent column 256 half0
+            for (int cb = 0; cb < 256 * nhalf; cb += 32) {
                 uint32_t v[32];
                 tmem_ld32(tbase + lane_off + cb, v);
                 tmem_wait_ld();
@@ -415,7 +446,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
     if (!ok && lane == 0 && p.dev_err) atomicOr(p.dev_err, (int32_t)MLA_DEVERR_TIMEOUT);
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();  // neither CTA of a pair leaves while the other may still write into it
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tbase, 512);
 }
@@ -633,6 +664,21 @@ cudaError_t launch_prolog_q(void* q_abs, const void* c_q, const void* gamma_q, c
         p.eps = eps;
         p.theta_scale = theta_scale;
         p.dev_err = dev_err;
+        // a head over a CTA pair while the pairs of all heads and row tiles fit
+        // the SMs in one wave: GEMM 1's blocks halved (rounded up to CTA 0), all
+        // of W^QR's with CTA 1
+        const int tiles = (rows + 127) / 128;
+        {
+            int dev = 0, sms = 0;
+            if (cudaGetDevice(&dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+                sms = 0;
+            const int nuq = Dn / 64, nat = (Dn + P) / 64;
+            int ab1 = (nat + 1) / 2;
+            if (ab1 > nuq) ab1 = nuq;
+            p.split = (nat >= 2 && ab1 >= 1 && (long long)H * tiles * 2 <= sms) ? 1 : 0;
+            p.ab1 = ab1;
+        }
         const int smem = p.gam + q_rank * 2 + 1024;  // + alignment slack
         static std::once_flag once[2];
         static cudaError_t attr_err[2] = {cudaSuccess, cudaSuccess};
@@ -646,11 +692,21 @@ cudaError_t launch_prolog_q(void* q_abs, const void* c_q, const void* gamma_q, c
                                            kPSmemMax + 1024);
         });
         if (attr_err[f16 ? 1 : 0] != cudaSuccess) return attr_err[f16 ? 1 : 0];
-        const dim3 grid((unsigned)H, (unsigned)((rows + 127) / 128), 1);
-        if (f16)
-            tc_prolog_q_kernel<true><<<grid, kPThreads, smem, s>>>(cqm, uq, qr, uk, p);
-        else
-            tc_prolog_q_kernel<false><<<grid, kPThreads, smem, s>>>(cqm, uq, qr, uk, p);
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = p.split ? 2 : 1;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3((unsigned)(H * (p.split ? 2 : 1)), (unsigned)tiles, 1);
+        cfg.blockDim = dim3(kPThreads, 1, 1);
+        cfg.dynamicSmemBytes = (size_t)smem;
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = f16 ? cudaLaunchKernelEx(&cfg, tc_prolog_q_kernel<true>, cqm, uq, qr, uk, p)
+                                  : cudaLaunchKernelEx(&cfg, tc_prolog_q_kernel<false>, cqm, uq, qr, uk, p);
+        if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
     const size_t smem = (size_t)(q_rank + Dn + P + 8) * sizeof(float);
