@@ -76,6 +76,10 @@ def geom(name, dtype=None, t_q=None):
     ("glm52_prefill_chunk", 512, None), # four full row tiles
     ("glm52_decode", 8, "f16"),         # f16 operands
     ("deepseek_decode", 33, "f16"),
+    ("deepseek_decode", 8, None),       # 128 heads: one CTA a head
+    ("glm53_flash_nope", 24, None),     # a head over a CTA pair, no rope part
+    ("glm52_decode", 40, None),         # a head over a CTA pair, 40-row tile
+    ("glm52_decode", 47, None),         # ragged last 8-row group
 ])
 def test_prolog_q_tensor_cores(name, rows, dtype):
     check(W.make_prolog_q(geom(name, dtype), rows))
