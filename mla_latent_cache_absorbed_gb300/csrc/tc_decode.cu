@@ -161,16 +161,18 @@ struct Params {
 };
 
 // ------------------------------------------------------------------ schedule
-// The work split is the one tc_split.cuh defines (even or request-aligned).
-// With G > 1 row groups the G sets read the same cache tiles at about the
-// same time: one HBM read, the rest from L2. One warp per CTA works out the
-// pair's walk; every warp of both CTAs then follows it.
+// The work split is the one tc_split.cuh defines (even or request-aligned
+// within each set, or pooled over the sets). With G > 1 row groups and one
+// set of pairs per row group, the G sets read the same cache tiles at about
+// the same time: one HBM read, the rest from L2. One warp per CTA works out
+// the pair's walk; every warp of both CTAs then follows it.
 static_assert(kTok == split::kTok, "unit size");
 struct Walk {
     int b, g, tile, ntiles, S;
     long long u, u_end;
-    // more row groups than pairs: pair k walks sets k, k + NP, ... one after
-    // the other, U units each; pass_end is where the current set's units end
+    // pooled split: the walk goes on from one set into the next (U units
+    // each); pass_end is where the current set's units end, and a new set
+    // starts again at (b0, S0, nt0), the first request with tiles
     long long pass_end;
     int U, b0, S0, nt0;
 };
@@ -186,6 +188,49 @@ __device__ bool walk_init(const Params& p, int pair, Walk& w) {
     int U = c0.total;
     for (int b0 = 32; b0 < p.B; b0 += 32) U += scan_chunk(p, b0, lane).total;
     if (U == 0) return false;
+    if (split::pooled_split(p, G)) {
+        // this pair's share of the pooled units, from set g's unit ui
+        const int np = split::pooled_pairs(p, G, U);
+        if (pair >= np) return false;
+        const long long T = (long long)G * U;
+        const long long ub = T * pair / np, ue = T * (pair + 1) / np;
+        if (ub >= ue) return false;
+        const int g = (int)(ub / U);
+        const int ui = (int)(ub - (long long)g * U);
+        int base = 0, fb = -1, first = 0, S = 0, b0r = -1, S0 = 0;
+        for (int b0 = 0; b0 < p.B; b0 += 32) {
+            const ChunkScan c = b0 == 0 ? c0 : scan_chunk(p, b0, lane);
+            const int excl = base + c.incl - c.v, incl = base + c.incl;
+            const unsigned hit = __ballot_sync(0xffffffffu, incl > ui && c.v > 0);
+            if (fb < 0 && hit) {
+                const int l = __ffs(hit) - 1;
+                fb = b0 + l;
+                first = __shfl_sync(0xffffffffu, excl, l);
+                S = __shfl_sync(0xffffffffu, c.S, l);
+            }
+            const unsigned any = __ballot_sync(0xffffffffu, c.v > 0);
+            if (b0r < 0 && any) {
+                const int l = __ffs(any) - 1;
+                b0r = b0 + l;
+                S0 = __shfl_sync(0xffffffffu, c.S, l);
+            }
+            base += c.total;
+        }
+        if (fb < 0 || b0r < 0) return false;
+        w.b = fb;
+        w.g = g;
+        w.S = S;
+        w.ntiles = ntiles_of(S, p.T, p.max_blocks);
+        w.tile = ui - first;
+        w.u = ub;
+        w.u_end = ue;
+        w.pass_end = (long long)(g + 1) * U;
+        w.U = U;
+        w.b0 = b0r;
+        w.S0 = S0;
+        w.nt0 = ntiles_of(S0, p.T, p.max_blocks);
+        return true;
+    }
     const int np_g = pairs_per_set(p, G, U);
     const int g = pair / np_g, k = pair % np_g;
     if (g >= G) return false;
@@ -247,18 +292,11 @@ __device__ bool walk_init(const Params& p, int pair, Walk& w) {
     w.tile = ub - first;
     w.u = ub;
     w.u_end = ue;
-    w.pass_end = ue;
+    w.pass_end = ue;  // (one set: no next one)
     w.U = U;
     w.b0 = fb;
     w.S0 = S;
     w.nt0 = w.ntiles;
-    if (G > p.NP) {
-        // one pair per set (np_g = 1: the pair's range is the whole set, from
-        // the first request with tiles), and this pair also takes sets
-        // pair + NP, pair + 2 NP, ...
-        const int npass = (G - 1 - pair) / p.NP + 1;
-        w.u_end = (long long)npass * U;
-    }
     return true;
 }
 
@@ -267,9 +305,9 @@ __device__ __forceinline__ void walk_next(const Params& p, Walk& w) {
     ++w.u;
     if (w.u >= w.u_end) return;
     if (w.u == w.pass_end) {
-        // the pair's next row group: the same requests and tiles again
+        // the next row group (pooled split): the same requests and tiles again
         w.pass_end += w.U;
-        w.g += p.NP;
+        w.g += 1;
         w.b = w.b0;
         w.S = w.S0;
         w.ntiles = w.nt0;

@@ -537,8 +537,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
                                     atomicOr(p.dev_err, (int32_t)MLA_DEVERR_SEQ_TOO_LONG);
                             }
                         } else {
-                            const split::Parts q = split::parts_from(base + c.incl - c.v, c.v, sh.U,
-                                                                     sh.np_g, sh.aligned, qi >> 7);
+                            const split::Parts q = split::parts_of(sh, base + c.incl - c.v, c.v, qi >> 7);
                             sh_np[r] = q.nparts;
                             sh_pf[r] = q.pf;
                             sh_s0[r] = q.slot0_off;
@@ -568,7 +567,11 @@ __global__ void __launch_bounds__(kMThreads, 1)
                 sh_off[mrows + 2] = others;
                 // a long decode (pairs past 32 tiles) wrote its first partial rows
                 // long before it ends: they are prefetched back into L2 below
-                sh_off[mrows + 3] = sh.U > split::kAlignedMaxShare * sh.np_g ? 1 : 0;
+                sh_off[mrows + 3] = (sh.pooled ? (long long)sh.G * sh.U >
+                                                     (long long)split::kAlignedMaxShare * sh.np_all
+                                               : sh.U > split::kAlignedMaxShare * sh.np_g)
+                                        ? 1
+                                        : 0;
             }
         }
         named_sync(1, kMT);

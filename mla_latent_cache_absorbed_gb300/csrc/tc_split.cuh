@@ -42,10 +42,26 @@ __device__ __forceinline__ int ntiles_of(int S, int T, int max_blocks) {
 }
 
 // pairs per set (np_g) and the set size cap
+// Pooled split: when the G sets would share the pairs unevenly (G does not
+// divide the pairs, or exceeds them), the sets' units are numbered one after
+// the other (set g's unit i is g U + i) and pair k takes the even share
+// [G U k / np, G U (k + 1) / np) of all of them, walking on into the next set.
+// A set ends with a request's last tile, so a pair still holds at most two
+// partial segments: its first and its last.
+template <class P>
+__device__ __forceinline__ bool pooled_split(const P& p, int G) {
+    return G > 1 && (G > p.NP || p.NP % G != 0);
+}
+template <class P>
+__device__ __forceinline__ int pooled_pairs(const P& p, int G, long long U) {
+    const long long cap = ((long long)G * U + p.min_units - 1) / p.min_units;
+    return (int)(cap < p.NP ? cap : p.NP);
+}
+
 template <class P>
 __device__ __forceinline__ int pairs_per_set(const P& p, int G, long long U) {
     int np_g = p.NP / G;
-    if (np_g < 1) np_g = 1;  // more row groups than pairs: one pair per set, pairs walk several sets
+    if (np_g < 1) np_g = 1;
     const long long cap = (U + p.min_units - 1) / p.min_units;
     if (cap < np_g) np_g = (int)(cap > 0 ? cap : 1);
     return np_g;
@@ -140,11 +156,34 @@ __device__ __forceinline__ Parts parts_from(int before, int nt, int U, int np_g,
     return q;
 }
 
+// The parts of a request under the pooled split: its units are g U + before
+// .. + nt - 1 of the G U pooled units, shared by np pairs as evenly as the
+// even split shares a set's.
+__device__ __forceinline__ Parts parts_pooled(int before, int nt, int U, int G, int np, int g) {
+    Parts q;
+    q.nt = nt;
+    const long long T = (long long)G * U;
+    const long long u0 = (long long)g * U + before, u1 = u0 + nt;
+    auto owner = [&](long long u) {
+        long long pp = (u * np) / T;
+        while (pp + 1 < np && T * (pp + 1) / np <= u) ++pp;
+        while (pp > 0 && T * pp / np > u) --pp;
+        return (int)pp;
+    };
+    const int kf = owner(u0), kl = owner(u1 - 1);
+    q.pf = kf;
+    q.nparts = kl - kf + 1;
+    q.slot0_off = (T * kf / np) >= u0 ? 0 : 1;
+    return q;
+}
+
 // Warp-cooperative: the set's unit total U, its pairs np_g and whether the
 // aligned split is in use (every lane gets the same answer).
 struct SplitShape {
     int U, np_g;
     bool aligned;
+    bool pooled;   // pooled split over np_all pairs
+    int G, np_all;
 };
 template <class P>
 __device__ SplitShape split_shape(const P& p, int lane) {
@@ -154,6 +193,10 @@ __device__ SplitShape split_shape(const P& p, int lane) {
     for (int b0 = 0; b0 < p.B; b0 += 32) sh.U += scan_chunk(p, b0, lane).total;
     sh.np_g = sh.U > 0 ? pairs_per_set(p, G, sh.U) : 1;
     sh.aligned = false;
+    sh.G = G;
+    sh.pooled = pooled_split(p, G);
+    sh.np_all = sh.U > 0 ? pooled_pairs(p, G, sh.U) : 1;
+    if (sh.pooled) return sh;
     if (sh.U > 0 && aligned_tried(sh.U, sh.np_g)) {
         int base = 0, worst = 0, bad = 0;
         for (int b0 = 0; b0 < p.B; b0 += 32) {
@@ -168,6 +211,12 @@ __device__ SplitShape split_shape(const P& p, int lane) {
 
 // Warp-cooperative: the parts of request b's row group g (every lane gets
 // the same answer). nparts is 0 for an empty or invalid request.
+// the parts of a request of row group g under the split in use
+__device__ __forceinline__ Parts parts_of(const SplitShape& sh, int before, int nt, int g) {
+    return sh.pooled ? parts_pooled(before, nt, sh.U, sh.G, sh.np_all, g)
+                     : parts_from(before, nt, sh.U, sh.np_g, sh.aligned, g);
+}
+
 template <class P>
 __device__ Parts request_parts(const P& p, int b, int g, int lane) {
     Parts q;
@@ -187,7 +236,7 @@ __device__ Parts request_parts(const P& p, int b, int g, int lane) {
     }
     if (q.nt == 0) return q;
     const SplitShape sh = split_shape(p, lane);
-    return parts_from(before, q.nt, sh.U, sh.np_g, sh.aligned, g);
+    return parts_of(sh, before, q.nt, g);
 }
 
 // The merge weights of one row, by a group of 8 adjacent lanes: w holds the
