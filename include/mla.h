@@ -190,8 +190,8 @@ mla_status mla_decode_workspace_size(int32_t batch, int32_t max_blocks,
  *             device data is invalid (the row is then zero / -inf); the
  *             library never clears it
  * Supported: R+P in {576, 512} with R == 512 for bf16 and f16 (the tensor-core
- * path, for query blocks t_q * H of any size: past 128 x (SMs / 2) rows per
- * request each pair of CTAs works through several 128-row groups in turn);
+ * path, for query blocks t_q * H of any size: the 128-row groups' tiles are
+ * shared out over the grid's CTA pairs);
  * any R <= 1024, R+P <= 1152 for f32 (the SIMT kernels).
  * batch * t_q * H must stay below 2^31 and max_blocks below 2^27
  * (MLA_ERR_UNSUPPORTED otherwise, also from mla_decode_workspace_size).
