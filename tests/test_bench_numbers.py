@@ -115,3 +115,43 @@ def test_default_run_covers_every_workload_with_the_largest_as_headline():
         g = W.geometry(name)
         sizes[name] = int(lens.sum()) * g.width * (2 if g.dtype == "bf16" else 4)
     assert bench.HEADLINE == max(sizes, key=sizes.get)
+
+
+def _kernel_tree(tmp_path, extra=""):
+    """A copy of the pair decode kernel's sources under tmp_path (as bench.py
+    finds them below its root), with `extra` appended to tc_decode.cu."""
+    import os
+    import shutil
+    src = os.path.join(bench.ROOT, "mla_latent_cache_absorbed_gb300", "csrc")
+    dst = tmp_path / "mla_latent_cache_absorbed_gb300" / "csrc"
+    dst.mkdir(parents=True)
+    for name in ("tc_decode.cu", "tc_split.cuh", "sm100.cuh"):
+        shutil.copy(os.path.join(src, name), dst / name)
+    with open(dst / "tc_decode.cu", "a") as f:
+        f.write(extra)
+    (tmp_path / "profiles").mkdir()
+    return tmp_path
+
+
+def test_fingerprint_ignores_comments_not_code(tmp_path, monkeypatch):
+    """The decode kernel's fingerprint keys the committed ncu traffic: a
+    comment or blank-line edit keeps it, a code edit changes it."""
+    base = bench.kernel_fingerprint()
+    monkeypatch.setattr(bench, "ROOT", str(_kernel_tree(tmp_path / "a", "\n// a comment\n\n")))
+    assert bench.kernel_fingerprint() == base
+    monkeypatch.setattr(bench, "ROOT", str(_kernel_tree(tmp_path / "b", "\nstatic int k_x;\n")))
+    assert bench.kernel_fingerprint() != base
+
+
+def test_profiled_traffic_only_for_the_captured_kernel(tmp_path, monkeypatch):
+    """traffic is the summary's DRAM bytes while its recorded fingerprint is
+    the kernel's own, and null once the kernel has changed."""
+    root = _kernel_tree(tmp_path)
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    fp = bench.kernel_fingerprint()
+    prof = root / "profiles" / "decode_pair_some_workload.md"
+    prof.write_text(f"traffic_bytes_per_launch: 123456\nkernel_fingerprint: {fp[:12]}\n")
+    assert bench.profiled_traffic("some_workload") == 123456
+    prof.write_text("traffic_bytes_per_launch: 123456\nkernel_fingerprint: 000000000000\n")
+    assert bench.profiled_traffic("some_workload") is None
+    assert bench.profiled_traffic("no_such_workload") is None
