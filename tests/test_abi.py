@@ -196,3 +196,30 @@ def test_cache_append_rmsnorm_rope_validation(lib):
     f(0, 0, 0, 0, 0, 0, 0, 2, N.MLA_F32, ok["eps"], ok["rope_base"], d, None, 0)  # no tokens: no-op
     nope = N.MlaDims(4, 16, 0, 16, 32, 1, 16, N.MLA_BF16)
     f(0, 0, 0, 0, 0, 0, 0, 2, N.MLA_F32, ok["eps"], 0.0, nope, None, 0)  # rope_base unused without rope
+
+
+def test_prolog_q_validation(lib):
+    """Argument checks of the query prolog, all before any launch: the query
+    rank, eps, the rope base and d_rope's parity, NULL and misaligned buffers;
+    zero rows is a no-op."""
+    d = N.MlaDims(4, 16, 8, 16, 32, 1, 16, N.MLA_BF16)
+    f = N.mla_prolog_q
+    ok = dict(q_abs=256, c_q=512, gamma_q=768, w_uq=1024, w_qr=1280, w_uk=1536, positions=1792)
+
+    def call(rows=2, q_rank=64, eps=1e-6, rope_base=10000.0, dims=d, **kw):
+        a = dict(ok, **kw)
+        f(a["q_abs"], a["c_q"], a["gamma_q"], a["w_uq"], a["w_qr"], a["w_uk"], a["positions"],
+          rows, q_rank, eps, rope_base, dims, None, 0)
+
+    for bad in (dict(q_rank=0), dict(q_rank=12), dict(q_rank=16392), dict(rows=-1),
+                dict(eps=-1.0), dict(eps=float("nan")), dict(rope_base=0.0),
+                dict(rope_base=float("inf")), dict(q_abs=0), dict(w_uk=0), dict(positions=0),
+                dict(w_qr=0), dict(c_q=520), dict(positions=1796)):
+        with pytest.raises(N.MlaError) as e:
+            call(**bad)
+        assert e.value.status == 1, bad
+    with pytest.raises(N.MlaError):
+        call(dims=N.MlaDims(4, 16, 7, 16, 32, 1, 16, N.MLA_BF16))  # odd d_rope
+    nope = N.MlaDims(4, 16, 0, 16, 32, 1, 16, N.MLA_BF16)
+    call(rows=0, dims=nope, w_qr=0, positions=0)      # no rows, no rope: nothing to do
+    call(rows=0)                                      # no rows: a no-op before the pointers
