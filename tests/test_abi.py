@@ -223,3 +223,40 @@ def test_prolog_q_validation(lib):
     nope = N.MlaDims(4, 16, 0, 16, 32, 1, 16, N.MLA_BF16)
     call(rows=0, dims=nope, w_qr=0, positions=0)      # no rows, no rope: nothing to do
     call(rows=0)                                      # no rows: a no-op before the pointers
+
+
+def test_static_decode_refuses_oversize_batch(lib):
+    """mla_decode_paged_static compares the batch's scratch need with its
+    fixed device array before touching the device: too large a batch is an
+    argument error naming both sizes; an empty batch is a no-op."""
+    d = N.MlaDims(4, 16, 8, 16, 32, 1, 16, N.MLA_F32)
+    limit = 64 << 20  # MLA_STATIC_SCRATCH_BYTES
+    batch = 4096
+    while N.mla_decode_workspace_size(batch, 4096, d) <= limit:
+        batch *= 2
+    with pytest.raises(N.MlaError) as e:
+        N.mla_decode_paged_static(256, 0, 256, 256, 256, 256, batch, 4096, 8, d, 0.2, None, 0)
+    assert e.value.status == 1 and "static scratch" in N.mla_last_error()
+    N.mla_decode_paged_static(0, 0, 0, 0, 0, 0, 0, 4, 8, d, 0.2, None, 0)
+
+
+def test_attend_validation(lib):
+    """Argument checks of the fused step, before any launch."""
+    d = N.MlaDims(4, 16, 8, 16, 32, 1, 16, N.MLA_F32)
+    n = N.mla_attend_workspace_size(2, 4, d)
+    args = dict(out=256, lse=0, q_nope=512, q_pe=768, w_uk=1024, w_uv=1280, kv_cache=1536,
+                block_table=1792, seq_lens=2048, workspace=4096)
+
+    def call(batch=2, scale=0.2, nbytes=n, **kw):
+        a = dict(args, **kw)
+        N.mla_attend_absorbed(a["out"], a["lse"], a["q_nope"], a["q_pe"], a["w_uk"], a["w_uv"],
+                              a["kv_cache"], a["block_table"], a["seq_lens"], batch, 4, 8, d,
+                              scale, a["workspace"], nbytes, None, 0)
+
+    for bad in (dict(batch=-1), dict(out=0), dict(q_pe=0), dict(workspace=0),
+                dict(q_nope=520), dict(workspace=4112), dict(scale=float("nan")),
+                dict(nbytes=n - 1)):
+        with pytest.raises(N.MlaError) as e:
+            call(**bad)
+        assert e.value.status == 1, bad
+    call(batch=0)  # empty batch: nothing to do
