@@ -22,8 +22,8 @@
 //     GB/s) overlaps the next tile's softmax instead of stalling it.
 //   CTA 1 ("O-CTA") holds O [128 x 512] f32 in all 512 TMEM columns and
 //     computes O += P V (M=128, N=2x256, K=64) with V the leading 512 columns
-//     of the same tile, which it loads itself (L2 hits: its prefetcher warp
-//     pulls the tiles ahead of both CTAs).
+//     of the same tile, which it loads itself (mostly L2 hits: the S-CTA
+//     loaded the tile shortly before).
 // The O accumulator alone fills a TMEM, so splitting the roles keeps both the
 // QK^T and the P*V contractions at M=128 with no repeated work; the only
 // exchange is P (16 KB per 64-token tile) plus per-row rescale factors.
@@ -93,7 +93,6 @@ constexpr int kSenders = 4;                   // S-CTA P senders: one per TMEM l
 constexpr uint64_t kWaitLimit = 2000000000ull;  // ns before a wait gives up (default)
 constexpr uint32_t kSuspendHintNs = 1000;     // longest suspension of one wait poll
 constexpr float kRescaleThreshold = 8.0f;     // lazy rescale, log2 units
-constexpr int kPrefetchAhead = 6;             // tiles the L2 prefetcher runs ahead of V landing
 
 // per-tile rescale message from the S-CTA's softmax to the O-CTA (st.async)
 struct __align__(16) AlphaMsg {
@@ -129,7 +128,6 @@ struct Ctrl {
     int32_t evt_slot;
     int32_t bad;            // O: the segment met an invalid block id
     int32_t badw[kSmxWarps];  // S: per softmax warp, the segment met an invalid block id
-    int32_t landed;         // O: tiles whose V has landed (paces the L2 prefetcher)
     float mstat[128];       // O: segment max (log2 units) per row
     float lstat[128];       // O: segment sum per row
     long long walk_u, walk_ue, walk_pe;  // both: the pair's unit range (see walk_init)
@@ -401,7 +399,9 @@ __device__ __forceinline__ int valid_blocks(const Walk& w) {
 //   O-CTA  warp 0     V loader: one 4-D box per cache block
 //          warp 1     V landing: zeroes the rows of a partial last block past
 //                     the request, releases the stage
-//          warp 2     L2 prefetcher of upcoming cache blocks
+//          warp 2     idle after working out the walk (an L2 prefetcher of the
+//                     coming cache blocks here cost 6% of the causal t_q = 4
+//                     decode: its requests competed with the loads)
 //          warp 4     O += P V MMA issuer; owns the TMEM allocation
 //          warps 5-12 rescale and epilogue: warp w takes the TMEM lanes of
 //                     its quadrant (w % 4) and half the 512 columns
@@ -456,7 +456,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(&c.rowbar), 256);
         mbar_init(smem_u32(&c.never), 1);
         c.abort = 0;
-        c.landed = 0;
         fence_mbar_init();
     }
     if (warp == 4) {
@@ -928,10 +927,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     fence_proxy_async_smem();
                 }
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(smem_u32(&c.vready[s]));
-                    *(volatile int32_t*)&c.landed = (int32_t)(i + 1);
-                }
+                if (lane == 0) mbar_arrive(smem_u32(&c.vready[s]));
             }
         } else if (warp == 3) {
             // ---------------- relay: once the P*V that read P slot i % kNP has
@@ -944,28 +940,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const int slot = (int)(i % kNP);
                     if (!wt.wait(smem_u32(&c.pdone[slot]), (uint32_t)((i / kNP) & 1))) break;
                     mbar_arrive_remote(pempty_remote + slot * 8);
-                }
-            }
-        } else if (warp == 2) {
-            // ---------------- L2 prefetcher: pulls the cache blocks of the tiles
-            // kPrefetchAhead past the V landing point into L2 (plain prefetches,
-            // so the TMA queues of both CTAs only carry the real loads)
-            long long i = 0;
-            const uint64_t t_start = globaltimer_ns();
-            for (; w.u < w.u_end; walk_next(p, w), ++i) {
-                while (i > *(volatile int32_t*)&c.landed + kPrefetchAhead) {
-                    if (c.abort || globaltimer_ns() - t_start > 4 * p.wait_ns) break;
-                    __nanosleep(200);
-                }
-                if (c.abort) break;
-                const int nb = valid_blocks(w);
-                const int32_t* bt = p.block_table + (long long)w.b * p.max_blocks + w.tile * 4;
-                constexpr int kLines = 16 * W * 2 / 128;  // 128-byte lines in one block
-                for (int k = 0; k < nb; ++k) {
-                    const int32_t blk = bt[k];
-                    if (blk < 0 || blk >= p.num_blocks) continue;
-                    const char* base = reinterpret_cast<const char*>(p.kv + (long long)blk * 16 * W);
-                    for (int ln = lane; ln < kLines; ln += 32) prefetch_l2_line(base + ln * 128);
                 }
             }
         } else if (warp == 4) {
