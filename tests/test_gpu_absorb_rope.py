@@ -2,7 +2,7 @@
 
 Tolerances, per part of each q_abs row:
   latent part   as the absorb's (test_gpu_parity.py): f32 max abs diff 1e-4;
-                bf16 1e-2 + 2^-8 |ref|;
+                bf16 1e-2 plus half a bf16 ulp of |ref|;
   rope part     both sides turn the pair (a, b) by the same f32 theta (the same
                 recurrence from the same f32 ratio), so they differ by their
                 sin / cos (a few f32 ulps) and the products' rounding:

@@ -8,7 +8,8 @@ the oracle's: the softmax weights P enter the P*V tensor-core product as a
 first is part of what the stated 1e-2 bounds. The second alone exceeds 1e-2
 once |ref| >= 4, so it cannot be inside the stated bound everywhere: the gate
 is the stated 1e-2 plus one rounding of the output, half a bf16 ulp of |ref|
-(at most 2^-9 |ref|, against the 2^-8 |ref| an earlier form allowed).
+(between 2^-9 |ref| and 2^-8 |ref| depending on where |ref| sits in its
+binade, against the flat 2^-8 |ref| an earlier form allowed).
 
 f16 is not among the stated gates. Its gate is the bf16 one scaled by f16's
 finer quantum (3 more mantissa bits, so its roundings of P and of the output
