@@ -13,7 +13,8 @@
 // or K (P*V) dimension. A unit of work is (request, row group, 64-token
 // tile). A persistent grid of CTA pairs splits the unit sequence as
 // tc_split.cuh describes (evenly, or aligned to requests when pairs get few
-// tiles). In each pair:
+// tiles, or pooled over the row groups when they do not divide the pairs).
+// In each pair:
 //   CTA 0 ("S-CTA") holds the 128 query rows in TMEM (A operand) and computes
 //     S = Q K^T for each tile (M=128, N=64, K=576 or 512) into TMEM, runs the
 //     online softmax (two threads per query row, lazy rescaling) and stages
