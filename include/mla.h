@@ -193,7 +193,8 @@ mla_status mla_decode_workspace_size(int32_t batch, int32_t max_blocks,
  * path, for query blocks t_q * H of any size: the 128-row groups' tiles are
  * shared out over the grid's CTA pairs);
  * any R <= 1024, R+P <= 1152 for f32 (the SIMT kernels).
- * batch * t_q * H must stay below 2^31 and max_blocks below 2^27
+ * batch * t_q * H must stay below 2^31, max_blocks below 2^27 and the cache
+ * tiles batch * ceil(max_blocks / 4) (64 tokens each) below 2^31
  * (MLA_ERR_UNSUPPORTED otherwise, also from mla_decode_workspace_size).
  */
 mla_status mla_decode_paged(void* out, float* lse, const void* q_abs,

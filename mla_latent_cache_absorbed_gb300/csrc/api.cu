@@ -277,8 +277,10 @@ mla_status mla_decompress_out(void* out, const void* o_lat, const void* w_uv, in
 }
 
 namespace {
-// Index limits of the decode kernels: query rows (batch * t_q * n_head) and
-// cache positions (max_blocks * 16) are 32-bit counts.
+// Index limits of the decode kernels: query rows (batch * t_q * n_head),
+// cache positions (max_blocks * 16) and the work split's units (64-token
+// tiles, at most ceil(max_blocks / 4) a request, summed over the batch) are
+// 32-bit counts.
 mla_status check_decode_shape(int32_t batch, int32_t max_blocks, const mla_dims& d) {
     if ((long long)batch * d.t_q * d.n_head > INT32_MAX || max_blocks >= (1 << 27)) {
         set_error("decode: batch * t_q * n_head = %lld query rows (at most 2^31 - 1) and "
@@ -286,14 +288,20 @@ mla_status check_decode_shape(int32_t batch, int32_t max_blocks, const mla_dims&
                   (long long)batch * d.t_q * d.n_head, max_blocks);
         return MLA_ERR_UNSUPPORTED;
     }
+    const long long tiles = (long long)batch * ((max_blocks + 3) / 4);
+    if (tiles > INT32_MAX) {
+        set_error("decode: batch * ceil(max_blocks / 4) = %lld cache tiles of 64 tokens "
+                  "(at most 2^31 - 1) are supported", tiles);
+        return MLA_ERR_UNSUPPORTED;
+    }
     return MLA_OK;
 }
 
 // The 16-bit types take the tensor-core decode. It gives each row group of a
 // request (128 of its t_q * n_head query rows) a set of CTA pairs of its own;
-// with more row groups than the grid has pairs (more than 9728 query rows per
-// request on 152 SMs, a long prefill chunk), each row group gets one pair and
-// a pair walks several row groups in turn.
+// when the row groups do not divide the grid's pairs, or outnumber them (a
+// long prefill chunk), all row groups' tiles are pooled and shared out
+// evenly, a pair walking on from one row group into the next.
 bool use_tc_decode(const mla_dims& d) {
     if (d.dtype == MLA_F32 || !tc_decode_supported(d)) return false;
     size_t bytes = 0;

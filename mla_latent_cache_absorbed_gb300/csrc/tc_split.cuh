@@ -70,7 +70,7 @@ __device__ __forceinline__ int pairs_per_set(const P& p, int G, long long U) {
 // One chunk of 32 requests, warp-cooperative: lane l holds request b0 + l's
 // units v (0 past the batch), its seq_len S, and the inclusive prefix of v
 // within the chunk; total is the chunk's sum. Unit counts fit 32 bits (the
-// host requires batch * max_blocks <= 2^33).
+// host requires batch * ceil(max_blocks / 4) < 2^31).
 struct ChunkScan {
     int v, S, incl, total;
 };

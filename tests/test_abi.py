@@ -146,6 +146,17 @@ def test_decode_workspace_and_validation(lib):
         N.mla_decode_workspace_size(2, 1 << 27, d)
     assert e.value.status == 2
     assert N.mla_decode_workspace_size(2, (1 << 27) - 1, d) > 0
+    # the work split's 64-token tiles, batch * ceil(max_blocks / 4), are a
+    # 32-bit count: 2^24 requests of 509 blocks (ceil(509 / 4) = 2^7 tiles
+    # each) make 2^31 tiles, one too many, although batch * max_blocks is
+    # below 2^33
+    one_head = N.MlaDims(1, 16, 8, 16, 32, 1, 16, N.MLA_F32)
+    with pytest.raises(N.MlaError) as e:
+        N.mla_decode_workspace_size(1 << 24, 509, one_head)
+    assert e.value.status == 2 and "cache tiles" in N.mla_last_error()
+    with pytest.raises(N.MlaError):
+        N.mla_attend_workspace_size(1 << 24, 512, one_head)
+    assert N.mla_decode_workspace_size((1 << 24) - 1, 512, one_head) > 0
 
 
 def test_f16_dims(lib):
